@@ -1,0 +1,199 @@
+"""Plain CPU oracle for the DiT elementwise hot path -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never links, loads or
+calls it, and it shares no code with it: the C source here (dit_oracle.c) has
+its own header, its own codecs and its own build step.
+
+Operations (see dit_oracle.h for the passages each one follows):
+
+* :func:`residual_gate_add` -- ``out = hidden + update * gate`` (sglang PR
+  #29361, section Motivation), full ``[B, L, D]`` or ``[B, 1, D]`` gate.
+* :func:`rmsnorm_modulate` -- ``rms_norm(x, eps) * (1 + scale) + shift``
+  (prhub summary of sglang PR #34172, section "key source snippet"), with a
+  weightless RMSNorm per row over D.
+* :func:`gate_add_rmsnorm_modulate` -- both, the RMS taken over the stored
+  (rounded) residual.
+
+Arrays are numpy arrays or CPU torch tensors, contiguous, holding the raw
+storage of the dtype: 16-bit words for bf16 and fp16, ``float32`` for fp32.
+Outputs are written in place.
+
+Every function is pinned in ``tests/test_oracle_*.py`` against values fixed by
+the mathematics (closed forms, invariants, exact rational brute force on tiny
+inputs) and by library routines (torch and numpy dtype conversions, torch's
+``rms_norm`` in float64).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dit_oracle.c")
+_HDR = os.path.join(_HERE, "dit_oracle.h")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
+LAYOUTS = {"full": 0, "bcast": 1}
+ELEM_SIZE = {"bf16": 2, "fp16": 2, "fp32": 4}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` from ``dit_oracle.c`` with gcc (no fast-math,
+    no FMA contraction).  Returns the library path."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                   os.path.getmtime(_HDR))):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC,
+           "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, vp, fp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+            ci = ctypes.c_int
+            lib.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_to_f32.restype = fp
+            lib.orc_f32_to_bf16.argtypes = [fp]
+            lib.orc_f32_to_bf16.restype = ctypes.c_uint16
+            lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.orc_f16_to_f32.restype = fp
+            lib.orc_f32_to_f16.argtypes = [fp]
+            lib.orc_f32_to_f16.restype = ctypes.c_uint16
+            lib.orc_decode_array.argtypes = [vp, vp, i64, ci]
+            lib.orc_decode_array.restype = None
+            lib.orc_encode_array.argtypes = [vp, vp, i64, ci]
+            lib.orc_encode_array.restype = None
+            lib.orc_rmsnorm_modulate.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64,
+                                                 fp, ci, ci, vp, i64]
+            lib.orc_rmsnorm_modulate.restype = ci
+            lib.orc_gate_add_rmsnorm_modulate.argtypes = [
+                vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
+            lib.orc_gate_add_rmsnorm_modulate.restype = ci
+            lib.orc_row_rms_inverse.argtypes = [vp, i64, fp, ci]
+            lib.orc_row_rms_inverse.restype = fp
+            lib.orc_residual_gate_add_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
+                                                     i64, ci, ci, vp, i64]
+            lib.orc_residual_gate_add_mt.restype = ci
+            lib.orc_rmsnorm_modulate_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
+                                                    i64, fp, ci, ci, vp, i64]
+            lib.orc_rmsnorm_modulate_mt.restype = ci
+            lib.orc_gate_add_rmsnorm_modulate_mt.argtypes = [
+                ci, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
+            lib.orc_gate_add_rmsnorm_modulate_mt.restype = ci
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    """Address of a contiguous numpy array or CPU torch tensor (None -> NULL)."""
+    if a is None:
+        return None
+    if hasattr(a, "data_ptr"):  # torch tensor
+        if a.device.type != "cpu" or not a.is_contiguous():
+            raise ValueError("oracle inputs must be contiguous CPU tensors")
+        return a.data_ptr() or None
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("oracle inputs must be C-contiguous arrays")
+    return a.ctypes.data or None
+
+
+def _rows(rows):
+    """(pointer, count, keep-alive) for an optional row selection."""
+    if rows is None:
+        return None, 0, None
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return (arr.ctypes.data if arr.size else None), int(arr.size), arr
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: bad argument")
+
+
+def decode(src, dtype):
+    """fp32 values of an array of dtype storage (numpy float32 result)."""
+    import numpy as np
+    n = int(src.numel() if hasattr(src, "numel") else src.size)
+    dst = np.empty(n, dtype=np.float32)
+    _load().orc_decode_array(_ptr(dst), _ptr(src), n, DTYPES[dtype])
+    return dst
+
+
+def encode(src_f32, dtype):
+    """Storage words of fp32 values rounded once to dtype (numpy uint16 for
+    bf16/fp16, float32 for fp32)."""
+    import numpy as np
+    src = np.ascontiguousarray(np.asarray(src_f32, dtype=np.float32)).ravel()
+    dst = np.empty(src.size, dtype=np.float32 if dtype == "fp32" else np.uint16)
+    _load().orc_encode_array(_ptr(dst), _ptr(src), src.size, DTYPES[dtype])
+    return dst
+
+
+def residual_gate_add(out, hidden, update, gate, B, L, D, dtype="bf16",
+                      gate_layout="full", rows=None, threads=1):
+    rp, n, keep = _rows(rows)
+    rc = _load().orc_residual_gate_add_mt(int(threads), _ptr(out), _ptr(hidden),
+                                          _ptr(update), _ptr(gate), B, L, D,
+                                          DTYPES[dtype], LAYOUTS[gate_layout], rp, n)
+    del keep
+    _check(rc, "residual_gate_add")
+
+
+def rmsnorm_modulate(out, x, scale, shift, B, L, D, eps=1e-6, dtype="bf16",
+                     mod_layout="bcast", rows=None, t_out=None, threads=1):
+    rp, n, keep = _rows(rows)
+    lib = _load()
+    if t_out is not None:
+        rc = lib.orc_rmsnorm_modulate(_ptr(out), _ptr(t_out), _ptr(x), _ptr(scale),
+                                      _ptr(shift), B, L, D, float(eps),
+                                      DTYPES[dtype], LAYOUTS[mod_layout], rp, n)
+    else:
+        rc = lib.orc_rmsnorm_modulate_mt(int(threads), _ptr(out), _ptr(x),
+                                         _ptr(scale), _ptr(shift), B, L, D,
+                                         float(eps), DTYPES[dtype],
+                                         LAYOUTS[mod_layout], rp, n)
+    del keep
+    _check(rc, "rmsnorm_modulate")
+
+
+def gate_add_rmsnorm_modulate(residual_out, modulated_out, hidden, update, gate,
+                              scale, shift, B, L, D, eps=1e-6, dtype="bf16",
+                              gate_layout="bcast", mod_layout="bcast", rows=None,
+                              t_out=None, threads=1):
+    rp, n, keep = _rows(rows)
+    lib = _load()
+    if t_out is not None:
+        rc = lib.orc_gate_add_rmsnorm_modulate(
+            _ptr(residual_out), _ptr(modulated_out), _ptr(t_out), _ptr(hidden),
+            _ptr(update), _ptr(gate), _ptr(scale), _ptr(shift), B, L, D,
+            float(eps), DTYPES[dtype], LAYOUTS[gate_layout], LAYOUTS[mod_layout],
+            rp, n)
+    else:
+        rc = lib.orc_gate_add_rmsnorm_modulate_mt(
+            int(threads), _ptr(residual_out), _ptr(modulated_out), _ptr(hidden),
+            _ptr(update), _ptr(gate), _ptr(scale), _ptr(shift), B, L, D,
+            float(eps), DTYPES[dtype], LAYOUTS[gate_layout], LAYOUTS[mod_layout],
+            rp, n)
+    del keep
+    _check(rc, "gate_add_rmsnorm_modulate")
+
+
+def row_rms_inverse(x_row, D, eps=1e-6, dtype="bf16") -> float:
+    return _load().orc_row_rms_inverse(_ptr(x_row), D, float(eps), DTYPES[dtype])

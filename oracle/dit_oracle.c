@@ -1,0 +1,418 @@
+/*
+ * dit_oracle.c -- plain CPU oracle for the DiT elementwise hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY (see dit_oracle.h).  Build with
+ *     gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared
+ * and never with -ffast-math: every `float` operation below must be one IEEE
+ * fp32 operation rounded to nearest-even, and `a * b + c` must stay two
+ * roundings.  (GCC contracts to FMA by default in GNU C mode, hence the flag.)
+ *
+ * Readings taken where the pages leave a step open (each is listed with its
+ * justification in the repository's design notes):
+ *   R1  residual gate: p = fl(update * gate), s = fl(hidden + p), then one
+ *       rounding of s to the storage dtype.  No FMA.
+ *   R2  RMS statistic: sum of x^2 accumulated in double in index order,
+ *       ms = (float)(sum / D), v = fl(ms + eps), r = (float)(1 / sqrt(v))
+ *       evaluated in double -- i.e. the correctly rounded fp32 value of the
+ *       inverse root of the fp32 v.  eps sits inside the root, added to the
+ *       mean square (the standard weightless RMSNorm).
+ *   R3  modulation order, left to right as the expression is written:
+ *       n = fl(x * r); one = fl(1 + scale); t = fl(n * one); y = fl(t + shift);
+ *       then one rounding of y to the storage dtype.  1 + scale is formed in
+ *       fp32, not in the storage dtype.
+ *   R4  fused op: the RMS of the fused op is taken over the residual as
+ *       stored (rounded to the dtype), so the fused result equals the
+ *       residual gate followed by the modulation.
+ *   R5  a [B, 1, D] operand serves rows b*L .. b*L+L-1 of batch b.
+ *   R6  fp32 -> bf16/fp16 rounding is round-to-nearest-even, overflow gives
+ *       +-inf, subnormals are kept, NaN stays NaN.
+ */
+#include "dit_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* dtype codecs                                                              */
+/* ------------------------------------------------------------------------ */
+
+static uint32_t f32_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return u;
+}
+
+static float bits_f32(uint32_t u) {
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* bf16 is the upper half of an fp32 word: widening is exact. */
+float orc_bf16_to_f32(uint16_t b) { return bits_f32((uint32_t)b << 16); }
+
+/* Round to nearest, ties to even, by adding just under half an ulp of bf16
+ * (0x7FFF) plus the lowest kept bit, then truncating.  A carry out of the
+ * fraction bumps the exponent, which is the correct rounding up to the next
+ * binade (and to infinity past the largest finite bf16). */
+uint16_t orc_f32_to_bf16(float f) {
+  uint32_t x = f32_bits(f);
+  if (isnan(f)) return (uint16_t)((x >> 16) | 0x0040u); /* quiet NaN */
+  uint32_t lsb = (x >> 16) & 1u;
+  x += 0x7FFFu + lsb;
+  return (uint16_t)(x >> 16);
+}
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+float orc_f16_to_f32(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1F;
+  int frac = h & 0x3FF;
+  float v;
+  if (e == 0)
+    v = ldexpf((float)frac, -24); /* zero or subnormal: frac * 2^-24 */
+  else if (e == 31)
+    v = frac ? NAN : INFINITY;
+  else
+    v = ldexpf((float)(frac + 1024), e - 25); /* (1.frac) * 2^(e-15) */
+  return sign ? -v : v;
+}
+
+/* Round |f| to the binary16 grid.  In the binade [2^E, 2^(E+1)) the spacing
+ * is 2^(E-10); below 2^-14 (subnormals) it is 2^-24.  Dividing by the spacing
+ * (a power of two, so exactly) gives a real number whose nearest integer,
+ * ties to even (nearbyintf in the default rounding mode), is the rounded
+ * significand. */
+uint16_t orc_f32_to_f16(float f) {
+  uint16_t sign = (uint16_t)((f32_bits(f) >> 16) & 0x8000u);
+  if (isnan(f)) return (uint16_t)(sign | 0x7E00u);
+  float a = fabsf(f);
+  if (isinf(a)) return (uint16_t)(sign | 0x7C00u);
+  if (a < 0x1p-14f) {
+    /* k in [0, 1024]; k = 1024 is the smallest normal, whose bit pattern is
+     * exactly 0x0400 = exponent field 1, fraction 0. */
+    float k = nearbyintf(a * 0x1p24f);
+    return (uint16_t)(sign | (uint16_t)k);
+  }
+  int e2;
+  (void)frexpf(a, &e2); /* a = m * 2^e2 with m in [0.5, 1) */
+  int E = e2 - 1;       /* a in [2^E, 2^(E+1)) */
+  float m = nearbyintf(a / ldexpf(1.0f, E - 10)); /* in [1024, 2048] */
+  if (m == 2048.0f) {
+    m = 1024.0f;
+    E += 1;
+  }
+  if (E > 15) return (uint16_t)(sign | 0x7C00u); /* past 65504: infinity */
+  return (uint16_t)(sign | (uint16_t)((E + 15) << 10) |
+                    (uint16_t)((int)m - 1024));
+}
+
+float orc_load(const void* p, int64_t i, int dtype) {
+  switch (dtype) {
+    case ORC_BF16: return orc_bf16_to_f32(((const uint16_t*)p)[i]);
+    case ORC_FP16: return orc_f16_to_f32(((const uint16_t*)p)[i]);
+    default:       return ((const float*)p)[i];
+  }
+}
+
+void orc_store(void* p, int64_t i, float v, int dtype) {
+  switch (dtype) {
+    case ORC_BF16: ((uint16_t*)p)[i] = orc_f32_to_bf16(v); break;
+    case ORC_FP16: ((uint16_t*)p)[i] = orc_f32_to_f16(v); break;
+    default:       ((float*)p)[i] = v; break;
+  }
+}
+
+void orc_decode_array(float* dst_f32, const void* src, int64_t n, int dtype) {
+  for (int64_t i = 0; i < n; ++i) dst_f32[i] = orc_load(src, i, dtype);
+}
+
+void orc_encode_array(void* dst, const float* src_f32, int64_t n, int dtype) {
+  for (int64_t i = 0; i < n; ++i) orc_store(dst, i, src_f32[i], dtype);
+}
+
+/* ------------------------------------------------------------------------ */
+/* one row of each operation                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Row r of  out = hidden + update * gate  (reading R1).  The gate row is r
+ * itself for a full gate and the batch index b = r / L for a [B, 1, D] gate
+ * (reading R5). */
+static void residual_gate_row(void* out, const void* hidden, const void* update,
+                              const void* gate, int64_t r, int64_t L, int64_t D,
+                              int dtype, int gate_layout) {
+  int64_t grow = (gate_layout == ORC_FULL) ? r : r / L;
+  for (int64_t d = 0; d < D; ++d) {
+    float h = orc_load(hidden, r * D + d, dtype);
+    float u = orc_load(update, r * D + d, dtype);
+    float g = orc_load(gate, grow * D + d, dtype);
+    float p = u * g;
+    float s = h + p;
+    orc_store(out, r * D + d, s, dtype);
+  }
+}
+
+/* r = 1 / sqrt(mean(x^2) + eps) for one row (reading R2). */
+float orc_row_rms_inverse(const void* x_row, int64_t D, float eps, int dtype) {
+  double sum = 0.0;
+  for (int64_t d = 0; d < D; ++d) {
+    double v = (double)orc_load(x_row, d, dtype);
+    sum += v * v;
+  }
+  float ms = (float)(sum / (double)D);
+  float v = ms + eps;
+  return (float)(1.0 / sqrt((double)v));
+}
+
+/* Row r of  out = rms_norm(x, eps) * (1 + scale) + shift  (reading R3). */
+static void rmsnorm_modulate_row(void* out, float* t_out, const void* x,
+                                 const void* scale, const void* shift,
+                                 int64_t r, int64_t L, int64_t D, float eps,
+                                 int dtype, int mod_layout) {
+  if (D == 0) return;
+  const size_t esize = (dtype == ORC_FP32) ? 4 : 2;
+  const void* x_row = (const char*)x + (size_t)(r * D) * esize;
+  float rinv = orc_row_rms_inverse(x_row, D, eps, dtype);
+  int64_t mrow = (mod_layout == ORC_FULL) ? r : r / L;
+  for (int64_t d = 0; d < D; ++d) {
+    float xv = orc_load(x, r * D + d, dtype);
+    float sc = orc_load(scale, mrow * D + d, dtype);
+    float sh = orc_load(shift, mrow * D + d, dtype);
+    float n = xv * rinv;
+    float one = 1.0f + sc;
+    float t = n * one;
+    float y = t + sh;
+    if (t_out) t_out[r * D + d] = t;
+    orc_store(out, r * D + d, y, dtype);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* argument checks and row iteration                                         */
+/* ------------------------------------------------------------------------ */
+
+static int bad_common(int64_t B, int64_t L, int64_t D, int dtype,
+                      const int64_t* rows, int64_t nrows) {
+  if (B < 0 || L < 0 || D < 0 || nrows < 0) return 1;
+  if (dtype != ORC_BF16 && dtype != ORC_FP16 && dtype != ORC_FP32) return 1;
+  if (rows) {
+    for (int64_t i = 0; i < nrows; ++i)
+      if (rows[i] < 0 || rows[i] >= B * L) return 1;
+  }
+  return 0;
+}
+
+static int bad_layout(int layout) {
+  return layout != ORC_FULL && layout != ORC_ROW_BCAST;
+}
+
+/* Row at position i of the selection: rows[i], or i itself when rows is NULL. */
+static int64_t row_at(const int64_t* rows, int64_t i) { return rows ? rows[i] : i; }
+
+static int64_t selection_size(int64_t B, int64_t L, const int64_t* rows,
+                              int64_t nrows) {
+  return rows ? nrows : B * L;
+}
+
+typedef struct {
+  int op; /* 0 residual gate, 1 modulate, 2 fused */
+  void* out;
+  void* out2;
+  float* t_out;
+  const void *hidden, *update, *gate, *scale, *shift;
+  int64_t B, L, D;
+  float eps;
+  int dtype, layout1, layout2;
+  const int64_t* rows;
+  int64_t begin, end; /* positions in the row selection */
+} orc_job;
+
+static void run_job(const orc_job* j) {
+  for (int64_t i = j->begin; i < j->end; ++i) {
+    int64_t r = row_at(j->rows, i);
+    if (j->op == 0) {
+      residual_gate_row(j->out, j->hidden, j->update, j->gate, r, j->L, j->D,
+                        j->dtype, j->layout1);
+    } else if (j->op == 1) {
+      rmsnorm_modulate_row(j->out, j->t_out, j->hidden, j->scale, j->shift, r,
+                           j->L, j->D, j->eps, j->dtype, j->layout1);
+    } else {
+      /* reading R4: the stored (rounded) residual is the modulation input */
+      residual_gate_row(j->out, j->hidden, j->update, j->gate, r, j->L, j->D,
+                        j->dtype, j->layout1);
+      rmsnorm_modulate_row(j->out2, j->t_out, j->out, j->scale, j->shift, r,
+                           j->L, j->D, j->eps, j->dtype, j->layout2);
+    }
+  }
+}
+
+static void* job_thread(void* arg) {
+  run_job((const orc_job*)arg);
+  return NULL;
+}
+
+/* Split the selection into nthreads contiguous parts; part 0 runs on the
+ * calling thread. */
+static int run_threads(int nthreads, orc_job base) {
+  int64_t n = base.end;
+  if (nthreads < 1) nthreads = 1;
+  if ((int64_t)nthreads > n) nthreads = (int)(n > 0 ? n : 1);
+  orc_job* jobs = (orc_job*)calloc((size_t)nthreads, sizeof(orc_job));
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !tids) {
+    free(jobs);
+    free(tids);
+    return -1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = base;
+    jobs[t].begin = n * t / nthreads;
+    jobs[t].end = n * (t + 1) / nthreads;
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tids[t], NULL, job_thread, &jobs[t]) != 0) break;
+    started = t;
+  }
+  run_job(&jobs[0]);
+  /* parts whose thread could not be started run here */
+  for (int t = started + 1; t < nthreads; ++t) run_job(&jobs[t]);
+  for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+  free(jobs);
+  free(tids);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* public entry points                                                       */
+/* ------------------------------------------------------------------------ */
+
+int orc_residual_gate_add_mt(int nthreads, void* out, const void* hidden,
+                             const void* update, const void* gate, int64_t B,
+                             int64_t L, int64_t D, int dtype, int gate_layout,
+                             const int64_t* rows, int64_t nrows) {
+  if (bad_common(B, L, D, dtype, rows, nrows) || bad_layout(gate_layout)) return -1;
+  if (B * L * D > 0 && (!out || !hidden || !update || !gate)) return -1;
+  orc_job j = {0};
+  j.op = 0;
+  j.out = out;
+  j.hidden = hidden;
+  j.update = update;
+  j.gate = gate;
+  j.B = B;
+  j.L = L;
+  j.D = D;
+  j.dtype = dtype;
+  j.layout1 = gate_layout;
+  j.rows = rows;
+  j.end = selection_size(B, L, rows, nrows);
+  return run_threads(nthreads, j);
+}
+
+int orc_residual_gate_add(void* out, const void* hidden, const void* update,
+                          const void* gate, int64_t B, int64_t L, int64_t D,
+                          int dtype, int gate_layout, const int64_t* rows,
+                          int64_t nrows) {
+  return orc_residual_gate_add_mt(1, out, hidden, update, gate, B, L, D, dtype,
+                                  gate_layout, rows, nrows);
+}
+
+static int modulate_impl(int nthreads, void* out, float* t_out, const void* x,
+                         const void* scale, const void* shift, int64_t B,
+                         int64_t L, int64_t D, float eps, int dtype,
+                         int mod_layout, const int64_t* rows, int64_t nrows) {
+  if (bad_common(B, L, D, dtype, rows, nrows) || bad_layout(mod_layout)) return -1;
+  if (B * L * D > 0 && (!out || !x || !scale || !shift)) return -1;
+  orc_job j = {0};
+  j.op = 1;
+  j.out = out;
+  j.t_out = t_out;
+  j.hidden = x;
+  j.scale = scale;
+  j.shift = shift;
+  j.B = B;
+  j.L = L;
+  j.D = D;
+  j.eps = eps;
+  j.dtype = dtype;
+  j.layout1 = mod_layout;
+  j.rows = rows;
+  j.end = selection_size(B, L, rows, nrows);
+  return run_threads(nthreads, j);
+}
+
+int orc_rmsnorm_modulate(void* out, float* t_out, const void* x,
+                         const void* scale, const void* shift, int64_t B,
+                         int64_t L, int64_t D, float eps, int dtype,
+                         int mod_layout, const int64_t* rows, int64_t nrows) {
+  return modulate_impl(1, out, t_out, x, scale, shift, B, L, D, eps, dtype,
+                       mod_layout, rows, nrows);
+}
+
+int orc_rmsnorm_modulate_mt(int nthreads, void* out, const void* x,
+                            const void* scale, const void* shift, int64_t B,
+                            int64_t L, int64_t D, float eps, int dtype,
+                            int mod_layout, const int64_t* rows, int64_t nrows) {
+  return modulate_impl(nthreads, out, NULL, x, scale, shift, B, L, D, eps,
+                       dtype, mod_layout, rows, nrows);
+}
+
+static int fused_impl(int nthreads, void* residual_out, void* modulated_out,
+                      float* t_out, const void* hidden, const void* update,
+                      const void* gate, const void* scale, const void* shift,
+                      int64_t B, int64_t L, int64_t D, float eps, int dtype,
+                      int gate_layout, int mod_layout, const int64_t* rows,
+                      int64_t nrows) {
+  if (bad_common(B, L, D, dtype, rows, nrows) || bad_layout(gate_layout) ||
+      bad_layout(mod_layout))
+    return -1;
+  if (B * L * D > 0 && (!residual_out || !modulated_out || !hidden || !update ||
+                        !gate || !scale || !shift))
+    return -1;
+  orc_job j = {0};
+  j.op = 2;
+  j.out = residual_out;
+  j.out2 = modulated_out;
+  j.t_out = t_out;
+  j.hidden = hidden;
+  j.update = update;
+  j.gate = gate;
+  j.scale = scale;
+  j.shift = shift;
+  j.B = B;
+  j.L = L;
+  j.D = D;
+  j.eps = eps;
+  j.dtype = dtype;
+  j.layout1 = gate_layout;
+  j.layout2 = mod_layout;
+  j.rows = rows;
+  j.end = selection_size(B, L, rows, nrows);
+  return run_threads(nthreads, j);
+}
+
+int orc_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out,
+                                  float* t_out, const void* hidden,
+                                  const void* update, const void* gate,
+                                  const void* scale, const void* shift,
+                                  int64_t B, int64_t L, int64_t D, float eps,
+                                  int dtype, int gate_layout, int mod_layout,
+                                  const int64_t* rows, int64_t nrows) {
+  return fused_impl(1, residual_out, modulated_out, t_out, hidden, update, gate,
+                    scale, shift, B, L, D, eps, dtype, gate_layout, mod_layout,
+                    rows, nrows);
+}
+
+int orc_gate_add_rmsnorm_modulate_mt(int nthreads, void* residual_out,
+                                     void* modulated_out, const void* hidden,
+                                     const void* update, const void* gate,
+                                     const void* scale, const void* shift,
+                                     int64_t B, int64_t L, int64_t D, float eps,
+                                     int dtype, int gate_layout, int mod_layout,
+                                     const int64_t* rows, int64_t nrows) {
+  return fused_impl(nthreads, residual_out, modulated_out, NULL, hidden, update,
+                    gate, scale, shift, B, L, D, eps, dtype, gate_layout,
+                    mod_layout, rows, nrows);
+}
