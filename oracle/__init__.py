@@ -60,43 +60,48 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(path):
+    """ctypes handle of an oracle library with its signatures declared."""
+    lib = ctypes.CDLL(path)
+    i64, vp, fp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+    ci = ctypes.c_int
+    lib.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.orc_bf16_to_f32.restype = fp
+    lib.orc_f32_to_bf16.argtypes = [fp]
+    lib.orc_f32_to_bf16.restype = ctypes.c_uint16
+    lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.orc_f16_to_f32.restype = fp
+    lib.orc_f32_to_f16.argtypes = [fp]
+    lib.orc_f32_to_f16.restype = ctypes.c_uint16
+    lib.orc_decode_array.argtypes = [vp, vp, i64, ci]
+    lib.orc_decode_array.restype = None
+    lib.orc_encode_array.argtypes = [vp, vp, i64, ci]
+    lib.orc_encode_array.restype = None
+    lib.orc_rmsnorm_modulate.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64,
+                                         fp, ci, ci, vp, i64]
+    lib.orc_rmsnorm_modulate.restype = ci
+    lib.orc_gate_add_rmsnorm_modulate.argtypes = [
+        vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
+    lib.orc_gate_add_rmsnorm_modulate.restype = ci
+    lib.orc_row_rms_inverse.argtypes = [vp, i64, fp, ci]
+    lib.orc_row_rms_inverse.restype = fp
+    lib.orc_residual_gate_add_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
+                                             i64, ci, ci, vp, i64]
+    lib.orc_residual_gate_add_mt.restype = ci
+    lib.orc_rmsnorm_modulate_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
+                                            i64, fp, ci, ci, vp, i64]
+    lib.orc_rmsnorm_modulate_mt.restype = ci
+    lib.orc_gate_add_rmsnorm_modulate_mt.argtypes = [
+        ci, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
+    lib.orc_gate_add_rmsnorm_modulate_mt.restype = ci
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            i64, vp, fp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
-            ci = ctypes.c_int
-            lib.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
-            lib.orc_bf16_to_f32.restype = fp
-            lib.orc_f32_to_bf16.argtypes = [fp]
-            lib.orc_f32_to_bf16.restype = ctypes.c_uint16
-            lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
-            lib.orc_f16_to_f32.restype = fp
-            lib.orc_f32_to_f16.argtypes = [fp]
-            lib.orc_f32_to_f16.restype = ctypes.c_uint16
-            lib.orc_decode_array.argtypes = [vp, vp, i64, ci]
-            lib.orc_decode_array.restype = None
-            lib.orc_encode_array.argtypes = [vp, vp, i64, ci]
-            lib.orc_encode_array.restype = None
-            lib.orc_rmsnorm_modulate.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64,
-                                                 fp, ci, ci, vp, i64]
-            lib.orc_rmsnorm_modulate.restype = ci
-            lib.orc_gate_add_rmsnorm_modulate.argtypes = [
-                vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
-            lib.orc_gate_add_rmsnorm_modulate.restype = ci
-            lib.orc_row_rms_inverse.argtypes = [vp, i64, fp, ci]
-            lib.orc_row_rms_inverse.restype = fp
-            lib.orc_residual_gate_add_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
-                                                     i64, ci, ci, vp, i64]
-            lib.orc_residual_gate_add_mt.restype = ci
-            lib.orc_rmsnorm_modulate_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
-                                                    i64, fp, ci, ci, vp, i64]
-            lib.orc_rmsnorm_modulate_mt.restype = ci
-            lib.orc_gate_add_rmsnorm_modulate_mt.argtypes = [
-                ci, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
-            lib.orc_gate_add_rmsnorm_modulate_mt.restype = ci
-            _lib = lib
+            _lib = _bind(build())
     return _lib
 
 
@@ -197,3 +202,22 @@ def gate_add_rmsnorm_modulate(residual_out, modulated_out, hidden, update, gate,
 
 def row_rms_inverse(x_row, D, eps=1e-6, dtype="bf16") -> float:
     return _load().orc_row_rms_inverse(_ptr(x_row), D, float(eps), DTYPES[dtype])
+
+
+def variant(lib_path: str):
+    """A namespace with this module's functions bound to another build of the
+    oracle source (used by the tests that plant mistakes in a copy of it)."""
+    import sys
+    import types
+    ns = types.ModuleType("oracle_variant")
+    src = sys.modules[__name__]
+    lib = _bind(lib_path)
+    for name in ("decode", "encode", "residual_gate_add", "rmsnorm_modulate",
+                 "gate_add_rmsnorm_modulate", "row_rms_inverse"):
+        fn = getattr(src, name)
+        g = dict(fn.__globals__)
+        g["_load"] = lambda lib=lib: lib
+        setattr(ns, name, types.FunctionType(fn.__code__, g, name, fn.__defaults__))
+    for name in ("DTYPES", "LAYOUTS", "ELEM_SIZE"):
+        setattr(ns, name, getattr(src, name))
+    return ns
