@@ -1,0 +1,618 @@
+#!/usr/bin/env python3
+"""Benchmark of the DiT elementwise hot path on GB300.
+
+Metric: achieved HBM GB/s (algorithmic bytes / device time) and its fraction
+of the measured GB300 copy bandwidth, with microseconds per call per kernel.
+
+Default workload ("hotpath"): one step is one pass of every operation of the
+path over the largest broadcast shape, [B, L, D] = [1, 32640, 4096] bf16
+(about 267 MB per tensor; shape from sglang PR #29361, B200 kernel benchmark
+table, ltx2_bcast_s32640_c4096):
+
+  rga_bcast          out = hidden + update * gate[1,1,D]
+  rga_bcast_inplace  hidden += update * gate[1,1,D]
+  rga_full           out = hidden + update * gate[1,L,D]
+  mod_bcast          out = rms_norm(x, 1e-6) * (1 + scale[1,1,D]) + shift[1,1,D]
+  fused_bcast        residual, modulated = both in one pass
+
+Every op reads its own input tensors, each larger than the 129 MB L2, so no
+op or step re-reads another's data from L2.  Other workloads: "chain" (the
+8-block DiT chain at B=2, 25 launches per step) and "shapes" (one line per
+workload shape and op, for the per-shape table).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same workload on its own GPU (the rows of
+these ops are independent: no data-path collective); value = bytes of all
+ranks / max over ranks of the timed region.  --impl reference times the CPU
+oracle (the reference arm of this repository) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 peak per shape; µs/call (device-timed)"
+FALLBACK_HBM_GBS = 6800.0
+EPS = 1e-6
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources (ties a stored ncu traffic figure to them)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "diffusion_transformer_elementwise_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key):
+    """DRAM bytes per launch from profiles/traffic.json, if taken on the
+    current sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = data.get(kernel_key)
+    if not entry or entry.get("source_sha") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class Op:
+    def __init__(self, name, fn, nbytes, inputs, outputs, sample):
+        self.name = name
+        self.fn = fn            # enqueue the op on the current stream
+        self.bytes = nbytes     # algorithmic bytes per call
+        self.inputs = inputs    # device tensors copied in for the e2e number
+        self.outputs = outputs  # device tensors copied out for the e2e number
+        self.sample = sample    # callable(rows) -> oracle callable for the CPU baseline
+
+
+def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16"):
+    import torch
+
+    import diffusion_transformer_elementwise_gb300 as dit
+    from diffusion_transformer_elementwise_gb300.synth import draw, seed_for
+
+    es = 2 if dtype != "fp32" else 4
+    N = B * L * D
+
+    def act(name):
+        return draw("act", (B, L, D), seed_for("bench", name), dtype, device)
+
+    g_b = draw("gate", (B, 1, D), seed_for("bench", "gate_b"), dtype, device)
+    g_f = draw("gate", (B, L, D), seed_for("bench", "gate_f"), dtype, device)
+    sc = draw("mod", (B, 1, D), seed_for("bench", "scale"), dtype, device)
+    sh = draw("mod", (B, 1, D), seed_for("bench", "shift"), dtype, device)
+    h1, u1 = act("h1"), act("u1")
+    h2, u2 = act("h2"), act("u2")
+    h3, u3 = act("h3"), act("u3")
+    x4 = act("x4")
+    h5, u5 = act("h5"), act("u5")
+    o1, o3, o4 = (torch.empty_like(h1) for _ in range(3))
+    r5, m5 = torch.empty_like(h1), torch.empty_like(h1)
+
+    def sampler(kind, tensors, layout=None):
+        def make(rows):
+            import oracle
+            host = [t[:, :rows].contiguous().cpu() if t.shape[1] == L else t.cpu()
+                    for t in tensors]
+            outs = [torch.empty((B, rows, D), dtype=host[0].dtype) for _ in range(2)]
+
+            def run(threads):
+                if kind == "rga":
+                    oracle.residual_gate_add(outs[0], host[0], host[1], host[2], B, rows, D,
+                                             dtype, layout, threads=threads)
+                elif kind == "mod":
+                    oracle.rmsnorm_modulate(outs[0], host[0], host[1], host[2], B, rows, D,
+                                            EPS, dtype, "bcast", threads=threads)
+                else:
+                    oracle.gate_add_rmsnorm_modulate(outs[0], outs[1], *host, B, rows, D, EPS,
+                                                     dtype, "bcast", "bcast", threads=threads)
+            return run
+        return make
+
+    vb = B * D * es
+    return [
+        Op("rga_bcast", lambda: dit.residual_gate_add(h1, u1, g_b, out=o1),
+           3 * N * es + vb, [h1, u1, g_b], [o1], sampler("rga", [h1, u1, g_b], "bcast")),
+        Op("rga_bcast_inplace", lambda: dit.residual_gate_add(h2, u2, g_b, out=h2),
+           3 * N * es + vb, [h2, u2, g_b], [h2], sampler("rga", [h2, u2, g_b], "bcast")),
+        Op("rga_full", lambda: dit.residual_gate_add(h3, u3, g_f, out=o3),
+           4 * N * es, [h3, u3, g_f], [o3], sampler("rga", [h3, u3, g_f], "full")),
+        Op("mod_bcast", lambda: dit.rmsnorm_modulate(x4, sc, sh, EPS, out=o4),
+           2 * N * es + 2 * vb, [x4, sc, sh], [o4], sampler("mod", [x4, sc, sh])),
+        Op("fused_bcast",
+           lambda: dit.gate_add_rmsnorm_modulate(h5, u5, g_b, sc, sh, EPS, residual_out=r5,
+                                                 modulated_out=m5),
+           4 * N * es + 3 * vb, [h5, u5, g_b, sc, sh], [r5, m5],
+           sampler("fused", [h5, u5, g_b, sc, sh])),
+    ]
+
+
+def chain_ops(device, B=2, L=32640, D=4096, blocks=8, dtype="bf16"):
+    """The chain as one op per launch (so each kernel is timed)."""
+    import torch
+
+    import diffusion_transformer_elementwise_gb300 as dit
+    from diffusion_transformer_elementwise_gb300 import chain
+
+    es = 2 if dtype != "fp32" else 4
+    x, updates, tables = chain.make_inputs(B, L, D, blocks, dtype, device, seed_tag="bench")
+    m = torch.empty_like(x)
+    N, vb = B * L * D, B * D * es
+    sites = chain.site_list(blocks)
+    ops = []
+    s0 = tables[0][chain.SITES[0]]
+    ops.append(Op("chain_mod", lambda: dit.rmsnorm_modulate(x, s0[1], s0[0], EPS, out=m),
+                  2 * N * es + 2 * vb, [x], [m], None))
+    for j, (blk, k) in enumerate(sites):
+        gate = tables[blk][chain.SITES[k]][2]
+        u = updates[k]
+        if j + 1 < len(sites):
+            nb, nk = sites[j + 1]
+            shf, scl, _ = tables[nb][chain.SITES[nk]]
+            fn = (lambda u=u, gate=gate, scl=scl, shf=shf:
+                  dit.gate_add_rmsnorm_modulate(x, u, gate, scl, shf, EPS, residual_out=x,
+                                                modulated_out=m))
+            ops.append(Op("chain_fused", fn, 4 * N * es + 3 * vb, [], [], None))
+        else:
+            ops.append(Op("chain_rga", lambda u=u, gate=gate:
+                          dit.residual_gate_add(x, u, gate, out=x), 3 * N * es + vb, [],
+                          [x], None))
+    ops[0].inputs = [x] + updates
+    return ops
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+
+def time_steps(ops, steps, warmup, dist=None):
+    """Warm up, then time exactly `steps` steps with CUDA events on the
+    current stream (one event pair per op, and one around everything)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for op in ops:
+            op.fn()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in ops] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s in range(steps):
+        for i, op in enumerate(ops):
+            ev[s][i][0].record(stream)
+            op.fn()
+            ev[s][i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    per_op = {}
+    for i, op in enumerate(ops):
+        t = [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)]
+        d = per_op.setdefault(op.name, {"ms": [], "bytes": op.bytes, "calls": 0})
+        d["ms"].extend(t)
+        d["calls"] += steps
+    return total_ms, per_op
+
+
+def time_e2e(ops, steps):
+    """The same step through the public API from pinned host buffers: every
+    step copies its inputs host -> device, runs the ops and copies the
+    results device -> host, all inside the timed region."""
+    import torch
+    hin = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for op in ops
+           for t in op.inputs]
+    hout = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for op in ops
+            for t in op.outputs]
+    for d, h in hin:
+        h.copy_(d)
+    h2d = sum(t.numel() * t.element_size() for t, _ in hin)
+    d2h = sum(t.numel() * t.element_size() for t, _ in hout)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for d, h in hin:
+            d.copy_(h, non_blocking=True)
+        for op in ops:
+            op.fn()
+        for d, h in hout:
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end), h2d, d2h
+
+
+def cpu_baseline(ops, budget_s=12.0, rows=512):
+    """The oracle (as it stands) on the host cores: the same ops on the first
+    `rows` rows, repeated for about budget_s seconds, all cores and one core."""
+    import torch  # noqa: F401
+    cores = os.cpu_count() or 1
+    runs = [(op, op.sample(rows)) for op in ops if op.sample is not None]
+    frac = rows / 32640
+
+    def rate(threads, seconds):
+        done, t0 = 0.0, time.perf_counter()
+        while True:
+            for op, run in runs:
+                run(threads)
+                done += op.bytes * frac
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return done / el / 1e9, el
+
+    multi, el_m = rate(cores, budget_s * 0.75)
+    single, el_s = rate(1, budget_s * 0.25)
+    return {"value": multi, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_thread_value": single,
+            "sample": f"the step's {len(runs)} ops on the first {rows} of 32640 rows "
+                      f"([1,{rows},4096] bf16), repeated for {el_m:.1f} s on {cores} threads "
+                      f"and {el_s:.1f} s on 1 thread; GB/s on the same algorithmic bytes"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, each step a
+    bounded sample of the hot-path workload."""
+    import torch
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    from diffusion_transformer_elementwise_gb300.synth import draw, seed_for
+    B, L, D, es = 1, 32640, 4096, 2
+    cores = os.cpu_count() or 1
+    total_steps = args.steps + args.warmup
+    rows = max(16, min(1024, int(32 * 300 / max(total_steps, 1))))
+    h = draw("act", (B, rows, D), seed_for("ref", "h"), "bf16")
+    u = draw("act", (B, rows, D), seed_for("ref", "u"), "bf16")
+    gb = draw("gate", (B, 1, D), seed_for("ref", "gb"), "bf16")
+    gf = draw("gate", (B, rows, D), seed_for("ref", "gf"), "bf16")
+    sc = draw("mod", (B, 1, D), seed_for("ref", "sc"), "bf16")
+    sh = draw("mod", (B, 1, D), seed_for("ref", "sh"), "bf16")
+    o, o2 = torch.empty_like(h), torch.empty_like(h)
+    hh = h.clone()  # updated in place every step
+    n = B * rows * D
+    vb = B * D * es
+    step_bytes = 2 * (3 * n * es + vb) + 4 * n * es + (2 * n * es + 2 * vb) + (4 * n * es + 3 * vb)
+
+    def step():
+        oracle.residual_gate_add(o, h, u, gb, B, rows, D, "bf16", "bcast", threads=cores)
+        oracle.residual_gate_add(hh, hh, u, gb, B, rows, D, "bf16", "bcast", threads=cores)
+        oracle.residual_gate_add(o, h, u, gf, B, rows, D, "bf16", "full", threads=cores)
+        oracle.rmsnorm_modulate(o, h, sc, sh, B, rows, D, EPS, "bf16", "bcast", threads=cores)
+        oracle.gate_add_rmsnorm_modulate(o, o2, h, u, gb, sc, sh, B, rows, D, EPS, "bf16",
+                                         "bcast", "bcast", threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = step_bytes * args.steps / el / 1e9
+    sample = (f"each step: the 5 hot-path ops on {rows} of the 32640 rows of "
+              f"[1,32640,4096] bf16 on {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "ltx2_bcast_s32640_c4096 hot path (sampled rows)",
+                       "B": 1, "L": 32640, "D": 4096, "rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+
+    from diffusion_transformer_elementwise_gb300.build import build
+    if rank == 0:
+        build()
+    if dist is not None:
+        dist.barrier()
+    build()  # no-op when up to date
+
+    if args.workload == "chain":
+        ops = chain_ops(device)
+        workload = {"workload": "ltx2_chain_b2_s32640_c4096: 8 DiT blocks x 3 sites "
+                                "(1 modulation + 23 fused + 1 residual gate per step)",
+                    "B": 2, "L": 32640, "D": 4096, "blocks": 8}
+    else:
+        ops = hotpath_ops(device)
+        workload = {"workload": "ltx2_bcast_s32640_c4096 hot path: rga_bcast, "
+                                "rga_bcast_inplace, rga_full, mod_bcast, fused_bcast",
+                    "B": 1, "L": 32640, "D": 4096}
+    workload["l2"] = ("no flush: every op reads its own inputs, each 267 MB or more, "
+                      "above the 129 MB L2")
+    workload["eps"] = EPS
+
+    with ClockSampler(local) as clk:
+        total_ms, per_op = time_steps(ops, args.steps, args.warmup, dist)
+    clocks = clk.summary()
+
+    max_ms = total_ms
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+    step_bytes = sum(op.bytes for op in ops)
+    value = step_bytes * args.steps * world / (max_ms * 1e-3) / 1e9
+
+    peak, peak_kind = hbm_peak()
+    table = {}
+    for name, d in per_op.items():
+        avg_ms = sum(d["ms"]) / len(d["ms"])
+        gbs = d["bytes"] / (avg_ms * 1e-3) / 1e9
+        table[name] = {"us_per_call": avg_ms * 1e3, "median_us": statistics.median(d["ms"]) * 1e3,
+                       "min_us": min(d["ms"]) * 1e3, "bytes": d["bytes"], "GB_s": gbs,
+                       "frac_of_peak": gbs / peak, "calls": d["calls"],
+                       "share": sum(d["ms"]) / sum(sum(x["ms"]) for x in per_op.values())}
+    dom = max(table, key=lambda k: table[k]["share"])
+    roof = {"bound": "hbm", "kernel": dom, "achieved": table[dom]["GB_s"], "peak": peak,
+            "unit": "GB/s", "frac": table[dom]["GB_s"] / peak,
+            "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "traffic": stored_traffic(dom)}
+
+    e2e = None
+    if not args.no_e2e:
+        e_steps = max(3, min(args.steps, 20))
+        e_ms, h2d, d2h = time_e2e(ops, e_steps)
+        e_max = e_ms
+        if dist is not None:
+            t = torch.tensor([e_ms], device=device, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_max = float(t.item())
+        e2e = {"value": step_bytes * e_steps * world / (e_max * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "ms_per_step": e_max / e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu and args.workload != "chain":
+        cpu = cpu_baseline(ops)
+
+    if dist is not None:
+        dist.barrier()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": workload, "roofline": roof,
+                "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": len(ops) * args.steps, "clocks": clocks, "per_op": table}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_shapes(args):
+    """One line per (shape, op): device-timed us per call with an L2 flush
+    before every call (a write of 4x the L2 size outside the timed region)."""
+    import torch
+
+    import diffusion_transformer_elementwise_gb300 as dit
+    from diffusion_transformer_elementwise_gb300.build import build
+    from diffusion_transformer_elementwise_gb300.synth import draw, seed_for
+    build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev)
+    peak, _ = hbm_peak()
+    shapes = [("ltx2_full_s126_c2048", 1, 126, 2048, "full", "bf16"),
+              ("flux2_bcast_s4608_c3072", 1, 4608, 3072, "bcast", "bf16"),
+              ("ideogram4_bcast_s4096_c4608", 1, 4096, 4608, "bcast", "bf16"),
+              ("flux2_bcast_s4096_c3072", 1, 4096, 3072, "bcast", "bf16"),
+              ("flux2_bcast_s512_c3072", 1, 512, 3072, "bcast", "bf16"),
+              ("ltx2_full_s8160_c4096", 1, 8160, 4096, "full", "bf16"),
+              ("ltx2_bcast_s32640_c4096", 1, 32640, 4096, "bcast", "bf16")]
+    shapes += [(f"tail_s4097_c{D}_{dt}", 1, 4097, D, "bcast", dt)
+               for D in (3080, 3076, 3077) for dt in ("bf16", "fp16", "fp32")]
+    shapes += [(f"flux2_bcast_s4608_c3072_{dt}", 1, 4608, 3072, "bcast", dt)
+               for dt in ("fp16", "fp32")]
+    for name, B, L, D, lay, dt in shapes:
+        es = 4 if dt == "fp32" else 2
+        N, vbytes = B * L * D, B * D * es
+        shp = (B, L, D) if lay == "full" else (B, 1, D)
+        h = draw("act", (B, L, D), seed_for(name, "h"), dt, dev)
+        u = draw("act", (B, L, D), seed_for(name, "u"), dt, dev)
+        g = draw("gate", shp, seed_for(name, "g"), dt, dev)
+        sc = draw("mod", (B, 1, D), seed_for(name, "sc"), dt, dev)
+        sh = draw("mod", (B, 1, D), seed_for(name, "sh"), dt, dev)
+        o, o2 = torch.empty_like(h), torch.empty_like(h)
+        cases = [("residual_gate_" + lay, lambda: dit.residual_gate_add(h, u, g, out=o),
+                  (4 * N * es) if lay == "full" else (3 * N * es + vbytes)),
+                 ("modulate_bcast", lambda: dit.rmsnorm_modulate(h, sc, sh, EPS, out=o),
+                  2 * N * es + 2 * vbytes),
+                 ("fused_" + lay + "_bcast",
+                  lambda: dit.gate_add_rmsnorm_modulate(h, u, g, sc, sh, EPS, residual_out=o,
+                                                        modulated_out=o2),
+                  4 * N * es + (3 * vbytes if lay == "bcast" else N * es + 2 * vbytes))]
+        for op, fn, nbytes in cases:
+            for _ in range(10):
+                fn()
+            times, hot = [], []
+            for _ in range(max(args.steps, 30)):
+                flush.fill_(1.0)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                fn()
+                e.record()
+                torch.cuda.synchronize()
+                times.append(s.elapsed_time(e))
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(20):
+                fn()
+            e.record()
+            torch.cuda.synchronize()
+            med = statistics.median(times)
+            gbs = nbytes / (med * 1e-3) / 1e9
+            print(json.dumps({"shape": name, "op": op, "dtype": dt, "B": B, "L": L, "D": D,
+                              "bytes": nbytes, "median_us": med * 1e3,
+                              "min_us": min(times) * 1e3, "GB_s": gbs,
+                              "frac_of_peak": gbs / peak,
+                              "back_to_back_us": s.elapsed_time(e) / 20 * 1e3}), flush=True)
+        del h, u, g, o, o2
+    return 0
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["hotpath", "chain", "shapes"], default="hotpath")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.workload == "shapes":
+        return run_shapes(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

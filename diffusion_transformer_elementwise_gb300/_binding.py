@@ -1,0 +1,183 @@
+"""ctypes binding of libdit_elementwise.so (include/dit_elementwise.h).
+
+Argument marshalling only: every function checks that its tensors are
+contiguous CUDA tensors of one dtype, passes their addresses, sizes, dtype,
+layouts and the current torch stream to the C ABI, and raises
+:class:`DitError` on a non-OK status.  There is no other code path: without
+the built library, or with CPU tensors, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB
+
+DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+FULL, ROW_BCAST = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DitError(RuntimeError):
+    """A dit_* call returned a status other than DIT_OK."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(
+                    f"{LIB} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` "
+                    "(nvcc for sm_103a); there is no fallback path")
+            lib = ctypes.CDLL(LIB)
+            vp, i64, ci, cf = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            lib.dit_abi_version.argtypes = []
+            lib.dit_abi_version.restype = ci
+            lib.dit_status_string.argtypes = [ci]
+            lib.dit_status_string.restype = ctypes.c_char_p
+            lib.dit_residual_gate_add.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, vp]
+            lib.dit_residual_gate_add.restype = ci
+            lib.dit_rmsnorm_modulate.argtypes = [vp, vp, vp, vp, i64, i64, i64, cf, ci, ci, vp]
+            lib.dit_rmsnorm_modulate.restype = ci
+            lib.dit_gate_add_rmsnorm_modulate.argtypes = [
+                vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, cf, ci, ci, ci, vp]
+            lib.dit_gate_add_rmsnorm_modulate.restype = ci
+            _lib = lib
+    return _lib
+
+
+def check(status: int, what: str) -> None:
+    if status != 0:
+        msg = library().dit_status_string(status).decode()
+        raise DitError(status, f"{what}: {msg}")
+
+
+def _shape3(t: torch.Tensor, name: str):
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [B, L, D], got {tuple(t.shape)}")
+    return tuple(int(s) for s in t.shape)
+
+
+def _cuda(*tensors):
+    dev = None
+    for name, t in tensors:
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise TypeError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, expected {dev}")
+    return dev
+
+
+def _dtype(ref: torch.Tensor, *others) -> int:
+    if ref.dtype not in DTYPE_CODES:
+        raise TypeError(f"unsupported dtype {ref.dtype}: bf16, fp16 or fp32")
+    for name, t in others:
+        if t.dtype != ref.dtype:
+            raise TypeError(f"{name} is {t.dtype}, expected {ref.dtype}")
+    return DTYPE_CODES[ref.dtype]
+
+
+def layout_of(t: torch.Tensor, B: int, L: int, D: int, name: str) -> int:
+    """FULL for [B, L, D], ROW_BCAST for [B, 1, D]."""
+    shape = tuple(t.shape)
+    if shape == (B, L, D):
+        return FULL
+    if shape == (B, 1, D):
+        return ROW_BCAST
+    raise ValueError(f"{name} must be [{B}, {L}, {D}] or [{B}, 1, {D}], got {shape}")
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def residual_gate_add(hidden, update, gate, out=None, stream=None):
+    """out = hidden + update * gate; gate [B, L, D] or [B, 1, D].  Pass
+    out=hidden for the in-place update.  Returns out."""
+    B, L, D = _shape3(hidden, "hidden")
+    if out is None:
+        out = torch.empty_like(hidden)
+    dev = _cuda(("hidden", hidden), ("update", update), ("gate", gate), ("out", out))
+    dt = _dtype(hidden, ("update", update), ("gate", gate), ("out", out))
+    if tuple(update.shape) != (B, L, D) or tuple(out.shape) != (B, L, D):
+        raise ValueError("update and out must have the shape of hidden")
+    lay = layout_of(gate, B, L, D, "gate")
+    with torch.cuda.device(dev):
+        st = library().dit_residual_gate_add(out.data_ptr(), hidden.data_ptr(),
+                                             update.data_ptr(), gate.data_ptr(), B, L, D,
+                                             dt, lay, _stream(dev, stream))
+    check(st, "dit_residual_gate_add")
+    return out
+
+
+def rmsnorm_modulate(x, scale, shift, eps=1e-6, out=None, stream=None):
+    """out = rms_norm(x, eps) * (1 + scale) + shift; scale/shift [B, L, D] or
+    [B, 1, D] (the same layout for both).  Returns out."""
+    B, L, D = _shape3(x, "x")
+    if out is None:
+        out = torch.empty_like(x)
+    dev = _cuda(("x", x), ("scale", scale), ("shift", shift), ("out", out))
+    dt = _dtype(x, ("scale", scale), ("shift", shift), ("out", out))
+    if tuple(out.shape) != (B, L, D):
+        raise ValueError("out must have the shape of x")
+    lay = layout_of(scale, B, L, D, "scale")
+    if layout_of(shift, B, L, D, "shift") != lay:
+        raise ValueError("scale and shift must have the same layout")
+    with torch.cuda.device(dev):
+        st = library().dit_rmsnorm_modulate(out.data_ptr(), x.data_ptr(), scale.data_ptr(),
+                                            shift.data_ptr(), B, L, D, float(eps), dt, lay,
+                                            _stream(dev, stream))
+    check(st, "dit_rmsnorm_modulate")
+    return out
+
+
+def gate_add_rmsnorm_modulate(hidden, update, gate, scale, shift, eps=1e-6,
+                              residual_out=None, modulated_out=None, stream=None):
+    """residual_out = hidden + update * gate; modulated_out =
+    rms_norm(residual_out, eps) * (1 + scale) + shift, in one pass.  Pass
+    residual_out=hidden to update the residual in place.  Returns
+    (residual_out, modulated_out)."""
+    B, L, D = _shape3(hidden, "hidden")
+    if residual_out is None:
+        residual_out = torch.empty_like(hidden)
+    if modulated_out is None:
+        modulated_out = torch.empty_like(hidden)
+    dev = _cuda(("hidden", hidden), ("update", update), ("gate", gate), ("scale", scale),
+                ("shift", shift), ("residual_out", residual_out),
+                ("modulated_out", modulated_out))
+    dt = _dtype(hidden, ("update", update), ("gate", gate), ("scale", scale),
+                ("shift", shift), ("residual_out", residual_out),
+                ("modulated_out", modulated_out))
+    for name, t in (("update", update), ("residual_out", residual_out),
+                    ("modulated_out", modulated_out)):
+        if tuple(t.shape) != (B, L, D):
+            raise ValueError(f"{name} must have the shape of hidden")
+    glay = layout_of(gate, B, L, D, "gate")
+    mlay = layout_of(scale, B, L, D, "scale")
+    if layout_of(shift, B, L, D, "shift") != mlay:
+        raise ValueError("scale and shift must have the same layout")
+    with torch.cuda.device(dev):
+        st = library().dit_gate_add_rmsnorm_modulate(
+            residual_out.data_ptr(), modulated_out.data_ptr(), hidden.data_ptr(),
+            update.data_ptr(), gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D,
+            float(eps), dt, glay, mlay, _stream(dev, stream))
+    check(st, "dit_gate_add_rmsnorm_modulate")
+    return residual_out, modulated_out

@@ -1,0 +1,95 @@
+"""A synthetic DiT block chain over the three ops: the residual stream of
+LTX-2-style transformer blocks with the attention and MLP replaced by
+stand-in updates.
+
+Each block carries an adaLN table of nine [B, 1, D] vectors: (shift, scale,
+gate) for each of its three sites -- self-attention, prompt cross-attention,
+feed-forward (prhub summary of sglang PR #34172, "implementation breakdown"
+item 3: the adaLN modulation sites of LTX2TransformerBlock.forward).  The
+sites run in the order sa -> ca -> ff -> next block's sa.  With x the
+residual stream:
+
+    m = rmsnorm_modulate(x; scale, shift of site 0)
+    for each site j:
+        u = stand-in update of site j's kind (independent of m)
+        if j is not the last site:
+            x, m = gate_add_rmsnorm_modulate(x, u, gate_j; scale, shift of site j+1)
+        else:
+            x = residual_gate_add(x, u, gate_j)
+
+so 8 blocks = 24 sites = 1 modulation + 23 fused + 1 residual gate.  x is
+updated in place.  The chain moves (2 + 23 * 4 + 3) * N * s bytes of
+activations (N = B * L * D elements of s bytes) plus the small vectors.
+"""
+from __future__ import annotations
+
+from ._binding import gate_add_rmsnorm_modulate, residual_gate_add, rmsnorm_modulate
+from .synth import draw, seed_for
+
+SITES = ("sa", "ca", "ff")
+
+
+def make_inputs(B, L, D, blocks=8, dtype="bf16", device="cuda", seed_tag="chain"):
+    """x [B, L, D], one stand-in update per site kind, and per block a dict
+    site -> (shift, scale, gate), all seeded."""
+    x = draw("act", (B, L, D), seed_for(seed_tag, "x", B, L, D), dtype, device)
+    updates = [draw("act", (B, L, D), seed_for(seed_tag, "u", k, B, L, D), dtype, device)
+               for k in range(len(SITES))]
+    tables = []
+    for blk in range(blocks):
+        t = {}
+        for site in SITES:
+            t[site] = tuple(draw("mod", (B, 1, D), seed_for(seed_tag, "table", blk, site, part,
+                                                           B, D), dtype, device)
+                            for part in ("shift", "scale", "gate"))
+        tables.append(t)
+    return x, updates, tables
+
+
+def site_list(blocks):
+    return [(b, k) for b in range(blocks) for k in range(len(SITES))]
+
+
+def run(x, updates, tables, eps=1e-6, m=None, on_site=None, stream=None):
+    """Run the chain on the GPU through the C ABI.  x is updated in place;
+    m (allocated if None) holds the last modulated input.  on_site(j, x, m)
+    is called after site j's op is enqueued (j = -1 after the first
+    modulation).  Returns (x, m)."""
+    import torch
+    sites = site_list(len(tables))
+    if m is None:
+        m = torch.empty_like(x)
+    shift0, scale0, _ = tables[0][SITES[0]]
+    rmsnorm_modulate(x, scale0, shift0, eps, out=m, stream=stream)
+    if on_site:
+        on_site(-1, x, m)
+    for j, (blk, k) in enumerate(sites):
+        gate = tables[blk][SITES[k]][2]
+        u = updates[k]
+        if j + 1 < len(sites):
+            nb, nk = sites[j + 1]
+            shift, scale, _ = tables[nb][SITES[nk]]
+            gate_add_rmsnorm_modulate(x, u, gate, scale, shift, eps, residual_out=x,
+                                      modulated_out=m, stream=stream)
+        else:
+            residual_gate_add(x, u, gate, out=x, stream=stream)
+        if on_site:
+            on_site(j, x, m)
+    return x, m
+
+
+def launches(blocks: int) -> int:
+    return 1 + 3 * blocks
+
+
+def algorithmic_bytes(B, L, D, blocks, es):
+    """Bytes the chain must move: the first modulation reads x and writes m,
+    each fused site reads x and u and writes x and m, the last residual gate
+    reads x and u and writes x; each op's [B, 1, D] vectors counted once."""
+    n = B * L * D * es
+    v = B * D * es
+    sites = 3 * blocks
+    first = 2 * n + 2 * v
+    fused = (sites - 1) * (4 * n + 3 * v)
+    last = 3 * n + v
+    return first + fused + last

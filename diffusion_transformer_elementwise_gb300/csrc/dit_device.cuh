@@ -1,0 +1,266 @@
+// dit_device.cuh -- device helpers for the DiT elementwise kernels (sm_103a).
+//
+// * Raw<VB>: VB bytes of storage held in registers (VB = 32, 16, 8, 4 or 2).
+// * ld_stream / st_stream: vector accesses for data touched once (activations),
+//   issued as one ld/st of VB bytes; 32-byte accesses use the 256-bit vector
+//   forms that sm_100-class GPUs add to ld/st.  Loads skip L1 allocation.
+// * ld_bcast: vector loads of the small [B, 1, D] operands, which every CTA of
+//   a batch re-reads; they go through the read-only path and stay cached.
+// * Vec<T, VB>: exact widening of VB bytes of T to fp32 and one
+//   round-to-nearest-even narrowing back (cvt.rn; subnormals kept, no FTZ).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace dit {
+
+template <int VB>
+struct Raw {
+  uint32_t w[VB / 4];
+};
+template <>
+struct Raw<2> {
+  uint16_t h;
+};
+
+// ---------------------------------------------------------------------------
+// loads and stores
+// ---------------------------------------------------------------------------
+
+template <int VB>
+__device__ __forceinline__ Raw<VB> ld_stream(const void* p);
+template <int VB>
+__device__ __forceinline__ Raw<VB> ld_bcast(const void* p);
+template <int VB>
+__device__ __forceinline__ void st_stream(void* p, const Raw<VB>& v);
+
+template <>
+__device__ __forceinline__ Raw<32> ld_stream<32>(const void* p) {
+  Raw<32> r;
+  asm volatile(
+      "ld.global.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+        "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+      : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<16> ld_stream<16>(const void* p) {
+  Raw<16> r;
+  asm volatile("ld.global.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+               : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<8> ld_stream<8>(const void* p) {
+  Raw<8> r;
+  asm volatile("ld.global.L1::no_allocate.v2.b32 {%0,%1}, [%2];"
+               : "=r"(r.w[0]), "=r"(r.w[1])
+               : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<4> ld_stream<4>(const void* p) {
+  Raw<4> r;
+  asm volatile("ld.global.L1::no_allocate.b32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<2> ld_stream<2>(const void* p) {
+  Raw<2> r;
+  asm volatile("ld.global.L1::no_allocate.b16 %0, [%1];" : "=h"(r.h) : "l"(p));
+  return r;
+}
+
+template <>
+__device__ __forceinline__ Raw<32> ld_bcast<32>(const void* p) {
+  Raw<32> r;
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]),
+                 "=r"(r.w[4]), "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<16> ld_bcast<16>(const void* p) {
+  Raw<16> r;
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+               : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<8> ld_bcast<8>(const void* p) {
+  Raw<8> r;
+  asm volatile("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<4> ld_bcast<4>(const void* p) {
+  Raw<4> r;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
+  return r;
+}
+template <>
+__device__ __forceinline__ Raw<2> ld_bcast<2>(const void* p) {
+  Raw<2> r;
+  asm volatile("ld.global.nc.b16 %0, [%1];" : "=h"(r.h) : "l"(p));
+  return r;
+}
+
+template <>
+__device__ __forceinline__ void st_stream<32>(void* p, const Raw<32>& v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+               "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]),
+               "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void st_stream<16>(void* p, const Raw<16>& v) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void st_stream<8>(void* p, const Raw<8>& v) {
+  asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void st_stream<4>(void* p, const Raw<4>& v) {
+  asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(v.w[0]) : "memory");
+}
+template <>
+__device__ __forceinline__ void st_stream<2>(void* p, const Raw<2>& v) {
+  asm volatile("st.global.b16 [%0], %1;" ::"l"(p), "h"(v.h) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// dtype conversion
+// ---------------------------------------------------------------------------
+
+template <class T, int VB>
+struct Vec;
+
+// bf16: a 32-bit word holds two elements, the lower address in the low half.
+template <int VB>
+struct Vec<__nv_bfloat16, VB> {
+  static constexpr int N = VB / 2;
+  __device__ __forceinline__ static void widen(const Raw<VB>& r, float (&f)[N]) {
+#pragma unroll
+    for (int i = 0; i < VB / 4; ++i) {
+      f[2 * i] = __uint_as_float(r.w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(r.w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ static Raw<VB> narrow(const float (&f)[N]) {
+    Raw<VB> r;
+#pragma unroll
+    for (int i = 0; i < VB / 4; ++i) {
+      __nv_bfloat162 p = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      r.w[i] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    return r;
+  }
+};
+template <>
+struct Vec<__nv_bfloat16, 2> {
+  static constexpr int N = 1;
+  __device__ __forceinline__ static void widen(const Raw<2>& r, float (&f)[1]) {
+    f[0] = __uint_as_float(static_cast<uint32_t>(r.h) << 16);
+  }
+  __device__ __forceinline__ static Raw<2> narrow(const float (&f)[1]) {
+    Raw<2> r;
+    r.h = __bfloat16_as_ushort(__float2bfloat16_rn(f[0]));
+    return r;
+  }
+};
+
+template <int VB>
+struct Vec<__half, VB> {
+  static constexpr int N = VB / 2;
+  __device__ __forceinline__ static void widen(const Raw<VB>& r, float (&f)[N]) {
+#pragma unroll
+    for (int i = 0; i < VB / 4; ++i) {
+      uint32_t w = r.w[i];
+      float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w));
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+  __device__ __forceinline__ static Raw<VB> narrow(const float (&f)[N]) {
+    Raw<VB> r;
+#pragma unroll
+    for (int i = 0; i < VB / 4; ++i) {
+      __half2 p = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      r.w[i] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    return r;
+  }
+};
+template <>
+struct Vec<__half, 2> {
+  static constexpr int N = 1;
+  __device__ __forceinline__ static void widen(const Raw<2>& r, float (&f)[1]) {
+    f[0] = __half2float(__ushort_as_half(r.h));
+  }
+  __device__ __forceinline__ static Raw<2> narrow(const float (&f)[1]) {
+    Raw<2> r;
+    r.h = __half_as_ushort(__float2half_rn(f[0]));
+    return r;
+  }
+};
+
+template <int VB>
+struct Vec<float, VB> {
+  static constexpr int N = VB / 4;
+  __device__ __forceinline__ static void widen(const Raw<VB>& r, float (&f)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) f[i] = __uint_as_float(r.w[i]);
+  }
+  __device__ __forceinline__ static Raw<VB> narrow(const float (&f)[N]) {
+    Raw<VB> r;
+#pragma unroll
+    for (int i = 0; i < N; ++i) r.w[i] = __float_as_uint(f[i]);
+    return r;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// the arithmetic of the two operations (explicit roundings: no contraction)
+// ---------------------------------------------------------------------------
+
+// hidden + update * gate: product rounded, then sum rounded.
+__device__ __forceinline__ float residual_gate(float h, float u, float g) {
+  return __fadd_rn(h, __fmul_rn(u, g));
+}
+
+// n * (1 + scale) + shift with n = x * r, left to right, each op rounded.
+__device__ __forceinline__ float modulate(float x, float r, float s, float h) {
+  const float n = __fmul_rn(x, r);
+  const float one = __fadd_rn(1.0f, s);
+  return __fadd_rn(__fmul_rn(n, one), h);
+}
+
+// 1 / sqrt(mean + eps) for the row's fp32 sum of squares over D elements:
+// the mean is the correctly rounded fp32 quotient (D < 2^24 is exact in fp32;
+// larger D divides in fp64), the root the correctly rounded fp32 inverse
+// square root.
+__device__ __forceinline__ float rms_inverse(float sumsq, int64_t D, float eps) {
+  const float ms =
+      D < (int64_t(1) << 24)
+          ? __fdiv_rn(sumsq, static_cast<float>(D))
+          : static_cast<float>(static_cast<double>(sumsq) / static_cast<double>(D));
+  return __frsqrt_rn(__fadd_rn(ms, eps));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+}  // namespace dit

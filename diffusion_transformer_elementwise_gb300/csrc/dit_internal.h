@@ -1,0 +1,127 @@
+// dit_internal.h -- host-side interface between the C ABI (dit_api.cu) and
+// the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace dit {
+
+enum Op { OP_RGA = 0, OP_MOD = 1, OP_FUSED = 2 };
+
+// Arguments of the flat (full-gate) residual-gate kernel.  Elements
+// [0, n_head) and the n_tail elements after the vector body are handled one
+// at a time; the body is n_vec vectors of the kernel's width.
+struct FlatArgs {
+  void* out;
+  const void* h;
+  const void* u;
+  const void* g;
+  int64_t n_head;
+  int64_t n_vec;
+  int64_t n_tail;
+};
+
+// Arguments of the row kernels.  Pointers are the tensors of the call; each
+// kernel reads only those its operation uses.
+struct RowArgs {
+  void* out;          // residual gate: out; modulation: out; fused: residual_out
+  void* out2;         // fused: modulated_out
+  const void* x;      // residual gate / fused: hidden; modulation: x
+  const void* u;      // update
+  const void* g;      // gate
+  const void* sc;     // scale
+  const void* sh;     // shift
+  int64_t L;          // rows per batch
+  int64_t D;          // elements per row
+  int64_t rows;       // B * L
+  int64_t rows_per_chunk;
+  int64_t chunks_per_batch;
+  int64_t nvec;       // vectors of the kernel's width per row
+  float eps;
+};
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+};
+
+// The current device's SM count, cached per device.
+cudaError_t current_device(DeviceInfo* info);
+// How many CTAs of `fn` at `block` threads are resident per SM (cached).
+int resident_ctas(const DeviceInfo& dev, const void* fn, int block);
+
+// Grid of the row kernels: (batch, row chunk) pairs on x, column slices on
+// y.  Chunks never straddle a batch, so a CTA loads its [B, 1, D] vectors
+// once.  Sized to one wave of resident CTAs.
+struct RowPlan {
+  dim3 grid;
+  dim3 block;
+  int64_t rows_per_chunk;
+  int64_t chunks_per_batch;
+};
+bool plan_rows(const DeviceInfo& dev, const void* fn, int block, int64_t B,
+               int64_t L, unsigned col_slices, RowPlan* plan);
+
+// Widest power-of-two access (<= 32 bytes) that divides every address and
+// byte pitch in `bits` (the OR of them all).
+inline int widest_access(uint64_t bits) {
+  int vb = 32;
+  while (vb > 1 && (bits & (uint64_t)(vb - 1))) vb >>= 1;
+  return vb;
+}
+
+// Launchers, one per operation family (defined in k_*.cu).  dtype is a
+// dit_dtype value, vb the access width in bytes.
+cudaError_t launch_rga_full(const DeviceInfo& dev, int dtype, void* out,
+                            const void* h, const void* u, const void* g,
+                            int64_t n, cudaStream_t stream);
+cudaError_t launch_rga_bcast(const DeviceInfo& dev, int dtype, int vb,
+                             const RowArgs& a, int64_t B, cudaStream_t stream);
+cudaError_t launch_modulate(const DeviceInfo& dev, int dtype, int vb,
+                            bool mod_full, const RowArgs& a, int64_t B,
+                            cudaStream_t stream);
+cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb,
+                         bool gate_full, bool mod_full, const RowArgs& a,
+                         int64_t B, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// compile-time dispatch over (dtype, access width)
+// ---------------------------------------------------------------------------
+template <class T>
+struct TypeTag {
+  using type = T;
+};
+template <int V>
+using Width = std::integral_constant<int, V>;
+
+template <class T, class Fn>
+cudaError_t dispatch_width(int vb, Fn&& fn) {
+  switch (vb) {
+    case 32: return fn(TypeTag<T>{}, Width<32>{});
+    case 16: return fn(TypeTag<T>{}, Width<16>{});
+    case 8:  return fn(TypeTag<T>{}, Width<8>{});
+    case 4:  return fn(TypeTag<T>{}, Width<4>{});
+    case 2:
+      if constexpr (sizeof(T) == 2) return fn(TypeTag<T>{}, Width<2>{});
+      return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class Fn>
+cudaError_t dispatch_dtype_width(int dtype, int vb, Fn&& fn) {
+  switch (dtype) {
+    case 0: return dispatch_width<__nv_bfloat16>(vb, fn);
+    case 1: return dispatch_width<__half>(vb, fn);
+    case 2: return dispatch_width<float>(vb, fn);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dit

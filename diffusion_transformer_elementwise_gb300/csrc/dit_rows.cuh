@@ -1,0 +1,321 @@
+// dit_rows.cuh -- row-tiled kernels for the residual gate with a [B, 1, D]
+// gate, the adaLN RMSNorm-modulation and the fused op.
+//
+// Tiling.  A CTA owns a run of consecutive rows of one batch (so each
+// [B, 1, D] vector is loaded once per CTA, into registers, and reused for all
+// its rows, with no per-element index arithmetic) and a column slice of
+// blockDim.x * 32 bytes (16 for narrow accesses).  Thread t owns the 32/VB
+// (16/VB) vectors of VB bytes at
+// vector indices col0 + t + k * blockDim.x: each warp-wide access is
+// contiguous.  R rows are in flight per thread (R * 32 bytes per streamed
+// operand), which with one wave of resident CTAs keeps enough bytes in
+// flight per SM to cover HBM latency.
+//
+// Reduction (modulation, fused).  The CTA spans the whole row (one column
+// slice).  Each thread sums x^2 over its elements in fp32, the warp reduces
+// with shuffles, the warps' partials go through shared memory (double
+// buffered, so one __syncthreads per R rows), and every thread adds the
+// partials in the same order, so all threads hold the same sum.
+//
+// Long rows (more than kRowBlockMax threads * 32 (16) bytes) use long_row_kernel: one CTA
+// per row at a time, a first pass that accumulates the sum of squares (and,
+// for the fused op, writes the residual), and a second pass that re-reads the
+// row -- for the fused op its own residual writes -- and writes the output.
+#pragma once
+
+#include "dit_device.cuh"
+#include "dit_internal.h"
+
+namespace dit {
+
+// Bytes of a row per thread per operand: 32 for 16/32-byte accesses, 16 for
+// the narrow accesses of unaligned rows (which would otherwise need too many
+// registers for their per-vector offsets).
+template <int VB>
+__host__ __device__ constexpr int thread_bytes() {
+  return VB >= 16 ? 32 : 16;
+}
+
+constexpr int kRowBlockMax = 512;  // threads; rows up to 16 KB stay in registers
+
+template <int OP, class T, int VB, int R, bool GFULL, bool MFULL>
+__global__ void __launch_bounds__(kRowBlockMax) row_kernel(RowArgs a) {
+  using V = Vec<T, VB>;
+  constexpr int N = V::N;
+  constexpr int VPT = thread_bytes<VB>() / VB;
+  constexpr bool kReduce = OP != OP_RGA;
+  constexpr bool kHasGate = OP != OP_MOD;
+
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int64_t b = blockIdx.x / a.chunks_per_batch;
+  const int64_t chunk = blockIdx.x - b * a.chunks_per_batch;
+  const int64_t r_begin = b * a.L + chunk * a.rows_per_chunk;
+  const int64_t r_stop = (b + 1) * a.L;
+  const int64_t r_end = r_begin + a.rows_per_chunk < r_stop ? r_begin + a.rows_per_chunk : r_stop;
+  if (r_begin >= r_end) return;  // uniform over the CTA
+
+  const int64_t pitch = a.D * (int64_t)sizeof(T);
+  const int64_t col0 = (int64_t)blockIdx.y * nthr * VPT;
+  int64_t coff[VPT];
+  bool cval[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int64_t cv = col0 + tid + (int64_t)k * nthr;
+    cval[k] = cv < a.nvec;
+    coff[k] = cv * VB;
+  }
+
+  // [B, 1, D] operands: loaded once for batch b.
+  Raw<VB> gb[VPT], scb[VPT], shb[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    if (!cval[k]) continue;
+    if constexpr (kHasGate && !GFULL) gb[k] = ld_bcast<VB>((const char*)a.g + b * pitch + coff[k]);
+    if constexpr (kReduce && !MFULL) {
+      scb[k] = ld_bcast<VB>((const char*)a.sc + b * pitch + coff[k]);
+      shb[k] = ld_bcast<VB>((const char*)a.sh + b * pitch + coff[k]);
+    }
+  }
+
+  __shared__ float part[2][R][32];
+  int buf = 0;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = nthr >> 5;
+
+  for (int64_t r0 = r_begin; r0 < r_end; r0 += R) {
+    Raw<VB> xv[R][VPT], uv[R][VPT], gv[R][VPT], scv[R][VPT], shv[R][VPT];
+    bool rval[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      rval[j] = r0 + j < r_end;
+      const int64_t rowoff = (r0 + j) * pitch;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!(rval[j] && cval[k])) continue;
+        const int64_t off = rowoff + coff[k];
+        xv[j][k] = ld_stream<VB>((const char*)a.x + off);
+        if constexpr (kHasGate) uv[j][k] = ld_stream<VB>((const char*)a.u + off);
+        if constexpr (kHasGate && GFULL) gv[j][k] = ld_stream<VB>((const char*)a.g + off);
+        if constexpr (kReduce && MFULL) {
+          scv[j][k] = ld_stream<VB>((const char*)a.sc + off);
+          shv[j][k] = ld_stream<VB>((const char*)a.sh + off);
+        }
+      }
+    }
+
+    float ss[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      ss[j] = 0.0f;
+      const int64_t rowoff = (r0 + j) * pitch;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!(rval[j] && cval[k])) continue;
+        float f[N];
+        if constexpr (kHasGate) {
+          float h[N], u[N], g[N];
+          V::widen(xv[j][k], h);
+          V::widen(uv[j][k], u);
+          V::widen(GFULL ? gv[j][k] : gb[k], g);
+#pragma unroll
+          for (int e = 0; e < N; ++e) f[e] = residual_gate(h[e], u[e], g[e]);
+          xv[j][k] = V::narrow(f);  // the residual as stored
+          st_stream<VB>((char*)a.out + rowoff + coff[k], xv[j][k]);
+        }
+        if constexpr (kReduce) {
+          V::widen(xv[j][k], f);
+#pragma unroll
+          for (int e = 0; e < N; ++e) ss[j] = fmaf(f[e], f[e], ss[j]);
+        }
+      }
+    }
+    if constexpr (kReduce) {
+      // sum over the row
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const float w = warp_sum(ss[j]);
+        if (lane == 0) part[buf][j][warp] = w;
+      }
+      __syncthreads();
+      float rinv[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        float tot = 0.0f;
+        for (int w = 0; w < nwarps; ++w) tot += part[buf][j][w];
+        rinv[j] = rms_inverse(tot, a.D, a.eps);
+      }
+      buf ^= 1;
+
+      void* mout = OP == OP_FUSED ? a.out2 : a.out;
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int64_t rowoff = (r0 + j) * pitch;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          if (!(rval[j] && cval[k])) continue;
+          float x[N], s[N], h[N], y[N];
+          V::widen(xv[j][k], x);
+          V::widen(MFULL ? scv[j][k] : scb[k], s);
+          V::widen(MFULL ? shv[j][k] : shb[k], h);
+#pragma unroll
+          for (int e = 0; e < N; ++e) y[e] = modulate(x[e], rinv[j], s[e], h[e]);
+          st_stream<VB>((char*)mout + rowoff + coff[k], V::narrow(y));
+        }
+      }
+    }
+  }
+}
+
+// Rows longer than one CTA can hold: two passes over each row.
+template <int OP, class T, int VB, bool GFULL, bool MFULL>
+__global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
+  using V = Vec<T, VB>;
+  constexpr int N = V::N;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = nthr >> 5;
+  const int64_t pitch = a.D * (int64_t)sizeof(T);
+  __shared__ float part[2][32];
+  int buf = 0;
+
+  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    const int64_t b = row / a.L;
+    const int64_t rowoff = row * pitch;
+    const int64_t goff = GFULL ? rowoff : b * pitch;
+    const int64_t moff = MFULL ? rowoff : b * pitch;
+    float ss = 0.0f;
+    for (int64_t v = tid; v < a.nvec; v += nthr) {
+      const int64_t c = v * VB;
+      float f[N];
+      Raw<VB> xr = ld_stream<VB>((const char*)a.x + rowoff + c);
+      if constexpr (OP == OP_FUSED) {
+        float h[N], u[N], g[N];
+        V::widen(xr, h);
+        V::widen(ld_stream<VB>((const char*)a.u + rowoff + c), u);
+        V::widen(GFULL ? ld_stream<VB>((const char*)a.g + goff + c)
+                       : ld_bcast<VB>((const char*)a.g + goff + c), g);
+#pragma unroll
+        for (int e = 0; e < N; ++e) f[e] = residual_gate(h[e], u[e], g[e]);
+        xr = V::narrow(f);
+        st_stream<VB>((char*)a.out + rowoff + c, xr);
+      }
+      V::widen(xr, f);
+#pragma unroll
+      for (int e = 0; e < N; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+    const float w = warp_sum(ss);
+    if (lane == 0) part[buf][warp] = w;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int i = 0; i < nwarps; ++i) tot += part[buf][i];
+    buf ^= 1;
+    const float rinv = rms_inverse(tot, a.D, a.eps);
+
+    // second pass: each thread re-reads exactly the vectors it handled above
+    // (for the fused op, its own residual stores)
+    const void* src = OP == OP_FUSED ? (const void*)a.out : a.x;
+    void* dst = OP == OP_FUSED ? a.out2 : a.out;
+    for (int64_t v = tid; v < a.nvec; v += nthr) {
+      const int64_t c = v * VB;
+      float x[N], s[N], h[N], y[N];
+      V::widen(ld_stream<VB>((const char*)src + rowoff + c), x);
+      if constexpr (MFULL) {
+        V::widen(ld_stream<VB>((const char*)a.sc + moff + c), s);
+        V::widen(ld_stream<VB>((const char*)a.sh + moff + c), h);
+      } else {
+        V::widen(ld_bcast<VB>((const char*)a.sc + moff + c), s);
+        V::widen(ld_bcast<VB>((const char*)a.sh + moff + c), h);
+      }
+#pragma unroll
+      for (int e = 0; e < N; ++e) y[e] = modulate(x[e], rinv, s[e], h[e]);
+      st_stream<VB>((char*)dst + rowoff + c, V::narrow(y));
+    }
+  }
+}
+
+// Rows per thread group by operation and layout: R * (streamed operands)
+// * 32 bytes stays near 128 bytes in flight per thread.
+// Narrow accesses (one or a few elements each) halve it: they need a
+// register per access, and the tail shapes that use them are not the ones
+// that set the bandwidth.
+template <int OP, bool GFULL, bool MFULL, int VB>
+__host__ __device__ constexpr int rows_in_flight() {
+  const int r = OP == OP_RGA ? 2 : OP == OP_MOD ? (MFULL ? 2 : 4) : ((GFULL || MFULL) ? 1 : 2);
+  return VB >= 16 ? r : (r > 1 ? r / 2 : 1);
+}
+
+// Two-pass kernel for rows that do not fit one CTA's registers.
+template <int OP, bool GFULL, bool MFULL>
+cudaError_t launch_long_rows(const DeviceInfo& dev, int dtype, int vb, RowArgs a,
+                             cudaStream_t stream) {
+  const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
+  // 16-byte accesses when the rows allow them, else one element at a time
+  const int lvb = vb >= 16 ? 16 : (dtype == 2 ? 4 : 2);
+  a.nvec = row_bytes / lvb;
+  return dispatch_dtype_width(dtype, lvb, [&](auto tt, auto w) -> cudaError_t {
+    using T = typename decltype(tt)::type;
+    constexpr int VB = decltype(w)::value;
+    if constexpr (VB == 16 || VB == (int)sizeof(T)) {
+      const void* fn = (const void*)long_row_kernel<OP, T, VB, GFULL, MFULL>;
+      const int block = 1024;
+      int64_t grid = (int64_t)dev.sm_count * resident_ctas(dev, fn, block);
+      if (grid > a.rows) grid = a.rows;
+      if (grid < 1) grid = 1;
+      long_row_kernel<OP, T, VB, GFULL, MFULL><<<(unsigned)grid, block, 0, stream>>>(a);
+      return cudaGetLastError();
+    } else {
+      return cudaErrorInvalidValue;
+    }
+  });
+}
+
+// Launch one row-kernel instantiation (rows that fit) or the two-pass kernel.
+template <int OP, bool GFULL, bool MFULL>
+cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, int64_t B,
+                          cudaStream_t stream) {
+  const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
+  a.nvec = row_bytes / vb;
+  bool too_long = false;
+  const cudaError_t e = dispatch_dtype_width(dtype, vb, [&](auto tt, auto w) -> cudaError_t {
+    using T = typename decltype(tt)::type;
+    constexpr int VB = decltype(w)::value;
+    constexpr int TB = thread_bytes<VB>();
+    constexpr int R = rows_in_flight<OP, GFULL, MFULL, VB>();
+    const int64_t threads_needed = (row_bytes + TB - 1) / TB;
+    const void* fn = (const void*)row_kernel<OP, T, VB, R, GFULL, MFULL>;
+    int block;
+    unsigned slices = 1;
+    if (OP == OP_RGA) {
+      block = (int)(threads_needed < 256 ? threads_needed : 256);
+      block = (block + 31) / 32 * 32;
+      const int64_t per_cta = (int64_t)block * (TB / VB);
+      const int64_t s = (a.nvec + per_cta - 1) / per_cta;
+      if (s > 65535) return cudaErrorInvalidConfiguration;
+      slices = (unsigned)s;
+    } else {
+      if (threads_needed > kRowBlockMax) {
+        too_long = true;
+        return cudaSuccess;
+      }
+      block = (int)((threads_needed + 31) / 32 * 32);
+    }
+    RowPlan plan;
+    if (!plan_rows(dev, fn, block, B, a.L, slices, &plan)) return cudaErrorInvalidConfiguration;
+    a.rows_per_chunk = plan.rows_per_chunk;
+    a.chunks_per_batch = plan.chunks_per_batch;
+    row_kernel<OP, T, VB, R, GFULL, MFULL><<<plan.grid, plan.block, 0, stream>>>(a);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess || !too_long) return e;
+  if constexpr (OP == OP_RGA) {
+    return cudaErrorInvalidValue;  // unreachable: the residual gate tiles columns
+  } else {
+    return launch_long_rows<OP, GFULL, MFULL>(dev, dtype, vb, a, stream);
+  }
+}
+
+}  // namespace dit

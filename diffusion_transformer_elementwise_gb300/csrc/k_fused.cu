@@ -1,0 +1,23 @@
+// k_fused.cu -- residual gate and RMSNorm-modulation in one pass on GB300.
+//
+// residual_out = hidden + update * gate (sglang PR #29361, Motivation), then
+// modulated_out = rms_norm(residual_out, eps) * (1 + scale) + shift (prhub
+// summary of sglang PR #34172, "key source snippet"), the statistic taken
+// over the residual as stored.  The rounded residual stays in registers
+// between the store and the modulation, so the row is read from HBM once
+// (hidden, update, gate) and written twice (residual, modulated input).
+// Kernels: dit_rows.cuh (OP_FUSED).
+#include "dit_rows.cuh"
+
+namespace dit {
+
+cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb, bool gate_full,
+                         bool mod_full, const RowArgs& a, int64_t B, cudaStream_t stream) {
+  if (gate_full)
+    return mod_full ? launch_row_op<OP_FUSED, true, true>(dev, dtype, vb, a, B, stream)
+                    : launch_row_op<OP_FUSED, true, false>(dev, dtype, vb, a, B, stream);
+  return mod_full ? launch_row_op<OP_FUSED, false, true>(dev, dtype, vb, a, B, stream)
+                  : launch_row_op<OP_FUSED, false, false>(dev, dtype, vb, a, B, stream);
+}
+
+}  // namespace dit

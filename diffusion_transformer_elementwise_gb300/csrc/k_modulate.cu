@@ -1,0 +1,22 @@
+// k_modulate.cu -- out = rms_norm(x, eps) * (1 + scale) + shift on GB300.
+//
+// Operation: prhub summary of sglang PR #34172 (LTX-2 quality=high fused
+// RMSNorm+modulate), section "key source snippet" (the expression of
+// _ltx2_rms_norm_modulate) and section "implementation breakdown", item 2
+// (weightless RMSNormNoWeight, the whole expression in one launch).
+//
+// One pass over x: each row is held in registers while its fp32 sum of
+// squares is reduced across the CTA, then normalised, modulated and written.
+// [B, 1, D] scale and shift are loaded once per CTA; [B, L, D] ones are
+// streamed with the row.  Kernels: dit_rows.cuh (OP_MOD).
+#include "dit_rows.cuh"
+
+namespace dit {
+
+cudaError_t launch_modulate(const DeviceInfo& dev, int dtype, int vb, bool mod_full,
+                            const RowArgs& a, int64_t B, cudaStream_t stream) {
+  return mod_full ? launch_row_op<OP_MOD, false, true>(dev, dtype, vb, a, B, stream)
+                  : launch_row_op<OP_MOD, false, false>(dev, dtype, vb, a, B, stream);
+}
+
+}  // namespace dit

@@ -1,0 +1,151 @@
+/*
+ * dit_elementwise.h -- C ABI of libdit_elementwise.so, the GB300 (sm_103a)
+ * kernels for the memory-bound elementwise hot path of LTX-2-style video
+ * diffusion transformers.
+ *
+ * Three operations, each one kernel launch on the caller's stream:
+ *
+ *   dit_residual_gate_add          out = hidden + update * gate
+ *   dit_rmsnorm_modulate           out = rms_norm(x, eps) * (1 + scale) + shift
+ *   dit_gate_add_rmsnorm_modulate  both in one pass: writes the new residual
+ *                                  and the modulated input of the next site
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors.  Every tensor is contiguous, row-major [B, L, D] in device memory
+ *   (or memory the device can address), all of one dtype.  A "row" is one
+ *   (b, l) pair of D elements.  An operand of layout DIT_ROW_BCAST has shape
+ *   [B, 1, D]: its row b is used for all L rows of batch b.
+ * Arithmetic.  Every element is loaded exactly into fp32, computed with IEEE
+ *   fp32 operations (round to nearest even, no fused multiply-add where the
+ *   formula below writes two operations, no flush of subnormals) and rounded
+ *   once to the output dtype (round to nearest even; overflow gives +-inf;
+ *   NaN propagates).
+ * Ownership.  The caller owns all memory.  The library allocates nothing,
+ *   keeps no per-call state and never synchronises: each call validates its
+ *   arguments on the host, enqueues one kernel on `stream` (0 = the legacy
+ *   default stream) and returns.  Outputs are complete once the stream
+ *   reaches that point.
+ * Aliasing.  out == hidden (exactly the same pointer) is allowed, as is
+ *   residual_out == hidden; any other overlap between an output and another
+ *   tensor returns DIT_ERR_ALIAS.
+ * Alignment.  Pointers must be aligned to the element size (2 bytes for
+ *   bf16/fp16, 4 for fp32); otherwise DIT_ERR_MISALIGNED.  Any such pointer
+ *   is accepted: the widest vector access that every pointer and the row
+ *   pitch D * element_size allow is chosen per call (up to 32 bytes).
+ * Errors.  Argument errors are returned before any launch and leave outputs
+ *   untouched.  B, L, D >= 0; a call with B * L * D == 0 returns DIT_OK and
+ *   launches nothing.  A launch failure reported by the CUDA runtime returns
+ *   DIT_ERR_LAUNCH; faults during execution surface at the caller's next
+ *   synchronisation, as for any CUDA kernel.  There is no fallback path.
+ * Threads.  Entry points may be called from several host threads; the only
+ *   shared state is a per-device cache of launch limits, filled on first use.
+ */
+#ifndef DIT_ELEMENTWISE_H
+#define DIT_ELEMENTWISE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The stream type of the CUDA runtime, without requiring its headers. */
+typedef struct CUstream_st* dit_stream_t;
+
+typedef enum { DIT_BF16 = 0, DIT_FP16 = 1, DIT_FP32 = 2 } dit_dtype;
+
+typedef enum {
+  DIT_FULL = 0,      /* [B, L, D]: one value per element            */
+  DIT_ROW_BCAST = 1  /* [B, 1, D]: one vector per batch, reused over L */
+} dit_layout;
+
+typedef enum {
+  DIT_OK = 0,
+  DIT_ERR_NULL_PTR = 1,     /* a tensor pointer is NULL while B*L*D > 0      */
+  DIT_ERR_BAD_SHAPE = 2,    /* B, L or D negative, or B*L*D overflows         */
+  DIT_ERR_BAD_DTYPE = 3,    /* dtype is not a dit_dtype value                 */
+  DIT_ERR_BAD_LAYOUT = 4,   /* layout is not a dit_layout value               */
+  DIT_ERR_ALIAS = 5,        /* an output overlaps another tensor (other than
+                               the allowed out == hidden)                     */
+  DIT_ERR_BAD_EPS = 6,      /* eps is negative, infinite or NaN               */
+  DIT_ERR_LAUNCH = 7,       /* the CUDA runtime rejected the launch           */
+  DIT_ERR_MISALIGNED = 8,   /* a pointer is not aligned to the element size   */
+  DIT_ERR_NO_DEVICE = 9     /* no current CUDA device could be queried        */
+} dit_status;
+
+/* Version of this interface; bumped on any incompatible change. */
+#define DIT_ABI_VERSION 1
+int dit_abi_version(void);
+
+/* A static, human-readable name for a status code. */
+const char* dit_status_string(dit_status status);
+
+/*
+ * Gated residual update:  out[b,l,d] = hidden[b,l,d] + update[b,l,d] * G
+ * with G = gate[b,l,d] (gate_layout DIT_FULL) or gate[b,0,d] (DIT_ROW_BCAST),
+ * evaluated as p = fl32(update * G), s = fl32(hidden + p), out = rnd(s).
+ *
+ * Source: sglang PR #29361 "Add diffusion residual-gate CUDA fast path for
+ * LTX2", section Motivation (the hot pattern hidden + update * gate for
+ * contiguous [B, L, D] tensors with a full gate or a [B, 1, D] gate) and
+ * section Modifications (full and row-broadcast gates, dtype coverage, tail
+ * shapes, rejection of unsupported inputs).
+ *
+ * out, hidden, update: [B, L, D].  gate: [B, L, D] or [B, 1, D].
+ * out may be hidden (in-place update).
+ */
+dit_status dit_residual_gate_add(void* out, const void* hidden,
+                                 const void* update, const void* gate,
+                                 int64_t B, int64_t L, int64_t D,
+                                 dit_dtype dtype, dit_layout gate_layout,
+                                 dit_stream_t stream);
+
+/*
+ * adaLN modulation with a weightless RMSNorm over each row:
+ *   r   = 1 / sqrt(mean_d(x[b,l,d]^2) + eps)     (fp32 statistic per row)
+ *   out = rnd(fl32(fl32(fl32(x * r) * fl32(1 + S)) + H))
+ * with S, H = scale, shift at [b,l,d] (mod_layout DIT_FULL) or [b,0,d]
+ * (DIT_ROW_BCAST).  The mean square is accumulated in fp32 (tree order) and
+ * r is the correctly rounded fp32 inverse root of fl32(mean + eps).
+ *
+ * Source: prhub summary of sglang PR #34172 (LTX-2 quality=high fused
+ * RMSNorm+modulate), section "key source snippet" (the eager expression
+ * rms_norm(x, eps) * (1 + scale) + shift of _ltx2_rms_norm_modulate, called
+ * with the block's norm_eps) and section "implementation breakdown", item 2
+ * (RMSNormNoWeight: the norm has no weight; one launch for the whole
+ * expression).
+ *
+ * out, x: [B, L, D].  scale, shift: [B, L, D] or [B, 1, D].  eps >= 0.
+ */
+dit_status dit_rmsnorm_modulate(void* out, const void* x, const void* scale,
+                                const void* shift, int64_t B, int64_t L,
+                                int64_t D, float eps, dit_dtype dtype,
+                                dit_layout mod_layout, dit_stream_t stream);
+
+/*
+ * Fused residual gate + modulation, one pass over the rows:
+ *   residual_out = dit_residual_gate_add(hidden, update, gate)   (stored)
+ *   modulated_out = dit_rmsnorm_modulate(residual_out, scale, shift, eps)
+ * The statistic is taken over the residual as stored (rounded to the dtype),
+ * so the two outputs are bitwise those of the two separate calls.  The
+ * residual is never re-read from memory.
+ *
+ * Source: the two operations above; the pages name the fused family member
+ * (fused_gate_rmsnorm, prhub summary of sglang PR #34172, "implementation
+ * breakdown" items 2 and 4) without describing it.
+ *
+ * residual_out, modulated_out, hidden, update: [B, L, D].
+ * gate: per gate_layout.  scale, shift: per mod_layout.
+ * residual_out may be hidden; modulated_out may not alias anything.
+ */
+dit_status dit_gate_add_rmsnorm_modulate(
+    void* residual_out, void* modulated_out, const void* hidden,
+    const void* update, const void* gate, const void* scale, const void* shift,
+    int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+    dit_layout gate_layout, dit_layout mod_layout, dit_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DIT_ELEMENTWISE_H */

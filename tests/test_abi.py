@@ -1,0 +1,133 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/dit_elementwise.h declares, and rejects bad arguments with the
+documented status before touching the device.  Pointers here are plain
+integers that are never dereferenced: validation happens on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from diffusion_transformer_elementwise_gb300 import library
+from diffusion_transformer_elementwise_gb300.build import build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
+                      "dit_elementwise.h")
+
+OK, NULLP, SHAPE, DTYPE, LAYOUT, ALIAS, EPS, LAUNCH, MISALIGNED, NODEV = range(10)
+BF16, FP16, FP32 = 0, 1, 2
+FULL, BCAST = 0, 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dit_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"dit_residual_gate_add", "dit_rmsnorm_modulate",
+            "dit_gate_add_rmsnorm_modulate", "dit_status_string",
+            "dit_abi_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    m = re.search(r"#define DIT_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.dit_abi_version() == int(m.group(1))
+    seen = set()
+    for code in range(10):
+        s = lib.dit_status_string(code).decode()
+        assert s.startswith("DIT_") and s not in seen
+        seen.add(s)
+    assert lib.dit_status_string(99).decode() == "unknown dit_status"
+
+
+A = 1 << 20  # fake, well-separated, 256-byte aligned "device" addresses
+H, U, G, O, O2, S, SH = (A * k for k in range(1, 8))
+
+
+def rga(lib, out=O, h=H, u=U, g=G, B=1, L=4, D=8, dt=BF16, lay=FULL):
+    return lib.dit_residual_gate_add(out, h, u, g, B, L, D, dt, lay, None)
+
+
+def mod(lib, out=O, x=H, s=S, sh=SH, B=1, L=4, D=8, eps=1e-6, dt=BF16, lay=BCAST):
+    return lib.dit_rmsnorm_modulate(out, x, s, sh, B, L, D, eps, dt, lay, None)
+
+
+def fused(lib, r=O, m=O2, h=H, u=U, g=G, s=S, sh=SH, B=1, L=4, D=8, eps=1e-6, dt=BF16,
+          gl=BCAST, ml=BCAST):
+    return lib.dit_gate_add_rmsnorm_modulate(r, m, h, u, g, s, sh, B, L, D, eps, dt, gl, ml,
+                                             None)
+
+
+def test_bad_dtype_layout_shape(lib):
+    assert rga(lib, dt=3) == DTYPE
+    assert rga(lib, lay=2) == LAYOUT
+    assert mod(lib, lay=-1) == LAYOUT
+    assert fused(lib, ml=7) == LAYOUT
+    assert rga(lib, D=-1) == SHAPE
+    assert mod(lib, B=-2) == SHAPE
+    assert fused(lib, B=1 << 40, L=1 << 40, D=4) == SHAPE  # overflows int64
+    assert rga(lib, B=1 << 31, L=1 << 31, D=1 << 2, dt=FP32) == SHAPE  # bytes overflow
+
+
+def test_bad_eps(lib):
+    for eps in (-1e-6, float("inf"), float("nan")):
+        assert mod(lib, eps=eps) == EPS
+        assert fused(lib, eps=eps) == EPS
+    assert mod(lib, eps=0.0) != EPS
+
+
+def test_empty_problems_need_no_pointers_and_no_device(lib):
+    assert rga(lib, out=None, h=None, u=None, g=None, L=0) == OK
+    assert mod(lib, out=None, x=None, s=None, sh=None, D=0) == OK
+    assert fused(lib, r=None, m=None, h=None, u=None, g=None, s=None, sh=None, B=0) == OK
+
+
+def test_null_pointers(lib):
+    assert rga(lib, g=None) == NULLP
+    assert mod(lib, sh=None) == NULLP
+    assert fused(lib, m=None) == NULLP
+
+
+def test_misaligned(lib):
+    assert rga(lib, u=U + 1) == MISALIGNED
+    assert mod(lib, x=H + 2, dt=FP32) == MISALIGNED
+    assert fused(lib, sh=SH + 3) == MISALIGNED
+    # 2-byte aligned bf16 pointers are accepted (they pass validation and only
+    # then fail for want of a device here)
+    assert rga(lib, u=U + 2) in (NODEV, LAUNCH, OK)
+
+
+def test_aliasing_rules(lib):
+    n = 1 * 4 * 8 * 2
+    assert rga(lib, out=H) in (NODEV, LAUNCH, OK)         # in place: allowed
+    assert rga(lib, out=H + 2) == ALIAS                   # partial overlap with hidden
+    assert rga(lib, out=U + n - 2) == ALIAS               # overlaps update's last element
+    assert rga(lib, out=U + n) not in (ALIAS,)            # adjacent, no overlap
+    assert rga(lib, out=G, lay=BCAST) == ALIAS
+    assert mod(lib, out=H) == ALIAS                       # modulation is not in place
+    assert mod(lib, out=S + 8) == ALIAS                   # inside the [1,1,8] scale
+    assert fused(lib, r=H) in (NODEV, LAUNCH, OK)         # residual in place: allowed
+    assert fused(lib, m=H) == ALIAS
+    assert fused(lib, r=O, m=O) == ALIAS
+    assert fused(lib, r=S) == ALIAS
+    assert fused(lib, m=G + 4) == ALIAS
+
+
+def test_valid_call_without_device_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert rga(lib) == NODEV
+    assert mod(lib) == NODEV
+    assert fused(lib) == NODEV

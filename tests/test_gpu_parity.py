@@ -1,0 +1,210 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on
+seeded inputs, element by element, at sizes the oracle finishes quickly that
+still span several CTAs, several column slices and ragged tails: every dtype,
+both layouts, odd D (3077: no vector access), D = 3076 (8-byte access for
+16-bit dtypes), long rows (two-pass kernel), misaligned sub-views, in-place
+updates, empty tensors, IEEE special values, and canaries around outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_elementwise_gb300 as dit
+from _cases import mod_inputs, oracle_fused, oracle_mod, oracle_rga, rga_inputs
+from _gpu import (assert_bit_exact, ensure_built, guarded, modulation_stats, offset_copy)
+from diffusion_transformer_elementwise_gb300.synth import TORCH_DTYPES
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["bf16", "fp16", "fp32"]
+SHAPES = [(1, 126, 2048), (2, 37, 3080), (1, 45, 3077), (1, 33, 3076), (2, 19, 4096),
+          (1, 9, 4608), (3, 5, 7), (1, 1, 1), (1, 2, 127), (2, 3, 9000), (1, 2, 20000)]
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def cuda(*ts):
+    return [t.cuda() for t in ts]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("layout", ["full", "bcast"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_residual_gate(orc, dtype, layout, shape):
+    B, L, D = shape
+    h, u, g = rga_inputs(B, L, D, dtype, layout, row_spread=True)
+    out, untouched = guarded(shape, TORCH_DTYPES[dtype], "cuda")
+    dit.residual_gate_add(*cuda(h, u, g), out=out)
+    torch.cuda.synchronize()
+    assert untouched()
+    assert_bit_exact(out, oracle_rga(orc, h, u, g, dtype, layout), f"{dtype} {layout} {shape}")
+
+
+@pytest.mark.parametrize("layout", ["full", "bcast"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_residual_gate_in_place(orc, dtype, layout):
+    B, L, D = 2, 41, 3080
+    h, u, g = rga_inputs(B, L, D, dtype, layout)
+    hd, ud, gd = cuda(h, u, g)
+    ret = dit.residual_gate_add(hd, ud, gd, out=hd)
+    torch.cuda.synchronize()
+    assert ret.data_ptr() == hd.data_ptr()
+    assert_bit_exact(hd, oracle_rga(orc, h, u, g, dtype, layout))
+
+
+@pytest.mark.parametrize("offsets", [(1, 1, 1, 1), (1, 2, 0, 3), (0, 0, 0, 1), (3, 3, 3, 3)])
+@pytest.mark.parametrize("layout", ["full", "bcast"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_residual_gate_misaligned(orc, dtype, layout, offsets):
+    """Sub-views starting 1-3 elements past an allocation boundary: same or
+    different misalignment per tensor (head/tail peel, narrow accesses)."""
+    B, L, D = 1, 29, 2048
+    h, u, g = rga_inputs(B, L, D, dtype, layout)
+    ho, uo, go = (offset_copy(t.cuda(), k) for t, k in zip((h, u, g), offsets[:3]))
+    out = offset_copy(torch.zeros_like(h).cuda(), offsets[3])
+    dit.residual_gate_add(ho, uo, go, out=out)
+    torch.cuda.synchronize()
+    assert_bit_exact(out, oracle_rga(orc, h, u, g, dtype, layout))
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("layout", ["bcast", "full"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_modulate(orc, dtype, layout, shape):
+    B, L, D = shape
+    x, sc, sh = mod_inputs(B, L, D, dtype, layout, row_spread=True)
+    out, untouched = guarded(shape, TORCH_DTYPES[dtype], "cuda")
+    dit.rmsnorm_modulate(*cuda(x, sc, sh), EPS, out=out)
+    torch.cuda.synchronize()
+    assert untouched()
+    ref, t = oracle_mod(orc, x, sc, sh, dtype, layout, EPS, with_t=True)
+    modulation_stats(out, ref, t.numpy(), dtype, f"{dtype} {layout} {shape}")
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_modulate_misaligned(orc, dtype, offset):
+    B, L, D = 2, 13, 4096
+    x, sc, sh = mod_inputs(B, L, D, dtype, "bcast")
+    xo = offset_copy(x.cuda(), offset)
+    out = offset_copy(torch.zeros_like(x).cuda(), 0)
+    dit.rmsnorm_modulate(xo, *cuda(sc, sh), EPS, out=out)
+    torch.cuda.synchronize()
+    ref, t = oracle_mod(orc, x, sc, sh, dtype, "bcast", EPS, with_t=True)
+    modulation_stats(out, ref, t.numpy(), dtype)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("gl,ml", [("bcast", "bcast"), ("full", "bcast"), ("bcast", "full"),
+                                   ("full", "full")])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_fused(orc, dtype, gl, ml, shape):
+    B, L, D = shape
+    h, u, g = rga_inputs(B, L, D, dtype, gl, tag="fz", row_spread=True)
+    _, sc, sh = mod_inputs(B, L, D, dtype, ml, tag="fz")
+    res, ok1 = guarded(shape, TORCH_DTYPES[dtype], "cuda")
+    mod, ok2 = guarded(shape, TORCH_DTYPES[dtype], "cuda")
+    dit.gate_add_rmsnorm_modulate(*cuda(h, u, g, sc, sh), EPS, residual_out=res,
+                                  modulated_out=mod)
+    torch.cuda.synchronize()
+    assert ok1() and ok2()
+    rref, mref, t = oracle_fused(orc, h, u, g, sc, sh, dtype, gl, ml, EPS, with_t=True)
+    assert_bit_exact(res, rref, f"residual {dtype} {gl}/{ml} {shape}")
+    modulation_stats(mod, mref, t.numpy(), dtype, f"modulated {dtype} {gl}/{ml} {shape}")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_fused_in_place_and_misaligned(orc, dtype):
+    B, L, D = 2, 23, 3072
+    h, u, g = rga_inputs(B, L, D, dtype, "bcast", tag="fzi")
+    _, sc, sh = mod_inputs(B, L, D, dtype, "bcast", tag="fzi")
+    rref, mref, t = oracle_fused(orc, h, u, g, sc, sh, dtype, "bcast", "bcast", EPS, with_t=True)
+    hd = h.cuda()
+    _, mod = dit.gate_add_rmsnorm_modulate(hd, *cuda(u, g, sc, sh), EPS, residual_out=hd)
+    torch.cuda.synchronize()
+    assert_bit_exact(hd, rref)
+    modulation_stats(mod, mref, t.numpy(), dtype)
+    ho = offset_copy(h.cuda(), 1)
+    res, mod = dit.gate_add_rmsnorm_modulate(ho, *cuda(u, g, sc, sh), EPS, residual_out=ho)
+    torch.cuda.synchronize()
+    assert_bit_exact(ho, rref)
+    modulation_stats(mod, mref, t.numpy(), dtype)
+
+
+@pytest.mark.parametrize("shape", [(0, 5, 8), (2, 0, 8), (2, 5, 0)])
+def test_empty_tensors_launch_nothing(shape):
+    z = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((shape[0], 1, shape[2]), dtype=torch.bfloat16, device="cuda")
+    dit.residual_gate_add(z, z.clone(), v)
+    dit.rmsnorm_modulate(z, v, v.clone())
+    dit.gate_add_rmsnorm_modulate(z, z.clone(), v, v.clone(), v.clone())
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_special_values(orc, dtype):
+    """inf, -inf, NaN, subnormals and overflow propagate as IEEE arithmetic
+    says, identically on both sides (NaN payloads aside)."""
+    B, L, D = 1, 4, 64
+    h, u, g = rga_inputs(B, L, D, dtype, "full", tag="special")
+    big = {"bf16": 3e38, "fp16": 6e4, "fp32": 3e38}[dtype]
+    tiny = {"bf16": 1e-39, "fp16": 1e-7, "fp32": 1e-44}[dtype]
+    hv = h.float()
+    hv[0, 0, :4] = torch.tensor([float("inf"), float("-inf"), float("nan"), big])
+    hv[0, 1, :3] = torch.tensor([tiny, -tiny, 0.0])
+    h = hv.to(h.dtype)
+    u = u.float()
+    u[0, 0, 3] = big
+    u = u.to(h.dtype)
+    g = g.float()
+    g[0, 0, 3] = 1.0
+    g = g.to(h.dtype)
+    out = dit.residual_gate_add(*cuda(h, u, g))
+    torch.cuda.synchronize()
+    ref = oracle_rga(orc, h, u, g, dtype, "full")
+    o, r = out.cpu().float(), ref.float()
+    assert torch.equal(torch.isnan(o), torch.isnan(r))
+    m = ~torch.isnan(r)
+    assert torch.equal(o[m], r[m])
+    # modulation: a row holding NaN is NaN throughout (its sum of squares is
+    # NaN); rows of subnormals and zeros are ordinary rows
+    _, sc, sh = mod_inputs(B, L, D, dtype, "bcast", tag="special")
+    mo = dit.rmsnorm_modulate(*cuda(h, sc, sh), EPS)
+    torch.cuda.synchronize()
+    mr, t = oracle_mod(orc, h, sc, sh, dtype, "bcast", EPS, with_t=True)
+    assert torch.isnan(mr[0, 0]).all()
+    modulation_stats(mo, mr, t.numpy(), dtype, "special values")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_zero_row_and_zero_eps(orc, dtype):
+    B, L, D = 1, 3, 256
+    x, sc, sh = mod_inputs(B, L, D, dtype, "bcast", tag="zero")
+    x[0, 1] = 0
+    for eps in (0.0, EPS):
+        out = dit.rmsnorm_modulate(*cuda(x, sc, sh), eps)
+        torch.cuda.synchronize()
+        ref, t = oracle_mod(orc, x, sc, sh, dtype, "bcast", eps, with_t=True)
+        modulation_stats(out, ref, t.numpy(), dtype, f"eps={eps}")
+
+
+def test_side_stream(orc):
+    B, L, D = 1, 300, 4096
+    h, u, g = rga_inputs(B, L, D, "bf16", "bcast", tag="stream")
+    hd, ud, gd = cuda(h, u, g)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out = dit.residual_gate_add(hd, ud, gd)
+    s.synchronize()
+    assert_bit_exact(out, oracle_rga(orc, h, u, g, "bf16", "bcast"))
+
+
+def test_cpu_tensors_are_rejected():
+    h = torch.zeros((1, 2, 8), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        dit.residual_gate_add(h, h, h)
