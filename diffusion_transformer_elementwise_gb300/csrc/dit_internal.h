@@ -70,8 +70,11 @@ bool plan_rows(const DeviceInfo& dev, const void* fn, int block, int64_t B,
 
 // Widest power-of-two access (<= 32 bytes) that divides every address and
 // byte pitch in `bits` (the OR of them all).
+#ifndef DIT_MAX_ACCESS
+#define DIT_MAX_ACCESS 32
+#endif
 inline int widest_access(uint64_t bits) {
-  int vb = 32;
+  int vb = DIT_MAX_ACCESS;
   while (vb > 1 && (bits & (uint64_t)(vb - 1))) vb >>= 1;
   return vb;
 }

@@ -38,8 +38,16 @@ __host__ __device__ constexpr int thread_bytes() {
 
 constexpr int kRowBlockMax = 512;  // threads; rows up to 16 KB stay in registers
 
+// Register budget of the row kernel: by default the launch bound alone (up to
+// 128 registers at 512 threads); DIT_ROW_MAXNREG caps it for tuning builds.
+#ifdef DIT_ROW_MAXNREG
+#define DIT_ROW_BOUNDS __maxnreg__(DIT_ROW_MAXNREG)
+#else
+#define DIT_ROW_BOUNDS __launch_bounds__(kRowBlockMax)
+#endif
+
 template <int OP, class T, int VB, int R, bool GFULL, bool MFULL>
-__global__ void __launch_bounds__(kRowBlockMax) row_kernel(RowArgs a) {
+__global__ void DIT_ROW_BOUNDS row_kernel(RowArgs a) {
   using V = Vec<T, VB>;
   constexpr int N = V::N;
   constexpr int VPT = thread_bytes<VB>() / VB;
@@ -242,9 +250,20 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
 // Narrow accesses (one or a few elements each) halve it: they need a
 // register per access, and the tail shapes that use them are not the ones
 // that set the bandwidth.
+#ifndef DIT_R_RGA
+#define DIT_R_RGA 2
+#endif
+#ifndef DIT_R_MOD
+#define DIT_R_MOD 4
+#endif
+#ifndef DIT_R_FUSED
+#define DIT_R_FUSED 2
+#endif
 template <int OP, bool GFULL, bool MFULL, int VB>
 __host__ __device__ constexpr int rows_in_flight() {
-  const int r = OP == OP_RGA ? 2 : OP == OP_MOD ? (MFULL ? 2 : 4) : ((GFULL || MFULL) ? 1 : 2);
+  const int r = OP == OP_RGA   ? DIT_R_RGA
+                : OP == OP_MOD ? (MFULL ? (DIT_R_MOD + 1) / 2 : DIT_R_MOD)
+                               : ((GFULL || MFULL) ? (DIT_R_FUSED + 1) / 2 : DIT_R_FUSED);
   return VB >= 16 ? r : (r > 1 ? r / 2 : 1);
 }
 
