@@ -17,7 +17,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];  // 0 = not yet queried
 std::mutex g_mu;
-std::map<std::tuple<int, const void*, int>, int> g_resident;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_resident;
 }  // namespace
 
 cudaError_t current_device(DeviceInfo* info) {
@@ -36,15 +36,15 @@ cudaError_t current_device(DeviceInfo* info) {
   return cudaSuccess;
 }
 
-int resident_ctas(const DeviceInfo& dev, const void* fn, int block) {
-  const auto key = std::make_tuple(dev.device, fn, block);
+int resident_ctas(const DeviceInfo& dev, const void* fn, int block, size_t smem) {
+  const auto key = std::make_tuple(dev.device, fn, block, smem);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = g_resident.find(key);
     if (it != g_resident.end()) return it->second;
   }
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, 0) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, smem) != cudaSuccess || n < 1) {
     (void)cudaGetLastError();  // the query's own error is not the caller's
     n = 1;
   }
@@ -54,8 +54,8 @@ int resident_ctas(const DeviceInfo& dev, const void* fn, int block) {
 }
 
 bool plan_rows(const DeviceInfo& dev, const void* fn, int block, int64_t B, int64_t L,
-               unsigned col_slices, RowPlan* plan) {
-  const int64_t target = (int64_t)dev.sm_count * resident_ctas(dev, fn, block);
+               unsigned col_slices, RowPlan* plan, size_t smem) {
+  const int64_t target = (int64_t)dev.sm_count * resident_ctas(dev, fn, block, smem);
   const int64_t per_chunk = B * (int64_t)col_slices;
   int64_t chunks = (target + per_chunk - 1) / per_chunk;
   if (chunks > L) chunks = L;

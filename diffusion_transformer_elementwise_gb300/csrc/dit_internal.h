@@ -53,8 +53,9 @@ struct DeviceInfo {
 
 // The current device's SM count, cached per device.
 cudaError_t current_device(DeviceInfo* info);
-// How many CTAs of `fn` at `block` threads are resident per SM (cached).
-int resident_ctas(const DeviceInfo& dev, const void* fn, int block);
+// How many CTAs of `fn` at `block` threads (and `smem` bytes of dynamic
+// shared memory) are resident per SM (cached).
+int resident_ctas(const DeviceInfo& dev, const void* fn, int block, size_t smem = 0);
 
 // Grid of the row kernels: (batch, row chunk) pairs on x, column slices on
 // y.  Chunks never straddle a batch, so a CTA loads its [B, 1, D] vectors
@@ -66,7 +67,7 @@ struct RowPlan {
   int64_t chunks_per_batch;
 };
 bool plan_rows(const DeviceInfo& dev, const void* fn, int block, int64_t B,
-               int64_t L, unsigned col_slices, RowPlan* plan);
+               int64_t L, unsigned col_slices, RowPlan* plan, size_t smem = 0);
 
 // Widest power-of-two access (<= 32 bytes) that divides every address and
 // byte pitch in `bits` (the OR of them all).

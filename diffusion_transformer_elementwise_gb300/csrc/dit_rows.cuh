@@ -25,6 +25,7 @@
 
 #include "dit_device.cuh"
 #include "dit_internal.h"
+#include "dit_pipe.cuh"
 
 namespace dit {
 
@@ -292,16 +293,30 @@ cudaError_t launch_long_rows(const DeviceInfo& dev, int dtype, int vb, RowArgs a
   });
 }
 
-// Launch one row-kernel instantiation (rows that fit) or the two-pass kernel.
+// Rows aligned to 16 bytes take the shared-memory-staged kernel (dit_pipe.cuh);
+// narrower alignments the register-resident row kernel; rows too long for
+// one CTA the two-pass kernel.
 template <int OP, bool GFULL, bool MFULL>
 cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, int64_t B,
                           cudaStream_t stream) {
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
+  if (vb >= 16) {
+    const cudaError_t e = launch_pipe<OP, GFULL, MFULL>(dev, dtype, a, B, stream);
+    if (e != cudaErrorNotSupported) return e;
+    if constexpr (OP == OP_RGA) {
+      return cudaErrorInvalidValue;  // unreachable: the residual gate tiles columns
+    } else {
+      return launch_long_rows<OP, GFULL, MFULL>(dev, dtype, vb, a, stream);
+    }
+  }
   a.nvec = row_bytes / vb;
   bool too_long = false;
   const cudaError_t e = dispatch_dtype_width(dtype, vb, [&](auto tt, auto w) -> cudaError_t {
     using T = typename decltype(tt)::type;
     constexpr int VB = decltype(w)::value;
+    if constexpr (VB >= 16) {
+      return cudaErrorInvalidValue;  // handled by the staged kernel above
+    } else {
     constexpr int TB = thread_bytes<VB>();
     constexpr int R = rows_in_flight<OP, GFULL, MFULL, VB>();
     const int64_t threads_needed = (row_bytes + TB - 1) / TB;
@@ -328,6 +343,7 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
     a.chunks_per_batch = plan.chunks_per_batch;
     row_kernel<OP, T, VB, R, GFULL, MFULL><<<plan.grid, plan.block, 0, stream>>>(a);
     return cudaGetLastError();
+    }
   });
   if (e != cudaSuccess || !too_long) return e;
   if constexpr (OP == OP_RGA) {
