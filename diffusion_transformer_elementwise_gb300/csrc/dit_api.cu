@@ -16,6 +16,7 @@ namespace dit {
 namespace {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];  // 0 = not yet queried
+int g_smem_optin[kMaxDevices];
 std::mutex g_mu;
 std::map<std::tuple<int, const void*, int, size_t>, int> g_resident;
 }  // namespace
@@ -24,15 +25,25 @@ cudaError_t current_device(DeviceInfo* info) {
   int d = -1;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
-  int c = 0;
-  if (d >= 0 && d < kMaxDevices) c = __atomic_load_n(&g_sm_count[d], __ATOMIC_ACQUIRE);
-  if (c == 0) {
+  int c = 0, optin = 0;
+  const bool cached = d >= 0 && d < kMaxDevices;
+  if (cached) {
+    c = __atomic_load_n(&g_sm_count[d], __ATOMIC_ACQUIRE);
+    optin = __atomic_load_n(&g_smem_optin[d], __ATOMIC_ACQUIRE);
+  }
+  if (c == 0 || optin == 0) {
     e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, d);
     if (e != cudaSuccess) return e;
-    if (d >= 0 && d < kMaxDevices) __atomic_store_n(&g_sm_count[d], c, __ATOMIC_RELEASE);
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    if (e != cudaSuccess) return e;
+    if (cached) {
+      __atomic_store_n(&g_smem_optin[d], optin, __ATOMIC_RELEASE);
+      __atomic_store_n(&g_sm_count[d], c, __ATOMIC_RELEASE);
+    }
   }
   info->device = d;
   info->sm_count = c > 0 ? c : 1;
+  info->smem_optin = optin;
   return cudaSuccess;
 }
 

@@ -49,9 +49,10 @@ struct RowArgs {
 struct DeviceInfo {
   int device;
   int sm_count;
+  int smem_optin;  // largest static + dynamic shared memory one CTA may use
 };
 
-// The current device's SM count, cached per device.
+// The current device's SM count and shared-memory limit, cached per device.
 cudaError_t current_device(DeviceInfo* info);
 // How many CTAs of `fn` at `block` threads (and `smem` bytes of dynamic
 // shared memory) are resident per SM (cached).

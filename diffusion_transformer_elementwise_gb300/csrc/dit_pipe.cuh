@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
 #endif
 constexpr int kPipeVPT = 2;           // 16-byte granules per thread per row
 constexpr int kPipeBlockMax = 512;    // threads: rows up to 16 KB
-constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory per CTA
+constexpr int kStaticSmemReserve = 1024;  // bytes kept for the static arrays
 
 template <int OP>
 __host__ __device__ constexpr int pipe_stages() {
@@ -271,12 +271,16 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
                           unsigned slices, size_t smem, cudaStream_t stream) {
   constexpr int RC = pipe_rows<OP>();
   auto kern = pipe_kernel<OP, T, kPipeVPT, S, RC, GFULL, MFULL>;
-  // allow the ring's dynamic shared memory (once per device)
-  static int configured[64];
-  if (dev.device < 0 || dev.device >= 64 || !configured[dev.device]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (e != cudaSuccess) return e;
-    if (dev.device >= 0 && dev.device < 64) configured[dev.device] = 1;
+  // allow the ring's dynamic shared memory: raised per device as needed
+  static size_t configured[64];
+  const bool cached = dev.device >= 0 && dev.device < 64;
+  if (smem > 48 * 1024 && (!cached || configured[dev.device] < smem)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // do not leave it for the next call to report
+      return e;
+    }
+    if (cached) configured[dev.device] = smem;
   }
   RowPlan plan;
   if (!plan_rows(dev, (const void*)kern, block, B, a.L, slices, &plan, smem))
@@ -307,9 +311,10 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
     block = (int)((threads_needed + 31) / 32 * 32);
   }
   const size_t per_stage = (size_t)RC * NS * kPipeVPT * block * 16;
+  const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
   int S = pipe_stages<OP>();
-  while (S > 2 && per_stage * S > (size_t)kSmemMax) S = S > 3 ? 3 : 2;
-  if (per_stage * S > (size_t)kSmemMax) return cudaErrorNotSupported;
+  while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;
+  if (per_stage * S > limit) return cudaErrorNotSupported;
   // instantiated stage counts: 2, 3 and the operation's default
   return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
     using T = typename decltype(tt)::type;
