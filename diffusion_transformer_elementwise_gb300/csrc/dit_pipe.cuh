@@ -274,7 +274,8 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
   // allow the ring's dynamic shared memory: raised per device as needed
   static size_t configured[64];
   const bool cached = dev.device >= 0 && dev.device < 64;
-  if (smem > 48 * 1024 && (!cached || configured[dev.device] < smem)) {
+  // (the default limit, 48 KB, covers static and dynamic shared memory together)
+  if (smem + kStaticSmemReserve > 48 * 1024 && (!cached || configured[dev.device] < smem)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();  // do not leave it for the next call to report

@@ -300,7 +300,11 @@ template <int OP, bool GFULL, bool MFULL>
 cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, int64_t B,
                           cudaStream_t stream) {
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
+#ifdef DIT_ROWS_IN_REGISTERS  // tuning builds: the register kernel for every width
+  if (false) {
+#else
   if (vb >= 16) {
+#endif
     const cudaError_t e = launch_pipe<OP, GFULL, MFULL>(dev, dtype, a, B, stream);
     if (e != cudaErrorNotSupported) return e;
     if constexpr (OP == OP_RGA) {
@@ -314,7 +318,11 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
   const cudaError_t e = dispatch_dtype_width(dtype, vb, [&](auto tt, auto w) -> cudaError_t {
     using T = typename decltype(tt)::type;
     constexpr int VB = decltype(w)::value;
+#ifdef DIT_ROWS_IN_REGISTERS
+    if constexpr (false) {
+#else
     if constexpr (VB >= 16) {
+#endif
       return cudaErrorInvalidValue;  // handled by the staged kernel above
     } else {
     constexpr int TB = thread_bytes<VB>();
