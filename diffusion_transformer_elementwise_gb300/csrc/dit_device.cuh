@@ -257,6 +257,99 @@ __device__ __forceinline__ float rms_inverse(float sumsq, int64_t D, float eps) 
   return __frsqrt_rn(__fadd_rn(ms, eps));
 }
 
+// ---------------------------------------------------------------------------
+// packed fp32 pairs (sm_100+ f32x2 arithmetic: two IEEE fp32 operations, each
+// rounded to nearest-even, per instruction)
+// ---------------------------------------------------------------------------
+struct F2 {
+  uint64_t v;
+};
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+  F2 r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(F2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(F2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return hi;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+
+// One 32-bit word of storage <-> a pair of fp32 values (bf16x2, half2), or
+// one fp32 word <-> one value.
+template <class T>
+struct Pair;
+template <>
+struct Pair<__nv_bfloat16> {
+  __device__ __forceinline__ static F2 widen(uint32_t w) {
+    return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  }
+  __device__ __forceinline__ static uint32_t narrow(F2 a) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(f2_lo(a), f2_hi(a));
+    return *reinterpret_cast<uint32_t*>(&p);
+  }
+};
+template <>
+struct Pair<__half> {
+  __device__ __forceinline__ static F2 widen(uint32_t w) {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    return f2(v.x, v.y);
+  }
+  __device__ __forceinline__ static uint32_t narrow(F2 a) {
+    __half2 p = __floats2half2_rn(f2_lo(a), f2_hi(a));
+    return *reinterpret_cast<uint32_t*>(&p);
+  }
+};
+
+// A 16-byte granule as fp32 pairs: 4 pairs of bf16/fp16, 2 pairs of fp32.
+template <class T>
+struct Granule {
+  static constexpr int P = sizeof(T) == 2 ? 4 : 2;
+  __device__ __forceinline__ static void widen(const Raw<16>& r, F2 (&f)[P]) {
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f[i] = Pair<T>::widen(r.w[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) f[i] = f2(__uint_as_float(r.w[2 * i]), __uint_as_float(r.w[2 * i + 1]));
+    }
+  }
+  __device__ __forceinline__ static Raw<16> narrow(const F2 (&f)[P]) {
+    Raw<16> r;
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) r.w[i] = Pair<T>::narrow(f[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        r.w[2 * i] = __float_as_uint(f2_lo(f[i]));
+        r.w[2 * i + 1] = __float_as_uint(f2_hi(f[i]));
+      }
+    }
+    return r;
+  }
+};
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

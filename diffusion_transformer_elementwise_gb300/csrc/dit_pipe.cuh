@@ -38,18 +38,21 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ Raw<16> lds16(const Raw<16>* p) {
+// 16-byte shared-memory access at a shared-window address
+__device__ __forceinline__ Raw<16> lds16(const Raw<16>*, uint32_t addr) {
   Raw<16> r;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
-               : "r"(smem_addr(p)));
+               : "r"(addr));
   return r;
 }
-__device__ __forceinline__ void sts16(Raw<16>* p, const Raw<16>& v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_addr(p)), "r"(v.w[0]),
-               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+__device__ __forceinline__ void sts16(uint32_t addr, const Raw<16>& v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.w[0]), "r"(v.w[1]),
+               "r"(v.w[2]), "r"(v.w[3])
                : "memory");
 }
+// an output's column pointer for granule g0
+__device__ __forceinline__ char* gp_out(void* p, int64_t g0) { return (char*)p + g0 * 16; }
 
 // Streamed operands of each operation (in ring slot order).
 template <int OP, bool GFULL, bool MFULL>
@@ -57,23 +60,53 @@ __host__ __device__ constexpr int streamed_operands() {
   return OP == OP_MOD ? (MFULL ? 3 : 1) : OP == OP_RGA ? 2 : (2 + (GFULL ? 1 : 0) + (MFULL ? 2 : 0));
 }
 
+// Sum each of RC per-lane values over the warp.  The rows are spread over
+// lane groups by exchanging halves (xor 16, then xor 8 for RC = 4) and each
+// group finishes with a butterfly, so RC rows cost about as many shuffles as
+// one.  Returns the sum of row (lane >> (5 - log2 RC)) in every lane.
+template <int RC>
+__device__ __forceinline__ float warp_sum_rows(const float (&v)[RC]) {
+  const int lane = threadIdx.x & 31;
+  float z;
+  if constexpr (RC == 1) {
+    z = v[0];
+  } else if constexpr (RC == 2) {
+    const bool hi = lane & 16;
+    const float send = hi ? v[0] : v[1];
+    const float keep = hi ? v[1] : v[0];
+    z = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+  } else {
+    static_assert(RC == 4, "rows per group: 1, 2 or 4");
+    const bool b4 = lane & 16, b3 = lane & 8;
+    const float s0 = b4 ? v[0] : v[2], s1 = b4 ? v[1] : v[3];
+    const float k0 = b4 ? v[2] : v[0], k1 = b4 ? v[3] : v[1];
+    const float w0 = k0 + __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+    const float w1 = k1 + __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+    z = (b3 ? w1 : w0) + __shfl_xor_sync(0xFFFFFFFFu, b3 ? w0 : w1, 8);
+  }
+  constexpr int first = RC == 1 ? 16 : RC == 2 ? 8 : 4;
+#pragma unroll
+  for (int o = first; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+  return z;
+}
+
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL>
 __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
-  using V = Vec<T, 16>;
-  constexpr int NE = V::N;  // elements per granule
+  using G = Granule<T>;
+  constexpr int P = G::P;  // fp32 pairs per 16-byte granule
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
   constexpr bool kReduce = OP != OP_RGA;
   constexpr bool kGate = OP != OP_MOD;
-  // ring slot index of each operand
-  constexpr int kX = 0;                                 // hidden / x
-  constexpr int kU = 1;                                 // update
-  constexpr int kG = 2;                                 // full gate
+  constexpr int kX = 0, kU = 1, kG = 2;                      // ring slots
   constexpr int kSc = (OP == OP_MOD) ? 1 : (GFULL ? 3 : 2);  // full scale
-  constexpr int kSh = kSc + 1;                          // full shift
+  constexpr int kSh = kSc + 1;                               // full shift
 
-  extern __shared__ Raw<16> ring[];  // [S][RC][NS][VPT][T]
+  extern __shared__ Raw<16> ring[];  // [S][RC][NS][VPT][T] granules
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = nthr >> 5;
 
   const int64_t b = blockIdx.x / a.chunks_per_batch;
   const int64_t chunk = blockIdx.x - b * a.chunks_per_batch;
@@ -82,152 +115,157 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
   const int64_t r_end = r_begin + a.rows_per_chunk < r_stop ? r_begin + a.rows_per_chunk : r_stop;
   if (r_begin >= r_end) return;  // uniform over the CTA
   const int64_t pitch = a.D * (int64_t)sizeof(T);
-  const int64_t col0 = (int64_t)blockIdx.y * nthr * VPT;  // column slices (residual gate)
 
-  int64_t coff[VPT];
+  // this thread's granules: t + k * T (+ the column slice of the residual gate)
+  const int64_t g0 = (int64_t)blockIdx.y * nthr * VPT + tid;
   bool cval[VPT];
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int64_t cg = col0 + tid + (int64_t)k * nthr;
-    cval[k] = cg < a.nvec;
-    coff[k] = cg * 16;
-  }
+  for (int k = 0; k < VPT; ++k) cval[k] = g0 + (int64_t)k * nthr < a.nvec;
 
-  // [B, 1, D] operands in fp32 registers
-  float gv[VPT][NE], onev[VPT][NE], shv[VPT][NE];
+  // [B, 1, D] operands, once, in fp32: gate; 1 + scale (one rounding); shift
+  F2 gv[VPT][P], onev[VPT][P], shv[VPT][P];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     if (!cval[k]) continue;
-    if constexpr (kGate && !GFULL) V::widen(ld_bcast<16>((const char*)a.g + b * pitch + coff[k]), gv[k]);
+    const int64_t off = b * pitch + (g0 + (int64_t)k * nthr) * 16;
+    if constexpr (kGate && !GFULL) G::widen(ld_bcast<16>((const char*)a.g + off), gv[k]);
     if constexpr (kReduce && !MFULL) {
-      V::widen(ld_bcast<16>((const char*)a.sc + b * pitch + coff[k]), onev[k]);
+      G::widen(ld_bcast<16>((const char*)a.sc + off), onev[k]);
 #pragma unroll
-      for (int e = 0; e < NE; ++e) onev[k][e] = __fadd_rn(1.0f, onev[k][e]);
-      V::widen(ld_bcast<16>((const char*)a.sh + b * pitch + coff[k]), shv[k]);
+      for (int i = 0; i < P; ++i) onev[k][i] = f2_add(f2(1.0f, 1.0f), onev[k][i]);
+      G::widen(ld_bcast<16>((const char*)a.sh + off), shv[k]);
     }
   }
 
-  const void* src[5] = {a.x, a.u, a.g, a.sc, a.sh};
-  const char* sptr[NS];
+  // global column pointers of the streamed operands
+  const char* gp[NS];
+  {
+    const void* src[5] = {a.x, a.u, a.g, a.sc, a.sh};
 #pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    int which = i;
-    if (OP == OP_MOD && i >= 1) which = 2 + i;       // x, scale, shift
-    if (OP == OP_FUSED && !GFULL && i >= 2) which = i + 1;  // h, u, scale, shift
-    sptr[i] = (const char*)src[which];
+    for (int i = 0; i < NS; ++i) {
+      int which = i;
+      if (OP == OP_MOD && i >= 1) which = 2 + i;              // x, scale, shift
+      if (OP == OP_FUSED && !GFULL && i >= 2) which = i + 1;  // h, u, scale, shift
+      gp[i] = (const char*)src[which] + g0 * 16;
+    }
   }
-  auto slot = [&](int stage, int j, int op, int k) -> Raw<16>* {
-    return ring + (((stage * RC + j) * NS + op) * VPT + k) * nthr + tid;
-  };
+  const int64_t kstride_g = (int64_t)nthr * 16;  // global bytes between granules k
+  // shared addresses: slot (stage, j, op, k) = base + stage*SS + j*JS + op*OS + k*KS
+  const uint32_t KS = (uint32_t)nthr * 16;
+  const uint32_t OS = VPT * KS, JS = NS * OS, SS = RC * JS;
+  const uint32_t base = smem_addr(ring) + (uint32_t)tid * 16;
 
   const int64_t ngroups = (r_end - r_begin + RC - 1) / RC;
-  auto issue = [&](int64_t grp) {
-    if (grp < ngroups) {
-      const int stage = (int)(grp % S);
+  uint32_t issue_stage = base;  // stage of the next group to issue
+  int64_t issue_row = r_begin;
+  auto issue = [&]() {
 #pragma unroll
-      for (int j = 0; j < RC; ++j) {
-        const int64_t row = r_begin + grp * RC + j;
-        if (row >= r_end) continue;
+    for (int j = 0; j < RC; ++j) {
+      const int64_t row = issue_row + j;
+      if (row < r_end) {
         const int64_t rowoff = row * pitch;
 #pragma unroll
         for (int op = 0; op < NS; ++op)
 #pragma unroll
           for (int k = 0; k < VPT; ++k)
-            if (cval[k]) cp_async16(smem_addr(slot(stage, j, op, k)), sptr[op] + rowoff + coff[k]);
+            if (cval[k])
+              cp_async16(issue_stage + j * JS + op * OS + k * KS, gp[op] + rowoff + k * kstride_g);
       }
     }
     cp_async_commit();  // possibly empty: keeps the group count uniform
+    issue_row += RC;
+    issue_stage += SS;
+    if (issue_stage == base + S * SS) issue_stage = base;
   };
 
 #pragma unroll
-  for (int s = 0; s < S - 1; ++s) issue(s);
+  for (int s = 0; s < S - 1; ++s) issue();
 
-  __shared__ float part[2][RC][16];  // per-warp partial sums (<= 16 warps)
+  __shared__ float part[2][RC][16];  // per-warp row partial sums (<= 16 warps)
   int buf = 0;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int nwarps = nthr >> 5;
+  uint32_t stage = base;
 
   for (int64_t grp = 0; grp < ngroups; ++grp) {
-    cp_async_wait<S - 2>();  // group grp has landed (for this thread's slots)
-    const int stage = (int)(grp % S);
-    // refill the stage consumed in the previous iteration
-    issue(grp + S - 1);
+    cp_async_wait<S - 2>();  // this thread's copies of group grp have landed
+    issue();                 // refill the stage consumed by the previous group
+    const int64_t row0 = r_begin + grp * RC;
 
     float ss[RC];
 #pragma unroll
     for (int j = 0; j < RC; ++j) {
       ss[j] = 0.0f;
-      const int64_t row = r_begin + grp * RC + j;
-      if (row >= r_end) continue;
-      const int64_t rowoff = row * pitch;
+      if (row0 + j >= r_end) continue;
+      const int64_t rowoff = (row0 + j) * pitch;
+      F2 acc = f2(0.0f, 0.0f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!cval[k]) continue;
-        float x[NE];
+        F2 x[P];
         if constexpr (kGate) {
-          float h[NE], u[NE], gf[NE];
-          V::widen(lds16(slot(stage, j, kX, k)), h);
-          V::widen(lds16(slot(stage, j, kU, k)), u);
-          if constexpr (GFULL) V::widen(lds16(slot(stage, j, kG, k)), gf);
+          F2 h[P], u[P], gf[P];
+          G::widen(lds16(nullptr, stage + j * JS + kX * OS + k * KS), h);
+          G::widen(lds16(nullptr, stage + j * JS + kU * OS + k * KS), u);
+          if constexpr (GFULL) G::widen(lds16(nullptr, stage + j * JS + kG * OS + k * KS), gf);
 #pragma unroll
-          for (int e = 0; e < NE; ++e) x[e] = residual_gate(h[e], u[e], GFULL ? gf[e] : gv[k][e]);
-          const Raw<16> r = V::narrow(x);
-          st_stream<16>((char*)a.out + rowoff + coff[k], r);
+          for (int i = 0; i < P; ++i) x[i] = f2_add(h[i], f2_mul(u[i], GFULL ? gf[i] : gv[k][i]));
+          const Raw<16> r = G::narrow(x);
+          st_stream<16>(gp_out(a.out, g0) + rowoff + k * kstride_g, r);
           if constexpr (kReduce) {
-            sts16(slot(stage, j, kX, k), r);  // the stored residual, for pass two
-            V::widen(r, x);
+            sts16(stage + j * JS + kX * OS + k * KS, r);  // the stored residual
+            G::widen(r, x);
           }
         } else {
-          V::widen(lds16(slot(stage, j, kX, k)), x);
+          G::widen(lds16(nullptr, stage + j * JS + kX * OS + k * KS), x);
         }
         if constexpr (kReduce) {
 #pragma unroll
-          for (int e = 0; e < NE; ++e) ss[j] = fmaf(x[e], x[e], ss[j]);
+          for (int i = 0; i < P; ++i) acc = f2_fma(x[i], x[i], acc);
         }
       }
+      if constexpr (kReduce) ss[j] = f2_lo(acc) + f2_hi(acc);
     }
+
     if constexpr (kReduce) {
-#pragma unroll
-      for (int j = 0; j < RC; ++j) {
-        const float w = warp_sum(ss[j]);
-        if (lane == 0) part[buf][j][warp] = w;
-      }
+      // row sums: warp (rows spread over lane groups), then across warps
+      const float w = warp_sum_rows<RC>(ss);
+      constexpr int group = 32 / RC;
+      if ((lane & (group - 1)) == 0) part[buf][lane / group][warp] = w;
       __syncthreads();
-      float rinv[RC];
-#pragma unroll
-      for (int j = 0; j < RC; ++j) {
-        float tot = 0.0f;
-        for (int w = 0; w < nwarps; ++w) tot += part[buf][j][w];
-        rinv[j] = rms_inverse(tot, a.D, a.eps);
-      }
+      // lane l finishes row l % RC (lane-parallel), then broadcasts
+      const int jr = lane % RC;
+      float tot = 0.0f;
+      for (int i = 0; i < nwarps; ++i) tot += part[buf][jr][i];
+      const float rl = rms_inverse(tot, a.D, a.eps);
       buf ^= 1;
       void* mout = OP == OP_FUSED ? a.out2 : a.out;
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
-        const int64_t row = r_begin + grp * RC + j;
-        if (row >= r_end) continue;
-        const int64_t rowoff = row * pitch;
+        const float r = __shfl_sync(0xFFFFFFFFu, rl, j);
+        if (row0 + j >= r_end) continue;
+        const int64_t rowoff = (row0 + j) * pitch;
+        const F2 r2 = f2(r, r);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           if (!cval[k]) continue;
-          float x[NE], y[NE];
-          V::widen(lds16(slot(stage, j, kX, k)), x);
+          F2 x[P], y[P];
+          G::widen(lds16(nullptr, stage + j * JS + kX * OS + k * KS), x);
           if constexpr (MFULL) {
-            float s[NE], h[NE];
-            V::widen(lds16(slot(stage, j, kSc, k)), s);
-            V::widen(lds16(slot(stage, j, kSh, k)), h);
+            F2 sc[P], sh[P];
+            G::widen(lds16(nullptr, stage + j * JS + kSc * OS + k * KS), sc);
+            G::widen(lds16(nullptr, stage + j * JS + kSh * OS + k * KS), sh);
 #pragma unroll
-            for (int e = 0; e < NE; ++e) y[e] = modulate(x[e], rinv[j], s[e], h[e]);
+            for (int i = 0; i < P; ++i)
+              y[i] = f2_add(f2_mul(f2_mul(x[i], r2), f2_add(f2(1.0f, 1.0f), sc[i])), sh[i]);
           } else {
 #pragma unroll
-            for (int e = 0; e < NE; ++e)
-              y[e] = __fadd_rn(__fmul_rn(__fmul_rn(x[e], rinv[j]), onev[k][e]), shv[k][e]);
+            for (int i = 0; i < P; ++i) y[i] = f2_add(f2_mul(f2_mul(x[i], r2), onev[k][i]), shv[k][i]);
           }
-          st_stream<16>((char*)mout + rowoff + coff[k], V::narrow(y));
+          st_stream<16>(gp_out(mout, g0) + rowoff + k * kstride_g, G::narrow(y));
         }
       }
     }
+    stage += SS;
+    if (stage == base + S * SS) stage = base;
   }
   cp_async_wait<0>();  // no copy may outlive the CTA's shared memory
 }
