@@ -3,7 +3,8 @@
 Each translation unit under csrc/ is compiled in parallel, then linked into
 one shared library (the CUDA runtime linked statically) at
 ``diffusion_transformer_elementwise_gb300/_lib/libdit_elementwise.so``.
-No fast-math: IEEE division, square root and denormals are kept.
+No fast-math: IEEE division, square root and denormals are kept, and no
+multiply-add pair is contracted into an FMA.
 """
 from __future__ import annotations
 
@@ -22,8 +23,10 @@ LIB = os.path.join(LIB_DIR, "libdit_elementwise.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-         "-I", INCLUDE, "-I", CSRC]
+# -fmad=false: a multiply followed by an add stays two roundings (the
+# operations' definitions); FMAs written as such (the sum of squares) remain.
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
+         "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC]
 
 
 def _nvcc() -> str:

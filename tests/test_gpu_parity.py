@@ -180,6 +180,37 @@ def test_special_values(orc, dtype):
     modulation_stats(mo, mr, t.numpy(), dtype, "special values")
 
 
+@pytest.mark.parametrize("layout", ["bcast", "full"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_modulation_rounding_order_bit_exact(orc, dtype, layout):
+    """Every row holds the same multiset of small dyadic values, so the sum of
+    squares is exact in fp32 in any order; eps = 1 - mean(x^2) makes the
+    inverse root exactly 1 on both sides.  What remains -- n = x * r,
+    1 + scale, n * (1 + scale), + shift, each rounded, then one rounding to the
+    dtype -- must then match the oracle bit for bit (a contracted
+    multiply-add, or another order, would not)."""
+    B, L, D = 2, 37, 1024
+    rng = np.random.default_rng(7)
+    base = rng.integers(-15, 16, size=D) / 16.0  # multiples of 1/16 in [-15/16, 15/16]
+    rows = np.stack([rng.permutation(base) for _ in range(B * L)]).reshape(B, L, D)
+    ms = float(np.mean(base * base))
+    eps = 1.0 - ms
+    assert np.float32(eps) == eps and 0 <= eps  # exact in fp32
+    x = torch.tensor(rows, dtype=torch.float64).to(TORCH_DTYPES[dtype])
+    assert torch.equal(x.double(), torch.tensor(rows))
+    _, sc, sh = mod_inputs(B, L, D, dtype, layout, tag="exactr")
+    out = dit.rmsnorm_modulate(*cuda(x, sc, sh), eps)
+    torch.cuda.synchronize()
+    ref = oracle_mod(orc, x, sc, sh, dtype, layout, eps)
+    assert_bit_exact(out, ref, f"{dtype} {layout}")
+    # the fused op, with hidden = x and a zero gate, must agree as well
+    z = torch.zeros((B, 1, D), dtype=x.dtype)
+    res, mod = dit.gate_add_rmsnorm_modulate(*cuda(x, x, z, sc, sh), eps)
+    torch.cuda.synchronize()
+    assert_bit_exact(res, x)
+    assert_bit_exact(mod, ref, f"fused {dtype} {layout}")
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_zero_row_and_zero_eps(orc, dtype):
     B, L, D = 1, 3, 256
