@@ -350,6 +350,27 @@ struct Granule {
   }
 };
 
+// hidden + update * gate on a pair.  For 16-bit storage the fp32 product of
+// two stored values is exact (8+8 or 11+11 significant bits), so one fused
+// multiply-add gives exactly fl(h + fl(u * g)); for fp32 storage the product
+// rounds, and the two operations are kept apart with the non-contractible
+// intrinsics.
+template <class T>
+__device__ __forceinline__ F2 residual_gate2(F2 h, F2 u, F2 g) {
+  if constexpr (sizeof(T) == 2) {
+    return f2_fma(u, g, h);
+  } else {
+    return f2(residual_gate(f2_lo(h), f2_lo(u), f2_lo(g)), residual_gate(f2_hi(h), f2_hi(u), f2_hi(g)));
+  }
+}
+
+// fl(fl(n * one) + shift) per lane with n = x * r already formed: the
+// multiply-then-add pair uses the non-contractible intrinsics.
+__device__ __forceinline__ F2 modulate2(F2 n, F2 one, F2 shift) {
+  return f2(__fadd_rn(__fmul_rn(f2_lo(n), f2_lo(one)), f2_lo(shift)),
+            __fadd_rn(__fmul_rn(f2_hi(n), f2_hi(one)), f2_hi(shift)));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
           G::widen(lds16(nullptr, stage + j * JS + kU * OS + k * KS), u);
           if constexpr (GFULL) G::widen(lds16(nullptr, stage + j * JS + kG * OS + k * KS), gf);
 #pragma unroll
-          for (int i = 0; i < P; ++i) x[i] = f2_add(h[i], f2_mul(u[i], GFULL ? gf[i] : gv[k][i]));
+          for (int i = 0; i < P; ++i) x[i] = residual_gate2<T>(h[i], u[i], GFULL ? gf[i] : gv[k][i]);
           const Raw<16> r = G::narrow(x);
           st_stream<16>(gp_out(a.out, g0) + rowoff + k * kstride_g, r);
           if constexpr (kReduce) {
@@ -255,10 +255,10 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
             G::widen(lds16(nullptr, stage + j * JS + kSh * OS + k * KS), sh);
 #pragma unroll
             for (int i = 0; i < P; ++i)
-              y[i] = f2_add(f2_mul(f2_mul(x[i], r2), f2_add(f2(1.0f, 1.0f), sc[i])), sh[i]);
+              y[i] = modulate2(f2_mul(x[i], r2), f2_add(f2(1.0f, 1.0f), sc[i]), sh[i]);
           } else {
 #pragma unroll
-            for (int i = 0; i < P; ++i) y[i] = f2_add(f2_mul(f2_mul(x[i], r2), onev[k][i]), shv[k][i]);
+            for (int i = 0; i < P; ++i) y[i] = modulate2(f2_mul(x[i], r2), onev[k][i], shv[k][i]);
           }
           st_stream<16>(gp_out(mout, g0) + rowoff + k * kstride_g, G::narrow(y));
         }
@@ -272,22 +272,22 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
 
 // Stages and rows per stage of each operation (tuning builds may override).
 #ifndef DIT_PIPE_S_RGA
-#define DIT_PIPE_S_RGA 4
+#define DIT_PIPE_S_RGA 2
 #endif
 #ifndef DIT_PIPE_RC_RGA
-#define DIT_PIPE_RC_RGA 1
+#define DIT_PIPE_RC_RGA 4
 #endif
 #ifndef DIT_PIPE_S_MOD
-#define DIT_PIPE_S_MOD 4
+#define DIT_PIPE_S_MOD 3
 #endif
 #ifndef DIT_PIPE_RC_MOD
-#define DIT_PIPE_RC_MOD 2
+#define DIT_PIPE_RC_MOD 4
 #endif
 #ifndef DIT_PIPE_S_FUSED
 #define DIT_PIPE_S_FUSED 3
 #endif
 #ifndef DIT_PIPE_RC_FUSED
-#define DIT_PIPE_RC_FUSED 2
+#define DIT_PIPE_RC_FUSED 1
 #endif
 constexpr int kPipeVPT = 2;           // 16-byte granules per thread per row
 constexpr int kPipeBlockMax = 512;    // threads: rows up to 16 KB
