@@ -171,7 +171,9 @@ class Op:
         self.sample = sample    # callable(rows) -> oracle callable for the CPU baseline
 
 
-def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16"):
+def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16", only=None):
+    """The five ops of the hot-path step, each with its own input tensors.
+    only: build just the op of that name."""
     import torch
 
     import diffusion_transformer_elementwise_gb300 as dit
@@ -179,21 +181,13 @@ def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16"):
 
     es = 2 if dtype != "fp32" else 4
     N = B * L * D
+    vb = B * D * es
 
     def act(name):
         return draw("act", (B, L, D), seed_for("bench", name), dtype, device)
 
-    g_b = draw("gate", (B, 1, D), seed_for("bench", "gate_b"), dtype, device)
-    g_f = draw("gate", (B, L, D), seed_for("bench", "gate_f"), dtype, device)
-    sc = draw("mod", (B, 1, D), seed_for("bench", "scale"), dtype, device)
-    sh = draw("mod", (B, 1, D), seed_for("bench", "shift"), dtype, device)
-    h1, u1 = act("h1"), act("u1")
-    h2, u2 = act("h2"), act("u2")
-    h3, u3 = act("h3"), act("u3")
-    x4 = act("x4")
-    h5, u5 = act("h5"), act("u5")
-    o1, o3, o4 = (torch.empty_like(h1) for _ in range(3))
-    r5, m5 = torch.empty_like(h1), torch.empty_like(h1)
+    def vec(kind, name):
+        return draw(kind, (B, 1, D), seed_for("bench", name), dtype, device)
 
     def sampler(kind, tensors, layout=None):
         def make(rows):
@@ -215,22 +209,46 @@ def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16"):
             return run
         return make
 
-    vb = B * D * es
-    return [
-        Op("rga_bcast", lambda: dit.residual_gate_add(h1, u1, g_b, out=o1),
-           3 * N * es + vb, [h1, u1, g_b], [o1], sampler("rga", [h1, u1, g_b], "bcast")),
-        Op("rga_bcast_inplace", lambda: dit.residual_gate_add(h2, u2, g_b, out=h2),
-           3 * N * es + vb, [h2, u2, g_b], [h2], sampler("rga", [h2, u2, g_b], "bcast")),
-        Op("rga_full", lambda: dit.residual_gate_add(h3, u3, g_f, out=o3),
-           4 * N * es, [h3, u3, g_f], [o3], sampler("rga", [h3, u3, g_f], "full")),
-        Op("mod_bcast", lambda: dit.rmsnorm_modulate(x4, sc, sh, EPS, out=o4),
-           2 * N * es + 2 * vb, [x4, sc, sh], [o4], sampler("mod", [x4, sc, sh])),
-        Op("fused_bcast",
-           lambda: dit.gate_add_rmsnorm_modulate(h5, u5, g_b, sc, sh, EPS, residual_out=r5,
-                                                 modulated_out=m5),
-           4 * N * es + 3 * vb, [h5, u5, g_b, sc, sh], [r5, m5],
-           sampler("fused", [h5, u5, g_b, sc, sh])),
-    ]
+    def rga_bcast():
+        h, u, g, o = act("h1"), act("u1"), vec("gate", "gate_b"), None
+        o = torch.empty_like(h)
+        return Op("rga_bcast", lambda: dit.residual_gate_add(h, u, g, out=o),
+                  3 * N * es + vb, [h, u, g], [o], sampler("rga", [h, u, g], "bcast"))
+
+    def rga_bcast_inplace():
+        h, u, g = act("h2"), act("u2"), vec("gate", "gate_b")
+        return Op("rga_bcast_inplace", lambda: dit.residual_gate_add(h, u, g, out=h),
+                  3 * N * es + vb, [h, u, g], [h], sampler("rga", [h, u, g], "bcast"))
+
+    def rga_full():
+        h, u = act("h3"), act("u3")
+        g = draw("gate", (B, L, D), seed_for("bench", "gate_f"), dtype, device)
+        o = torch.empty_like(h)
+        return Op("rga_full", lambda: dit.residual_gate_add(h, u, g, out=o),
+                  4 * N * es, [h, u, g], [o], sampler("rga", [h, u, g], "full"))
+
+    def mod_bcast():
+        x, sc, sh = act("x4"), vec("mod", "scale"), vec("mod", "shift")
+        o = torch.empty_like(x)
+        return Op("mod_bcast", lambda: dit.rmsnorm_modulate(x, sc, sh, EPS, out=o),
+                  2 * N * es + 2 * vb, [x, sc, sh], [o], sampler("mod", [x, sc, sh]))
+
+    def fused_bcast():
+        h, u = act("h5"), act("u5")
+        g, sc, sh = vec("gate", "gate_b"), vec("mod", "scale"), vec("mod", "shift")
+        r, m = torch.empty_like(h), torch.empty_like(h)
+        return Op("fused_bcast",
+                  lambda: dit.gate_add_rmsnorm_modulate(h, u, g, sc, sh, EPS, residual_out=r,
+                                                        modulated_out=m),
+                  4 * N * es + 3 * vb, [h, u, g, sc, sh], [r, m],
+                  sampler("fused", [h, u, g, sc, sh]))
+
+    builders = [rga_bcast, rga_bcast_inplace, rga_full, mod_bcast, fused_bcast]
+    if only is not None:
+        builders = [f for f in builders if f.__name__ == only]
+        if not builders:
+            raise SystemExit(f"unknown --op {only}")
+    return [f() for f in builders]
 
 
 def chain_ops(device, B=2, L=32640, D=4096, blocks=8, dtype="bf16"):
@@ -454,10 +472,12 @@ def run_ours(args):
                                 "(1 modulation + 23 fused + 1 residual gate per step)",
                     "B": 2, "L": 32640, "D": 4096, "blocks": 8}
     else:
-        ops = hotpath_ops(device)
+        ops = hotpath_ops(device, only=args.op)
         workload = {"workload": "ltx2_bcast_s32640_c4096 hot path: rga_bcast, "
                                 "rga_bcast_inplace, rga_full, mod_bcast, fused_bcast",
                     "B": 1, "L": 32640, "D": 4096}
+        if args.op:
+            workload["workload"] = f"ltx2_bcast_s32640_c4096 {args.op} only (profiling)"
     workload["l2"] = ("no flush: every op reads its own inputs, each 267 MB or more, "
                       "above the 129 MB L2")
     workload["eps"] = EPS
@@ -604,6 +624,9 @@ def main():
     p.add_argument("--workload", choices=["hotpath", "chain", "shapes"], default="hotpath")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--op", default=None,
+                   help="time one op of the hot path only (rga_bcast, rga_bcast_inplace, "
+                        "rga_full, mod_bcast, fused_bcast): for profiling")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
