@@ -254,7 +254,16 @@ __device__ __forceinline__ float rms_inverse(float sumsq, int64_t D, float eps) 
       D < (int64_t(1) << 24)
           ? __fdiv_rn(sumsq, static_cast<float>(D))
           : static_cast<float>(static_cast<double>(sumsq) / static_cast<double>(D));
-  return __frsqrt_rn(__fadd_rn(ms, eps));
+  const float v = __fadd_rn(ms, eps);
+#ifdef DIT_RSQRT_NEWTON
+  // tuning builds: hardware estimate plus one Newton-Raphson step for
+  // 1/sqrt(v): y1 = y0 + y0/2 * (1 - v*y0^2)
+  const float y0 = rsqrtf(v);
+  const float e = fmaf(-v * y0, y0, 1.0f);
+  return fmaf(0.5f * y0, e, y0);
+#else
+  return __frsqrt_rn(v);
+#endif
 }
 
 // ---------------------------------------------------------------------------

@@ -18,6 +18,8 @@
 // writes it back over its own hidden slot, and pass two reads it from there.
 #pragma once
 
+#include <type_traits>
+
 #include "dit_device.cuh"
 #include "dit_internal.h"
 
@@ -39,7 +41,7 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // 16-byte shared-memory access at a shared-window address
-__device__ __forceinline__ Raw<16> lds16(const Raw<16>*, uint32_t addr) {
+__device__ __forceinline__ Raw<16> lds16(uint32_t addr) {
   Raw<16> r;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
@@ -90,7 +92,11 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[RC]) {
   return z;
 }
 
-template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL>
+// ALLCOLS: every thread owns VPT valid granules (T * VPT * slices == nvec),
+// so no column predicate is evaluated.  A group of RC rows that lies wholly
+// inside the CTA's rows takes a path without row predicates; only the last
+// group of a ragged chunk checks them.
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS>
 __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
   using G = Granule<T>;
   constexpr int P = G::P;  // fp32 pairs per 16-byte granule
@@ -120,14 +126,15 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
   const int64_t g0 = (int64_t)blockIdx.y * nthr * VPT + tid;
   bool cval[VPT];
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) cval[k] = g0 + (int64_t)k * nthr < a.nvec;
+  for (int k = 0; k < VPT; ++k) cval[k] = ALLCOLS || g0 + (int64_t)k * nthr < a.nvec;
+  const int64_t kstride = (int64_t)nthr * 16;  // bytes between a thread's granules
 
   // [B, 1, D] operands, once, in fp32: gate; 1 + scale (one rounding); shift
   F2 gv[VPT][P], onev[VPT][P], shv[VPT][P];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     if (!cval[k]) continue;
-    const int64_t off = b * pitch + (g0 + (int64_t)k * nthr) * 16;
+    const int64_t off = b * pitch + g0 * 16 + k * kstride;
     if constexpr (kGate && !GFULL) G::widen(ld_bcast<16>((const char*)a.g + off), gv[k]);
     if constexpr (kReduce && !MFULL) {
       G::widen(ld_bcast<16>((const char*)a.sc + off), onev[k]);
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
     }
   }
 
-  // global column pointers of the streamed operands
+  // column pointers (row 0) of the streamed inputs and of the outputs
   const char* gp[NS];
   {
     const void* src[5] = {a.x, a.u, a.g, a.sc, a.sh};
@@ -149,13 +156,15 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
       gp[i] = (const char*)src[which] + g0 * 16;
     }
   }
-  const int64_t kstride_g = (int64_t)nthr * 16;  // global bytes between granules k
-  // shared addresses: slot (stage, j, op, k) = base + stage*SS + j*JS + op*OS + k*KS
+  char* const out1 = (char*)a.out + g0 * 16;
+  char* const out2 = (char*)(OP == OP_FUSED ? a.out2 : a.out) + g0 * 16;
+
+  // shared addresses: slot (stage, j, op, k) = stage + j*JS + op*OS + k*KS
   const uint32_t KS = (uint32_t)nthr * 16;
   const uint32_t OS = VPT * KS, JS = NS * OS, SS = RC * JS;
   const uint32_t base = smem_addr(ring) + (uint32_t)tid * 16;
+  const uint32_t ring_end = base + S * SS;
 
-  const int64_t ngroups = (r_end - r_begin + RC - 1) / RC;
   uint32_t issue_stage = base;  // stage of the next group to issue
   int64_t issue_row = r_begin;
   auto issue = [&]() {
@@ -165,17 +174,17 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
       if (row < r_end) {
         const int64_t rowoff = row * pitch;
 #pragma unroll
-        for (int op = 0; op < NS; ++op)
+        for (int op = 0; op < NS; ++op) {
+          const char* src = gp[op] + rowoff;
 #pragma unroll
           for (int k = 0; k < VPT; ++k)
-            if (cval[k])
-              cp_async16(issue_stage + j * JS + op * OS + k * KS, gp[op] + rowoff + k * kstride_g);
+            if (cval[k]) cp_async16(issue_stage + j * JS + op * OS + k * KS, src + k * kstride);
+        }
       }
     }
     cp_async_commit();  // possibly empty: keeps the group count uniform
     issue_row += RC;
-    issue_stage += SS;
-    if (issue_stage == base + S * SS) issue_stage = base;
+    issue_stage = issue_stage + SS == ring_end ? base : issue_stage + SS;
   };
 
 #pragma unroll
@@ -185,37 +194,36 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
   int buf = 0;
   uint32_t stage = base;
 
-  for (int64_t grp = 0; grp < ngroups; ++grp) {
-    cp_async_wait<S - 2>();  // this thread's copies of group grp have landed
-    issue();                 // refill the stage consumed by the previous group
-    const int64_t row0 = r_begin + grp * RC;
-
+  // one group of RC rows starting at row0; CHECK: some rows may lie past r_end
+  auto group = [&](int64_t row0, auto check_tag) {
+    constexpr bool CHECK = decltype(check_tag)::value;
     float ss[RC];
 #pragma unroll
     for (int j = 0; j < RC; ++j) {
       ss[j] = 0.0f;
-      if (row0 + j >= r_end) continue;
+      if (CHECK && row0 + j >= r_end) continue;
       const int64_t rowoff = (row0 + j) * pitch;
       F2 acc = f2(0.0f, 0.0f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!cval[k]) continue;
+        const uint32_t sl = stage + j * JS + k * KS;
         F2 x[P];
         if constexpr (kGate) {
           F2 h[P], u[P], gf[P];
-          G::widen(lds16(nullptr, stage + j * JS + kX * OS + k * KS), h);
-          G::widen(lds16(nullptr, stage + j * JS + kU * OS + k * KS), u);
-          if constexpr (GFULL) G::widen(lds16(nullptr, stage + j * JS + kG * OS + k * KS), gf);
+          G::widen(lds16(sl + kX * OS), h);
+          G::widen(lds16(sl + kU * OS), u);
+          if constexpr (GFULL) G::widen(lds16(sl + kG * OS), gf);
 #pragma unroll
           for (int i = 0; i < P; ++i) x[i] = residual_gate2<T>(h[i], u[i], GFULL ? gf[i] : gv[k][i]);
           const Raw<16> r = G::narrow(x);
-          st_stream<16>(gp_out(a.out, g0) + rowoff + k * kstride_g, r);
+          st_stream<16>(out1 + rowoff + k * kstride, r);
           if constexpr (kReduce) {
-            sts16(stage + j * JS + kX * OS + k * KS, r);  // the stored residual
+            sts16(sl + kX * OS, r);  // the stored residual, read again in pass two
             G::widen(r, x);
           }
         } else {
-          G::widen(lds16(nullptr, stage + j * JS + kX * OS + k * KS), x);
+          G::widen(lds16(sl + kX * OS), x);
         }
         if constexpr (kReduce) {
 #pragma unroll
@@ -228,8 +236,8 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
     if constexpr (kReduce) {
       // row sums: warp (rows spread over lane groups), then across warps
       const float w = warp_sum_rows<RC>(ss);
-      constexpr int group = 32 / RC;
-      if ((lane & (group - 1)) == 0) part[buf][lane / group][warp] = w;
+      constexpr int grp_lanes = 32 / RC;
+      if ((lane & (grp_lanes - 1)) == 0) part[buf][lane / grp_lanes][warp] = w;
       __syncthreads();
       // lane l finishes row l % RC (lane-parallel), then broadcasts
       const int jr = lane % RC;
@@ -237,22 +245,22 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
       for (int i = 0; i < nwarps; ++i) tot += part[buf][jr][i];
       const float rl = rms_inverse(tot, a.D, a.eps);
       buf ^= 1;
-      void* mout = OP == OP_FUSED ? a.out2 : a.out;
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
         const float r = __shfl_sync(0xFFFFFFFFu, rl, j);
-        if (row0 + j >= r_end) continue;
+        if (CHECK && row0 + j >= r_end) continue;
         const int64_t rowoff = (row0 + j) * pitch;
         const F2 r2 = f2(r, r);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           if (!cval[k]) continue;
+          const uint32_t sl = stage + j * JS + k * KS;
           F2 x[P], y[P];
-          G::widen(lds16(nullptr, stage + j * JS + kX * OS + k * KS), x);
+          G::widen(lds16(sl + kX * OS), x);
           if constexpr (MFULL) {
             F2 sc[P], sh[P];
-            G::widen(lds16(nullptr, stage + j * JS + kSc * OS + k * KS), sc);
-            G::widen(lds16(nullptr, stage + j * JS + kSh * OS + k * KS), sh);
+            G::widen(lds16(sl + kSc * OS), sc);
+            G::widen(lds16(sl + kSh * OS), sh);
 #pragma unroll
             for (int i = 0; i < P; ++i)
               y[i] = modulate2(f2_mul(x[i], r2), f2_add(f2(1.0f, 1.0f), sc[i]), sh[i]);
@@ -260,12 +268,20 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
 #pragma unroll
             for (int i = 0; i < P; ++i) y[i] = modulate2(f2_mul(x[i], r2), onev[k][i], shv[k][i]);
           }
-          st_stream<16>(gp_out(mout, g0) + rowoff + k * kstride_g, G::narrow(y));
+          st_stream<16>(out2 + rowoff + k * kstride, G::narrow(y));
         }
       }
     }
-    stage += SS;
-    if (stage == base + S * SS) stage = base;
+  };
+
+  for (int64_t row0 = r_begin; row0 < r_end; row0 += RC) {
+    cp_async_wait<S - 2>();  // this thread's copies of this group have landed
+    issue();                 // refill the stage consumed by the previous group
+    if (row0 + RC <= r_end)
+      group(row0, std::false_type{});
+    else
+      group(row0, std::true_type{});
+    stage = stage + SS == ring_end ? base : stage + SS;
   }
   cp_async_wait<0>();  // no copy may outlive the CTA's shared memory
 }
@@ -304,11 +320,11 @@ __host__ __device__ constexpr int pipe_rows() {
 
 // Launch the staged kernel with S stages; returns cudaErrorNotSupported when
 // the row is too long for it (the caller then uses the two-pass kernel).
-template <int OP, class T, int S, bool GFULL, bool MFULL>
+template <int OP, class T, int S, bool GFULL, bool MFULL, bool ALLCOLS>
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
   constexpr int RC = pipe_rows<OP>();
-  auto kern = pipe_kernel<OP, T, kPipeVPT, S, RC, GFULL, MFULL>;
+  auto kern = pipe_kernel<OP, T, kPipeVPT, S, RC, GFULL, MFULL, ALLCOLS>;
   // allow the ring's dynamic shared memory: raised per device as needed
   static size_t configured[64];
   const bool cached = dev.device >= 0 && dev.device < 64;
@@ -355,13 +371,22 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;
   if (per_stage * S > limit) return cudaErrorNotSupported;
   // instantiated stage counts: 2, 3 and the operation's default
+  const bool allcols = (int64_t)block * kPipeVPT * slices == a.nvec;
   return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
     using T = typename decltype(tt)::type;
     constexpr int SD = pipe_stages<OP>();
-    if (S == 2) return launch_pipe_s<OP, T, 2, GFULL, MFULL>(dev, a, B, block, slices, 2 * per_stage, stream);
+    auto go = [&](auto stages, auto cols) -> cudaError_t {
+      constexpr int SS_ = decltype(stages)::value;
+      return launch_pipe_s<OP, T, SS_, GFULL, MFULL, decltype(cols)::value>(
+          dev, a, B, block, slices, SS_ * per_stage, stream);
+    };
+    auto by_cols = [&](auto stages) -> cudaError_t {
+      return allcols ? go(stages, std::true_type{}) : go(stages, std::false_type{});
+    };
+    if (S == 2) return by_cols(std::integral_constant<int, 2>{});
     if constexpr (SD > 3)
-      if (S == SD) return launch_pipe_s<OP, T, SD, GFULL, MFULL>(dev, a, B, block, slices, SD * per_stage, stream);
-    return launch_pipe_s<OP, T, 3, GFULL, MFULL>(dev, a, B, block, slices, 3 * per_stage, stream);
+      if (S == SD) return by_cols(std::integral_constant<int, SD>{});
+    return by_cols(std::integral_constant<int, 3>{});
   });
 }
 
