@@ -203,7 +203,9 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
       ss[j] = 0.0f;
       if (CHECK && row0 + j >= r_end) continue;
       const int64_t rowoff = (row0 + j) * pitch;
-      F2 acc = f2(0.0f, 0.0f);
+      F2 acc[P];  // independent accumulators: no serial FMA chain
+#pragma unroll
+      for (int i = 0; i < P; ++i) acc[i] = f2(0.0f, 0.0f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!cval[k]) continue;
@@ -227,10 +229,14 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
         }
         if constexpr (kReduce) {
 #pragma unroll
-          for (int i = 0; i < P; ++i) acc = f2_fma(x[i], x[i], acc);
+          for (int i = 0; i < P; ++i) acc[i] = f2_fma(x[i], x[i], acc[i]);
         }
       }
-      if constexpr (kReduce) ss[j] = f2_lo(acc) + f2_hi(acc);
+      if constexpr (kReduce) {
+#pragma unroll
+        for (int i = 1; i < P; ++i) acc[0] = f2_add(acc[0], acc[i]);
+        ss[j] = f2_lo(acc[0]) + f2_hi(acc[0]);
+      }
     }
 
     if constexpr (kReduce) {
@@ -297,10 +303,10 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
 #define DIT_PIPE_S_MOD 3
 #endif
 #ifndef DIT_PIPE_RC_MOD
-#define DIT_PIPE_RC_MOD 4
+#define DIT_PIPE_RC_MOD 1
 #endif
 #ifndef DIT_PIPE_S_FUSED
-#define DIT_PIPE_S_FUSED 3
+#define DIT_PIPE_S_FUSED 2
 #endif
 #ifndef DIT_PIPE_RC_FUSED
 #define DIT_PIPE_RC_FUSED 1
