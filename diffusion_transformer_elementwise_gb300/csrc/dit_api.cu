@@ -211,6 +211,8 @@ dit_status dit_rmsnorm_modulate(void* out, const void* x, const void* scale, con
   a.D = D;
   a.rows = B * L;
   a.eps = eps;
+  a.d_f = (float)D;
+  a.inv_d = 1.0f / (float)D;
   const uint64_t bits = (uintptr_t)out | (uintptr_t)x | (uintptr_t)scale | (uintptr_t)shift |
                         (uint64_t)(D * es);
   return launch_status(dit::launch_modulate(dev, dtype, dit::widest_access(bits), full, a, B,
@@ -264,6 +266,8 @@ dit_status dit_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out
   a.D = D;
   a.rows = B * L;
   a.eps = eps;
+  a.d_f = (float)D;
+  a.inv_d = 1.0f / (float)D;
   const uint64_t bits = (uintptr_t)residual_out | (uintptr_t)modulated_out | (uintptr_t)hidden |
                         (uintptr_t)update | (uintptr_t)gate | (uintptr_t)scale |
                         (uintptr_t)shift | (uint64_t)(D * es);

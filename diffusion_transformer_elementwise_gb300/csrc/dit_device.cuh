@@ -245,25 +245,24 @@ __device__ __forceinline__ float modulate(float x, float r, float s, float h) {
   return __fadd_rn(__fmul_rn(n, one), h);
 }
 
-// 1 / sqrt(mean + eps) for the row's fp32 sum of squares over D elements:
-// the mean is the correctly rounded fp32 quotient (D < 2^24 is exact in fp32;
-// larger D divides in fp64), the root the correctly rounded fp32 inverse
-// square root.
-__device__ __forceinline__ float rms_inverse(float sumsq, int64_t D, float eps) {
-  const float ms =
-      D < (int64_t(1) << 24)
-          ? __fdiv_rn(sumsq, static_cast<float>(D))
-          : static_cast<float>(static_cast<double>(sumsq) / static_cast<double>(D));
+// 1 / sqrt(mean + eps) from the row's fp32 sum of squares S over D elements,
+// in fp32 throughout:
+// * mean: q = S * fl(1/D), then one correction with the exact residual
+//   e = S - q*D (an FMA), q + e * fl(1/D) -- Markstein's division refinement,
+//   which yields the correctly rounded S/D except in rare near-halfway cases
+//   (and exactly S/D whenever D is a power of two);
+// * inverse root: the hardware estimate y0 = rsqrtf(v), then one
+//   Newton-Raphson step y1 = y0 + y0/2 * (1 - v*y0^2), accurate to about an
+//   ulp.
+// The oracle takes the correctly rounded values; the difference is a few fp32
+// ulps of r, the same order as the one the summation order already makes.
+__device__ __forceinline__ float rms_inverse(float sumsq, float D, float inv_d, float eps) {
+  const float q = sumsq * inv_d;
+  const float ms = fmaf(fmaf(-q, D, sumsq), inv_d, q);
   const float v = __fadd_rn(ms, eps);
-#ifdef DIT_RSQRT_NEWTON
-  // tuning builds: hardware estimate plus one Newton-Raphson step for
-  // 1/sqrt(v): y1 = y0 + y0/2 * (1 - v*y0^2)
   const float y0 = rsqrtf(v);
   const float e = fmaf(-v * y0, y0, 1.0f);
   return fmaf(0.5f * y0, e, y0);
-#else
-  return __frsqrt_rn(v);
-#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -373,11 +372,12 @@ __device__ __forceinline__ F2 residual_gate2(F2 h, F2 u, F2 g) {
   }
 }
 
-// fl(fl(n * one) + shift) per lane with n = x * r already formed: the
-// multiply-then-add pair uses the non-contractible intrinsics.
+// fl(fl(n * one) + shift) per lane, n = x * r already formed: the product is
+// packed, the final add is the non-contractible scalar intrinsic (a packed
+// multiply followed by a packed add may be contracted into one FMA).
 __device__ __forceinline__ F2 modulate2(F2 n, F2 one, F2 shift) {
-  return f2(__fadd_rn(__fmul_rn(f2_lo(n), f2_lo(one)), f2_lo(shift)),
-            __fadd_rn(__fmul_rn(f2_hi(n), f2_hi(one)), f2_hi(shift)));
+  const F2 t = f2_mul(n, one);
+  return f2(__fadd_rn(f2_lo(t), f2_lo(shift)), __fadd_rn(f2_hi(t), f2_hi(shift)));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

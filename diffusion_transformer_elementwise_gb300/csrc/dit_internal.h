@@ -44,6 +44,8 @@ struct RowArgs {
   int64_t chunks_per_batch;
   int64_t nvec;       // vectors of the kernel's width per row
   float eps;
+  float d_f;          // D as fp32
+  float inv_d;        // fl(1 / D)
 };
 
 struct DeviceInfo {

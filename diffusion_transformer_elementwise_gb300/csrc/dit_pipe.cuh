@@ -96,8 +96,13 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[RC]) {
 // so no column predicate is evaluated.  A group of RC rows that lies wholly
 // inside the CTA's rows takes a path without row predicates; only the last
 // group of a ragged chunk checks them.
+#ifdef DIT_PIPE_MAXNREG  // tuning builds: cap the registers
+#define DIT_PIPE_BOUNDS __maxnreg__(DIT_PIPE_MAXNREG)
+#else
+#define DIT_PIPE_BOUNDS __launch_bounds__(512)
+#endif
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS>
-__global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
+__global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   using G = Granule<T>;
   constexpr int P = G::P;  // fp32 pairs per 16-byte granule
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
@@ -190,7 +195,10 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) issue();
 
-  __shared__ float part[2][RC][16];  // per-warp row partial sums (<= 16 warps)
+  __shared__ __align__(16) float part[2][RC][16];  // per-warp row partials (<= 16 warps)
+  // entries of warps this CTA does not have stay zero (read by the tree sum)
+  for (int i = tid; i < 2 * RC * 16; i += nthr)
+    if ((i & 15) >= nwarps) (&part[0][0][0])[i] = 0.0f;
   int buf = 0;
   uint32_t stage = base;
 
@@ -247,9 +255,11 @@ __global__ void __launch_bounds__(512) pipe_kernel(RowArgs a) {
       __syncthreads();
       // lane l finishes row l % RC (lane-parallel), then broadcasts
       const int jr = lane % RC;
-      float tot = 0.0f;
-      for (int i = 0; i < nwarps; ++i) tot += part[buf][jr][i];
-      const float rl = rms_inverse(tot, a.D, a.eps);
+      const float4* pp = reinterpret_cast<const float4*>(&part[buf][jr][0]);
+      const float4 p0 = pp[0], p1 = pp[1], p2 = pp[2], p3 = pp[3];
+      const float tot = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
+                        (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
+      const float rl = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
       buf ^= 1;
 #pragma unroll
       for (int j = 0; j < RC; ++j) {

@@ -153,7 +153,7 @@ __global__ void DIT_ROW_BOUNDS row_kernel(RowArgs a) {
       for (int j = 0; j < R; ++j) {
         float tot = 0.0f;
         for (int w = 0; w < nwarps; ++w) tot += part[buf][j][w];
-        rinv[j] = rms_inverse(tot, a.D, a.eps);
+        rinv[j] = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
       }
       buf ^= 1;
 
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
     float tot = 0.0f;
     for (int i = 0; i < nwarps; ++i) tot += part[buf][i];
     buf ^= 1;
-    const float rinv = rms_inverse(tot, a.D, a.eps);
+    const float rinv = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
 
     // second pass: each thread re-reads exactly the vectors it handled above
     // (for the fused op, its own residual stores)
