@@ -46,6 +46,12 @@ struct RowArgs {
   float eps;
   float d_f;          // D as fp32
   float inv_d;        // fl(1 / D)
+  // grid-stride schedule of the staged kernels: groups of rows, never
+  // straddling a batch; CTA c takes groups c, c + G, c + 2G, ...
+  int64_t gpb;        // groups per batch
+  int64_t ngroups;    // B * gpb
+  int64_t step_b;     // G / gpb
+  int64_t step_g;     // G % gpb
 };
 
 struct DeviceInfo {

@@ -10,7 +10,13 @@
 // no spin loop) is the only synchronisation the ring needs; the one
 // __syncthreads per group belongs to the row reduction.
 //
-// The [B, 1, D] operands are loaded once per CTA and kept in registers in
+// Schedule: rows are taken in groups of RC (never straddling a batch), and
+// CTA c of G takes groups c, c + G, c + 2G, ...: at any moment the G CTAs
+// stream one contiguous window of the tensors, as a flat grid-stride loop
+// would, instead of G scattered chunks.
+//
+// The [B, 1, D] operands are loaded per CTA (again only when its batch
+// changes) and kept in registers in
 // fp32, with 1 + scale already formed (one fp32 rounding, as in the
 // modulation's definition).  The modulation takes two passes over the staged
 // row: sum of squares, then -- after the reduction -- normalise, modulate and
@@ -119,12 +125,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   const int warp = tid >> 5;
   const int nwarps = nthr >> 5;
 
-  const int64_t b = blockIdx.x / a.chunks_per_batch;
-  const int64_t chunk = blockIdx.x - b * a.chunks_per_batch;
-  const int64_t r_begin = b * a.L + chunk * a.rows_per_chunk;
-  const int64_t r_stop = (b + 1) * a.L;
-  const int64_t r_end = r_begin + a.rows_per_chunk < r_stop ? r_begin + a.rows_per_chunk : r_stop;
-  if (r_begin >= r_end) return;  // uniform over the CTA
+  if ((int64_t)blockIdx.x >= a.ngroups) return;  // uniform over the CTA
   const int64_t pitch = a.D * (int64_t)sizeof(T);
 
   // this thread's granules: t + k * T (+ the column slice of the residual gate)
@@ -134,20 +135,22 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   for (int k = 0; k < VPT; ++k) cval[k] = ALLCOLS || g0 + (int64_t)k * nthr < a.nvec;
   const int64_t kstride = (int64_t)nthr * 16;  // bytes between a thread's granules
 
-  // [B, 1, D] operands, once, in fp32: gate; 1 + scale (one rounding); shift
+  // [B, 1, D] operands of batch bb in fp32: gate; 1 + scale (one rounding); shift
   F2 gv[VPT][P], onev[VPT][P], shv[VPT][P];
+  auto load_vectors = [&](int64_t bb) {
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    if (!cval[k]) continue;
-    const int64_t off = b * pitch + g0 * 16 + k * kstride;
-    if constexpr (kGate && !GFULL) G::widen(ld_bcast<16>((const char*)a.g + off), gv[k]);
-    if constexpr (kReduce && !MFULL) {
-      G::widen(ld_bcast<16>((const char*)a.sc + off), onev[k]);
+    for (int k = 0; k < VPT; ++k) {
+      if (!cval[k]) continue;
+      const int64_t off = bb * pitch + g0 * 16 + k * kstride;
+      if constexpr (kGate && !GFULL) G::widen(ld_bcast<16>((const char*)a.g + off), gv[k]);
+      if constexpr (kReduce && !MFULL) {
+        G::widen(ld_bcast<16>((const char*)a.sc + off), onev[k]);
 #pragma unroll
-      for (int i = 0; i < P; ++i) onev[k][i] = f2_add(f2(1.0f, 1.0f), onev[k][i]);
-      G::widen(ld_bcast<16>((const char*)a.sh + off), shv[k]);
+        for (int i = 0; i < P; ++i) onev[k][i] = f2_add(f2(1.0f, 1.0f), onev[k][i]);
+        G::widen(ld_bcast<16>((const char*)a.sh + off), shv[k]);
+      }
     }
-  }
+  };
 
   // column pointers (row 0) of the streamed inputs and of the outputs
   const char* gp[NS];
@@ -170,25 +173,39 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   const uint32_t base = smem_addr(ring) + (uint32_t)tid * 16;
   const uint32_t ring_end = base + S * SS;
 
-  uint32_t issue_stage = base;  // stage of the next group to issue
-  int64_t issue_row = r_begin;
+  const int64_t nbatch = a.ngroups / a.gpb;  // B
+  // group position (batch, group within batch) of the next group to issue
+  uint32_t issue_stage = base;
+  int64_t ib = (int64_t)blockIdx.x / a.gpb, ig = (int64_t)blockIdx.x - ib * a.gpb;
+  auto advance = [&](int64_t& bb, int64_t& gg) {
+    bb += a.step_b;
+    gg += a.step_g;
+    if (gg >= a.gpb) {
+      gg -= a.gpb;
+      ++bb;
+    }
+  };
   auto issue = [&]() {
+    if (ib < nbatch) {
+      const int64_t row0 = ib * a.L + ig * RC;
+      const int64_t rend = (ib + 1) * a.L;
 #pragma unroll
-    for (int j = 0; j < RC; ++j) {
-      const int64_t row = issue_row + j;
-      if (row < r_end) {
-        const int64_t rowoff = row * pitch;
+      for (int j = 0; j < RC; ++j) {
+        const int64_t row = row0 + j;
+        if (row < rend) {
+          const int64_t rowoff = row * pitch;
 #pragma unroll
-        for (int op = 0; op < NS; ++op) {
-          const char* src = gp[op] + rowoff;
+          for (int op = 0; op < NS; ++op) {
+            const char* src = gp[op] + rowoff;
 #pragma unroll
-          for (int k = 0; k < VPT; ++k)
-            if (cval[k]) cp_async16(issue_stage + j * JS + op * OS + k * KS, src + k * kstride);
+            for (int k = 0; k < VPT; ++k)
+              if (cval[k]) cp_async16(issue_stage + j * JS + op * OS + k * KS, src + k * kstride);
+          }
         }
       }
     }
     cp_async_commit();  // possibly empty: keeps the group count uniform
-    issue_row += RC;
+    advance(ib, ig);
     issue_stage = issue_stage + SS == ring_end ? base : issue_stage + SS;
   };
 
@@ -202,14 +219,14 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   int buf = 0;
   uint32_t stage = base;
 
-  // one group of RC rows starting at row0; CHECK: some rows may lie past r_end
-  auto group = [&](int64_t row0, auto check_tag) {
+  // one group of RC rows starting at row0; CHECK: rows at or past rend are skipped
+  auto group = [&](int64_t row0, int64_t rend, auto check_tag) {
     constexpr bool CHECK = decltype(check_tag)::value;
     float ss[RC];
 #pragma unroll
     for (int j = 0; j < RC; ++j) {
       ss[j] = 0.0f;
-      if (CHECK && row0 + j >= r_end) continue;
+      if (CHECK && row0 + j >= rend) continue;
       const int64_t rowoff = (row0 + j) * pitch;
       F2 acc[P];  // independent accumulators: no serial FMA chain
 #pragma unroll
@@ -264,7 +281,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
         const float r = __shfl_sync(0xFFFFFFFFu, rl, j);
-        if (CHECK && row0 + j >= r_end) continue;
+        if (CHECK && row0 + j >= rend) continue;
         const int64_t rowoff = (row0 + j) * pitch;
         const F2 r2 = f2(r, r);
 #pragma unroll
@@ -290,14 +307,23 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
     }
   };
 
-  for (int64_t row0 = r_begin; row0 < r_end; row0 += RC) {
+  int64_t cb = (int64_t)blockIdx.x / a.gpb, cg = (int64_t)blockIdx.x - cb * a.gpb;
+  int64_t vec_b = -1;  // batch whose vectors are in registers
+  while (cb < nbatch) {
     cp_async_wait<S - 2>();  // this thread's copies of this group have landed
     issue();                 // refill the stage consumed by the previous group
-    if (row0 + RC <= r_end)
-      group(row0, std::false_type{});
+    if (cb != vec_b) {       // uniform over the CTA
+      load_vectors(cb);
+      vec_b = cb;
+    }
+    const int64_t row0 = cb * a.L + cg * RC;
+    const int64_t rend = (cb + 1) * a.L;
+    if (row0 + RC <= rend)
+      group(row0, rend, std::false_type{});
     else
-      group(row0, std::true_type{});
+      group(row0, rend, std::true_type{});
     stage = stage + SS == ring_end ? base : stage + SS;
+    advance(cb, cg);
   }
   cp_async_wait<0>();  // no copy may outlive the CTA's shared memory
 }
@@ -353,12 +379,16 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
     }
     if (cached) configured[dev.device] = smem;
   }
-  RowPlan plan;
-  if (!plan_rows(dev, (const void*)kern, block, B, a.L, slices, &plan, smem))
-    return cudaErrorInvalidConfiguration;
-  a.rows_per_chunk = plan.rows_per_chunk;
-  a.chunks_per_batch = plan.chunks_per_batch;
-  kern<<<plan.grid, plan.block, smem, stream>>>(a);
+  // one wave of resident CTAs, each striding over the groups
+  a.gpb = (a.L + RC - 1) / RC;
+  a.ngroups = B * a.gpb;
+  int64_t G = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
+  if (G > a.ngroups) G = a.ngroups;
+  if (G < 1) G = 1;
+  if (G > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  a.step_b = G / a.gpb;
+  a.step_g = G - a.step_b * a.gpb;
+  kern<<<dim3((unsigned)G, slices, 1), dim3((unsigned)block, 1, 1), smem, stream>>>(a);
   return cudaGetLastError();
 }
 
