@@ -336,7 +336,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
 #define DIT_PIPE_RC_RGA 4
 #endif
 #ifndef DIT_PIPE_S_MOD
-#define DIT_PIPE_S_MOD 3
+#define DIT_PIPE_S_MOD 2
 #endif
 #ifndef DIT_PIPE_RC_MOD
 #define DIT_PIPE_RC_MOD 1
@@ -414,9 +414,10 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   const size_t per_stage = (size_t)RC * NS * kPipeVPT * block * 16;
   const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
   int S = pipe_stages<OP>();
-  while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;
+  while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;  // smaller rings
   if (per_stage * S > limit) return cudaErrorNotSupported;
-  // instantiated stage counts: 2, 3 and the operation's default
+  // instantiated stage counts: the operation's default, 3 and 2 (when the
+  // default ring does not fit in shared memory)
   const bool allcols = (int64_t)block * kPipeVPT * slices == a.nvec;
   return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
     using T = typename decltype(tt)::type;
@@ -429,10 +430,14 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
     auto by_cols = [&](auto stages) -> cudaError_t {
       return allcols ? go(stages, std::true_type{}) : go(stages, std::false_type{});
     };
-    if (S == 2) return by_cols(std::integral_constant<int, 2>{});
-    if constexpr (SD > 3)
+    if constexpr (SD == 2) {
+      return by_cols(std::integral_constant<int, 2>{});
+    } else {
       if (S == SD) return by_cols(std::integral_constant<int, SD>{});
-    return by_cols(std::integral_constant<int, 3>{});
+      if constexpr (SD > 3)
+        if (S == 3) return by_cols(std::integral_constant<int, 3>{});
+      return by_cols(std::integral_constant<int, 2>{});
+    }
   });
 }
 
