@@ -486,13 +486,10 @@ def run_ours(args):
         total_ms, per_op = time_steps(ops, args.steps, args.warmup, dist)
     clocks = clk.summary()
 
-    max_ms = total_ms
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
+    from diffusion_transformer_elementwise_gb300.replicas import aggregate_gbs, max_over_ranks
+    max_ms = max_over_ranks(total_ms, device)
     step_bytes = sum(op.bytes for op in ops)
-    value = step_bytes * args.steps * world / (max_ms * 1e-3) / 1e9
+    value = aggregate_gbs(step_bytes, args.steps, world, max_ms)
 
     peak, peak_kind = hbm_peak()
     table = {}
@@ -514,12 +511,8 @@ def run_ours(args):
     if not args.no_e2e:
         e_steps = max(3, min(args.steps, 20))
         e_ms, h2d, d2h = time_e2e(ops, e_steps)
-        e_max = e_ms
-        if dist is not None:
-            t = torch.tensor([e_ms], device=device, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_max = float(t.item())
-        e2e = {"value": step_bytes * e_steps * world / (e_max * 1e-3) / 1e9, "unit": "GB/s",
+        e_max = max_over_ranks(e_ms, device)
+        e2e = {"value": aggregate_gbs(step_bytes, e_steps, world, e_max), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                "ms_per_step": e_max / e_steps}
 
