@@ -347,7 +347,20 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
 #ifndef DIT_PIPE_RC_FUSED
 #define DIT_PIPE_RC_FUSED 1
 #endif
-constexpr int kPipeVPT = 2;           // 16-byte granules per thread per row
+// 16-byte granules per thread per row (tuning builds may override)
+#ifndef DIT_PIPE_VPT_RGA
+#define DIT_PIPE_VPT_RGA 2
+#endif
+#ifndef DIT_PIPE_VPT_MOD
+#define DIT_PIPE_VPT_MOD 2
+#endif
+#ifndef DIT_PIPE_VPT_FUSED
+#define DIT_PIPE_VPT_FUSED 2
+#endif
+template <int OP>
+__host__ __device__ constexpr int pipe_vpt() {
+  return OP == OP_RGA ? DIT_PIPE_VPT_RGA : OP == OP_MOD ? DIT_PIPE_VPT_MOD : DIT_PIPE_VPT_FUSED;
+}
 constexpr int kPipeBlockMax = 512;    // threads: rows up to 16 KB
 constexpr int kStaticSmemReserve = 1024;  // bytes kept for the static arrays
 
@@ -366,7 +379,7 @@ template <int OP, class T, int S, bool GFULL, bool MFULL, bool ALLCOLS>
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
   constexpr int RC = pipe_rows<OP>();
-  auto kern = pipe_kernel<OP, T, kPipeVPT, S, RC, GFULL, MFULL, ALLCOLS>;
+  auto kern = pipe_kernel<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS>;
   // allow the ring's dynamic shared memory: raised per device as needed
   static size_t configured[64];
   const bool cached = dev.device >= 0 && dev.device < 64;
@@ -399,26 +412,27 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   constexpr int RC = pipe_rows<OP>();
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
   a.nvec = row_bytes / 16;
-  const int64_t threads_needed = (a.nvec + kPipeVPT - 1) / kPipeVPT;
+  constexpr int VPT = pipe_vpt<OP>();
+  const int64_t threads_needed = (a.nvec + VPT - 1) / VPT;
   int block;
   unsigned slices = 1;
   if (OP == OP_RGA) {
     block = (int)((threads_needed < 256 ? threads_needed : 256) + 31) / 32 * 32;
-    const int64_t s = (a.nvec + (int64_t)block * kPipeVPT - 1) / ((int64_t)block * kPipeVPT);
+    const int64_t s = (a.nvec + (int64_t)block * VPT - 1) / ((int64_t)block * VPT);
     if (s > 65535) return cudaErrorInvalidConfiguration;
     slices = (unsigned)s;
   } else {
     if (threads_needed > kPipeBlockMax) return cudaErrorNotSupported;
     block = (int)((threads_needed + 31) / 32 * 32);
   }
-  const size_t per_stage = (size_t)RC * NS * kPipeVPT * block * 16;
+  const size_t per_stage = (size_t)RC * NS * VPT * block * 16;
   const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
   int S = pipe_stages<OP>();
   while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;  // smaller rings
   if (per_stage * S > limit) return cudaErrorNotSupported;
   // instantiated stage counts: the operation's default, 3 and 2 (when the
   // default ring does not fit in shared memory)
-  const bool allcols = (int64_t)block * kPipeVPT * slices == a.nvec;
+  const bool allcols = (int64_t)block * VPT * slices == a.nvec;
   return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
     using T = typename decltype(tt)::type;
     constexpr int SD = pipe_stages<OP>();
