@@ -538,7 +538,9 @@ def run_ours(args):
 
 def run_shapes(args):
     """One line per (shape, op): device-timed us per call with an L2 flush
-    before every call (a write of 4x the L2 size outside the timed region)."""
+    before every call, outside the timed region.  The flush *reads* a buffer
+    of 4x the L2 size: a write-flush would leave the L2 full of dirty lines
+    whose write-back then falls inside the next timed call."""
     import torch
 
     import diffusion_transformer_elementwise_gb300 as dit
@@ -548,7 +550,8 @@ def run_shapes(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev)
+    flush = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     peak, _ = hbm_peak()
     shapes = [("ltx2_full_s126_c2048", 1, 126, 2048, "full", "bf16"),
               ("flux2_bcast_s4608_c3072", 1, 4608, 3072, "bcast", "bf16"),
@@ -584,7 +587,7 @@ def run_shapes(args):
                 fn()
             times, hot = [], []
             for _ in range(max(args.steps, 30)):
-                flush.fill_(1.0)
+                torch.amax(flush, dim=0, out=sink)  # read-only eviction of the L2
                 s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 s.record()
                 fn()
