@@ -1,8 +1,10 @@
 """ctypes binding of libdit_elementwise.so (include/dit_elementwise.h).
 
 Argument marshalling only: every function checks that its tensors are
-contiguous CUDA tensors of one dtype, passes their addresses, sizes, dtype,
-layouts and the current torch stream to the C ABI, and raises
+contiguous CUDA tensors of one dtype (a [B, 1, D] gate, scale or shift may be
+a view with contiguous rows and any batch stride, e.g. a row of an adaLN
+table), passes their addresses, sizes, dtype, layouts, the vectors' batch
+stride and the current torch stream to the C ABI, and raises
 :class:`DitError` on a non-OK status.  There is no other code path: without
 the built library, or with CPU tensors, the call raises.
 """
@@ -54,6 +56,15 @@ def library() -> ctypes.CDLL:
             lib.dit_gate_add_rmsnorm_modulate.argtypes = [
                 vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, cf, ci, ci, ci, vp]
             lib.dit_gate_add_rmsnorm_modulate.restype = ci
+            lib.dit_residual_gate_add_strided.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci,
+                                                          i64, vp]
+            lib.dit_residual_gate_add_strided.restype = ci
+            lib.dit_rmsnorm_modulate_strided.argtypes = [vp, vp, vp, vp, i64, i64, i64, cf, ci,
+                                                         ci, i64, vp]
+            lib.dit_rmsnorm_modulate_strided.restype = ci
+            lib.dit_gate_add_rmsnorm_modulate_strided.argtypes = [
+                vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, cf, ci, ci, ci, i64, vp]
+            lib.dit_gate_add_rmsnorm_modulate_strided.restype = ci
             _lib = lib
     return _lib
 
@@ -75,8 +86,10 @@ def _cuda(*tensors):
     for name, t in tensors:
         if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
             raise TypeError(f"{name} must be a CUDA tensor (there is no CPU path)")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
+        vector = name in ("gate", "scale", "shift")
+        if not t.is_contiguous() and not (vector and _strided_vector(t)):
+            raise ValueError(f"{name} must be contiguous" +
+                             (" (or a [B, 1, D] view with contiguous rows)" if vector else ""))
         if dev is None:
             dev = t.device
         elif t.device != dev:
@@ -93,10 +106,26 @@ def _dtype(ref: torch.Tensor, *others) -> int:
     return DTYPE_CODES[ref.dtype]
 
 
+def _strided_vector(t: torch.Tensor) -> bool:
+    """A [B, 1, D] view whose rows are contiguous (e.g. rows of an adaLN
+    table [B, 9, D]): passed with a batch stride."""
+    return t.dim() == 3 and t.shape[1] == 1 and (t.shape[2] <= 1 or t.stride(2) == 1)
+
+
+def _vector_stride(D: int, *vectors) -> int:
+    """The common batch stride (elements) of the [B, 1, D] operands."""
+    strides = {int(t.stride(0)) for t in vectors if t.shape[0] > 1}
+    if len(strides) > 1:
+        raise ValueError("the [B, 1, D] operands of one call must share their batch stride")
+    return strides.pop() if strides else D
+
+
 def layout_of(t: torch.Tensor, B: int, L: int, D: int, name: str) -> int:
     """FULL for [B, L, D], ROW_BCAST for [B, 1, D]."""
     shape = tuple(t.shape)
-    if shape == (B, L, D):
+    if shape == (B, L, D) and (L != 1 or t.is_contiguous()):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
         return FULL
     if shape == (B, 1, D):
         return ROW_BCAST
@@ -120,10 +149,11 @@ def residual_gate_add(hidden, update, gate, out=None, stream=None):
     if tuple(update.shape) != (B, L, D) or tuple(out.shape) != (B, L, D):
         raise ValueError("update and out must have the shape of hidden")
     lay = layout_of(gate, B, L, D, "gate")
+    vs = _vector_stride(D, gate) if lay == ROW_BCAST else D
     with torch.cuda.device(dev):
-        st = library().dit_residual_gate_add(out.data_ptr(), hidden.data_ptr(),
-                                             update.data_ptr(), gate.data_ptr(), B, L, D,
-                                             dt, lay, _stream(dev, stream))
+        st = library().dit_residual_gate_add_strided(out.data_ptr(), hidden.data_ptr(),
+                                                     update.data_ptr(), gate.data_ptr(), B, L, D,
+                                                     dt, lay, vs, _stream(dev, stream))
     check(st, "dit_residual_gate_add")
     return out
 
@@ -141,10 +171,12 @@ def rmsnorm_modulate(x, scale, shift, eps=1e-6, out=None, stream=None):
     lay = layout_of(scale, B, L, D, "scale")
     if layout_of(shift, B, L, D, "shift") != lay:
         raise ValueError("scale and shift must have the same layout")
+    vs = _vector_stride(D, scale, shift) if lay == ROW_BCAST else D
     with torch.cuda.device(dev):
-        st = library().dit_rmsnorm_modulate(out.data_ptr(), x.data_ptr(), scale.data_ptr(),
-                                            shift.data_ptr(), B, L, D, float(eps), dt, lay,
-                                            _stream(dev, stream))
+        st = library().dit_rmsnorm_modulate_strided(out.data_ptr(), x.data_ptr(),
+                                                    scale.data_ptr(), shift.data_ptr(), B, L, D,
+                                                    float(eps), dt, lay, vs,
+                                                    _stream(dev, stream))
     check(st, "dit_rmsnorm_modulate")
     return out
 
@@ -174,10 +206,12 @@ def gate_add_rmsnorm_modulate(hidden, update, gate, scale, shift, eps=1e-6,
     mlay = layout_of(scale, B, L, D, "scale")
     if layout_of(shift, B, L, D, "shift") != mlay:
         raise ValueError("scale and shift must have the same layout")
+    vecs = ([gate] if glay == ROW_BCAST else []) + ([scale, shift] if mlay == ROW_BCAST else [])
+    vs = _vector_stride(D, *vecs)
     with torch.cuda.device(dev):
-        st = library().dit_gate_add_rmsnorm_modulate(
+        st = library().dit_gate_add_rmsnorm_modulate_strided(
             residual_out.data_ptr(), modulated_out.data_ptr(), hidden.data_ptr(),
             update.data_ptr(), gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D,
-            float(eps), dt, glay, mlay, _stream(dev, stream))
+            float(eps), dt, glay, mlay, vs, _stream(dev, stream))
     check(st, "dit_gate_add_rmsnorm_modulate")
     return residual_out, modulated_out

@@ -29,19 +29,24 @@ from .synth import draw, seed_for
 SITES = ("sa", "ca", "ff")
 
 
+PARTS = ("shift", "scale", "gate")
+
+
 def make_inputs(B, L, D, blocks=8, dtype="bf16", device="cuda", seed_tag="chain"):
-    """x [B, L, D], one stand-in update per site kind, and per block a dict
-    site -> (shift, scale, gate), all seeded."""
+    """x [B, L, D], one stand-in update per site kind, and per block an adaLN
+    table [B, 9, D] (shift, scale, gate of sa, ca, ff), all seeded.  Returns
+    (x, updates, tables) where tables[blk][site] = (shift, scale, gate) are
+    [B, 1, D] views into the block's table (batch stride 9 * D)."""
     x = draw("act", (B, L, D), seed_for(seed_tag, "x", B, L, D), dtype, device)
     updates = [draw("act", (B, L, D), seed_for(seed_tag, "u", k, B, L, D), dtype, device)
                for k in range(len(SITES))]
     tables = []
     for blk in range(blocks):
+        table = draw("mod", (B, 3 * len(SITES), D), seed_for(seed_tag, "table", blk, B, D),
+                     dtype, device)
         t = {}
-        for site in SITES:
-            t[site] = tuple(draw("mod", (B, 1, D), seed_for(seed_tag, "table", blk, site, part,
-                                                           B, D), dtype, device)
-                            for part in ("shift", "scale", "gate"))
+        for k, site in enumerate(SITES):
+            t[site] = tuple(table[:, 3 * k + i:3 * k + i + 1, :] for i in range(len(PARTS)))
         tables.append(t)
     return x, updates, tables
 

@@ -139,25 +139,41 @@ const char* dit_status_string(dit_status s) {
   return "unknown dit_status";
 }
 
-dit_status dit_residual_gate_add(void* out, const void* hidden, const void* update,
-                                 const void* gate, int64_t B, int64_t L, int64_t D,
-                                 dit_dtype dtype, dit_layout gate_layout,
-                                 dit_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Bytes a [B, 1, D] operand spans with a batch stride of vs elements.
+int64_t vector_span(int64_t B, int64_t D, int64_t vs, int es) { return ((B - 1) * vs + D) * es; }
+
+// A stride of vs elements between batches: at least D when B > 1 (any value
+// when B == 1, where only one vector is read), and no overflow of the span.
+bool valid_vector_stride(int64_t B, int64_t D, int64_t vs, int es) {
+  if (B <= 1) return true;
+  if (vs < D) return false;
+  int64_t t;
+  return !__builtin_mul_overflow(B - 1, vs, &t) && !__builtin_mul_overflow(t + D, (int64_t)es, &t);
+}
+
+dit_status residual_gate_impl(void* out, const void* hidden, const void* update, const void* gate,
+                              int64_t B, int64_t L, int64_t D, dit_dtype dtype,
+                              dit_layout gate_layout, int64_t vs, dit_stream_t stream) {
   if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
   if (!valid_layout(gate_layout)) return DIT_ERR_BAD_LAYOUT;
   const int es = elem_size(dtype);
   int64_t n;
   if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
+  const bool full = gate_layout == DIT_FULL;
+  if (!full && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
   if (n == 0) return DIT_OK;
   if (!out || !hidden || !update || !gate) return DIT_ERR_NULL_PTR;
   if (misaligned(out, es) || misaligned(hidden, es) || misaligned(update, es) ||
       misaligned(gate, es))
     return DIT_ERR_MISALIGNED;
-  const bool full = gate_layout == DIT_FULL;
   const int64_t bytes = n * es;
   const Span so = span(out, bytes);
   if (overlaps(so, span(update, bytes)) ||
-      overlaps(so, span(gate, full ? bytes : B * D * es)) ||
+      overlaps(so, span(gate, full ? bytes : vector_span(B, D, vs, es))) ||
       (out != hidden && overlaps(so, span(hidden, bytes))))
     return DIT_ERR_ALIAS;
 
@@ -174,27 +190,29 @@ dit_status dit_residual_gate_add(void* out, const void* hidden, const void* upda
   a.L = L;
   a.D = D;
   a.rows = B * L;
+  a.vstride = (B > 1 ? vs : D) * es;
   const uint64_t bits = (uintptr_t)out | (uintptr_t)hidden | (uintptr_t)update |
-                        (uintptr_t)gate | (uint64_t)(D * es);
+                        (uintptr_t)gate | (uint64_t)(D * es) | (uint64_t)a.vstride;
   return launch_status(dit::launch_rga_bcast(dev, dtype, dit::widest_access(bits), a, B, s));
 }
 
-dit_status dit_rmsnorm_modulate(void* out, const void* x, const void* scale, const void* shift,
-                                int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
-                                dit_layout mod_layout, dit_stream_t stream) {
+dit_status modulate_impl(void* out, const void* x, const void* scale, const void* shift,
+                         int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+                         dit_layout mod_layout, int64_t vs, dit_stream_t stream) {
   if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
   if (!valid_layout(mod_layout)) return DIT_ERR_BAD_LAYOUT;
   const int es = elem_size(dtype);
   int64_t n;
   if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
+  const bool full = mod_layout == DIT_FULL;
+  if (!full && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
   if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
   if (n == 0) return DIT_OK;
   if (!out || !x || !scale || !shift) return DIT_ERR_NULL_PTR;
   if (misaligned(out, es) || misaligned(x, es) || misaligned(scale, es) || misaligned(shift, es))
     return DIT_ERR_MISALIGNED;
-  const bool full = mod_layout == DIT_FULL;
   const int64_t bytes = n * es;
-  const int64_t vbytes = full ? bytes : B * D * es;
+  const int64_t vbytes = full ? bytes : vector_span(B, D, vs, es);
   const Span so = span(out, bytes);
   if (overlaps(so, span(x, bytes)) || overlaps(so, span(scale, vbytes)) ||
       overlaps(so, span(shift, vbytes)))
@@ -210,26 +228,28 @@ dit_status dit_rmsnorm_modulate(void* out, const void* x, const void* scale, con
   a.L = L;
   a.D = D;
   a.rows = B * L;
+  a.vstride = (B > 1 && !full ? vs : D) * es;
   a.eps = eps;
   a.d_f = (float)D;
   a.inv_d = 1.0f / (float)D;
   const uint64_t bits = (uintptr_t)out | (uintptr_t)x | (uintptr_t)scale | (uintptr_t)shift |
-                        (uint64_t)(D * es);
+                        (uint64_t)(D * es) | (uint64_t)a.vstride;
   return launch_status(dit::launch_modulate(dev, dtype, dit::widest_access(bits), full, a, B,
                                             (cudaStream_t)stream));
 }
 
-dit_status dit_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out,
-                                         const void* hidden, const void* update,
-                                         const void* gate, const void* scale,
-                                         const void* shift, int64_t B, int64_t L, int64_t D,
-                                         float eps, dit_dtype dtype, dit_layout gate_layout,
-                                         dit_layout mod_layout, dit_stream_t stream) {
+dit_status fused_impl(void* residual_out, void* modulated_out, const void* hidden,
+                      const void* update, const void* gate, const void* scale, const void* shift,
+                      int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+                      dit_layout gate_layout, dit_layout mod_layout, int64_t vs,
+                      dit_stream_t stream) {
   if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
   if (!valid_layout(gate_layout) || !valid_layout(mod_layout)) return DIT_ERR_BAD_LAYOUT;
   const int es = elem_size(dtype);
   int64_t n;
   if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
+  const bool any_bcast = gate_layout == DIT_ROW_BCAST || mod_layout == DIT_ROW_BCAST;
+  if (any_bcast && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
   if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
   if (n == 0) return DIT_OK;
   if (!residual_out || !modulated_out || !hidden || !update || !gate || !scale || !shift)
@@ -239,8 +259,9 @@ dit_status dit_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out
       misaligned(shift, es))
     return DIT_ERR_MISALIGNED;
   const int64_t bytes = n * es;
-  const int64_t gbytes = gate_layout == DIT_FULL ? bytes : B * D * es;
-  const int64_t mbytes = mod_layout == DIT_FULL ? bytes : B * D * es;
+  const int64_t vbytes = vector_span(B, D, vs, es);
+  const int64_t gbytes = gate_layout == DIT_FULL ? bytes : vbytes;
+  const int64_t mbytes = mod_layout == DIT_FULL ? bytes : vbytes;
   const Span sr = span(residual_out, bytes);
   const Span sm = span(modulated_out, bytes);
   const Span inputs[5] = {span(hidden, bytes), span(update, bytes), span(gate, gbytes),
@@ -265,15 +286,67 @@ dit_status dit_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out
   a.L = L;
   a.D = D;
   a.rows = B * L;
+  a.vstride = (B > 1 && any_bcast ? vs : D) * es;
   a.eps = eps;
   a.d_f = (float)D;
   a.inv_d = 1.0f / (float)D;
   const uint64_t bits = (uintptr_t)residual_out | (uintptr_t)modulated_out | (uintptr_t)hidden |
                         (uintptr_t)update | (uintptr_t)gate | (uintptr_t)scale |
-                        (uintptr_t)shift | (uint64_t)(D * es);
+                        (uintptr_t)shift | (uint64_t)(D * es) | (uint64_t)a.vstride;
   return launch_status(dit::launch_fused(dev, dtype, dit::widest_access(bits),
                                          gate_layout == DIT_FULL, mod_layout == DIT_FULL, a, B,
                                          (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+dit_status dit_residual_gate_add(void* out, const void* hidden, const void* update,
+                                 const void* gate, int64_t B, int64_t L, int64_t D,
+                                 dit_dtype dtype, dit_layout gate_layout,
+                                 dit_stream_t stream) {
+  return residual_gate_impl(out, hidden, update, gate, B, L, D, dtype, gate_layout, D, stream);
+}
+
+dit_status dit_rmsnorm_modulate(void* out, const void* x, const void* scale, const void* shift,
+                                int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+                                dit_layout mod_layout, dit_stream_t stream) {
+  return modulate_impl(out, x, scale, shift, B, L, D, eps, dtype, mod_layout, D, stream);
+}
+
+dit_status dit_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out,
+                                         const void* hidden, const void* update,
+                                         const void* gate, const void* scale,
+                                         const void* shift, int64_t B, int64_t L, int64_t D,
+                                         float eps, dit_dtype dtype, dit_layout gate_layout,
+                                         dit_layout mod_layout, dit_stream_t stream) {
+  return fused_impl(residual_out, modulated_out, hidden, update, gate, scale, shift, B, L, D, eps,
+                    dtype, gate_layout, mod_layout, D, stream);
+}
+
+dit_status dit_residual_gate_add_strided(void* out, const void* hidden, const void* update,
+                                         const void* gate, int64_t B, int64_t L, int64_t D,
+                                         dit_dtype dtype, dit_layout gate_layout,
+                                         int64_t vec_stride, dit_stream_t stream) {
+  return residual_gate_impl(out, hidden, update, gate, B, L, D, dtype, gate_layout, vec_stride,
+                            stream);
+}
+
+dit_status dit_rmsnorm_modulate_strided(void* out, const void* x, const void* scale,
+                                        const void* shift, int64_t B, int64_t L, int64_t D,
+                                        float eps, dit_dtype dtype, dit_layout mod_layout,
+                                        int64_t vec_stride, dit_stream_t stream) {
+  return modulate_impl(out, x, scale, shift, B, L, D, eps, dtype, mod_layout, vec_stride, stream);
+}
+
+dit_status dit_gate_add_rmsnorm_modulate_strided(
+    void* residual_out, void* modulated_out, const void* hidden, const void* update,
+    const void* gate, const void* scale, const void* shift, int64_t B, int64_t L, int64_t D,
+    float eps, dit_dtype dtype, dit_layout gate_layout, dit_layout mod_layout,
+    int64_t vec_stride, dit_stream_t stream) {
+  return fused_impl(residual_out, modulated_out, hidden, update, gate, scale, shift, B, L, D, eps,
+                    dtype, gate_layout, mod_layout, vec_stride, stream);
 }
 
 }  // extern "C"

@@ -40,6 +40,7 @@ struct RowArgs {
   int64_t L;          // rows per batch
   int64_t D;          // elements per row
   int64_t rows;       // B * L
+  int64_t vstride;    // bytes between batches of a [B, 1, D] operand (D * s when contiguous)
   int64_t rows_per_chunk;
   int64_t chunks_per_batch;
   int64_t nvec;       // vectors of the kernel's width per row

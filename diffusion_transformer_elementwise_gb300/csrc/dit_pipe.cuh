@@ -141,7 +141,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       if (!cval[k]) continue;
-      const int64_t off = bb * pitch + g0 * 16 + k * kstride;
+      const int64_t off = bb * a.vstride + g0 * 16 + k * kstride;
       if constexpr (kGate && !GFULL) G::widen(ld_bcast<16>((const char*)a.g + off), gv[k]);
       if constexpr (kReduce && !MFULL) {
         G::widen(ld_bcast<16>((const char*)a.sc + off), onev[k]);

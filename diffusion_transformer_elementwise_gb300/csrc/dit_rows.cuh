@@ -80,10 +80,10 @@ __global__ void DIT_ROW_BOUNDS row_kernel(RowArgs a) {
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     if (!cval[k]) continue;
-    if constexpr (kHasGate && !GFULL) gb[k] = ld_bcast<VB>((const char*)a.g + b * pitch + coff[k]);
+    if constexpr (kHasGate && !GFULL) gb[k] = ld_bcast<VB>((const char*)a.g + b * a.vstride + coff[k]);
     if constexpr (kReduce && !MFULL) {
-      scb[k] = ld_bcast<VB>((const char*)a.sc + b * pitch + coff[k]);
-      shb[k] = ld_bcast<VB>((const char*)a.sh + b * pitch + coff[k]);
+      scb[k] = ld_bcast<VB>((const char*)a.sc + b * a.vstride + coff[k]);
+      shb[k] = ld_bcast<VB>((const char*)a.sh + b * a.vstride + coff[k]);
     }
   }
 
@@ -194,8 +194,8 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t b = row / a.L;
     const int64_t rowoff = row * pitch;
-    const int64_t goff = GFULL ? rowoff : b * pitch;
-    const int64_t moff = MFULL ? rowoff : b * pitch;
+    const int64_t goff = GFULL ? rowoff : b * a.vstride;
+    const int64_t moff = MFULL ? rowoff : b * a.vstride;
     float ss = 0.0f;
     for (int64_t v = tid; v < a.nvec; v += nthr) {
       const int64_t c = v * VB;

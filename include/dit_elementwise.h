@@ -106,8 +106,10 @@ dit_status dit_residual_gate_add(void* out, const void* hidden,
  *   r   = 1 / sqrt(mean_d(x[b,l,d]^2) + eps)     (fp32 statistic per row)
  *   out = rnd(fl32(fl32(fl32(x * r) * fl32(1 + S)) + H))
  * with S, H = scale, shift at [b,l,d] (mod_layout DIT_FULL) or [b,0,d]
- * (DIT_ROW_BCAST).  The mean square is accumulated in fp32 (tree order) and
- * r is the correctly rounded fp32 inverse root of fl32(mean + eps).
+ * (DIT_ROW_BCAST).  The statistic is fp32: the sum of squares in tree order,
+ * the mean and the inverse root each within about one fp32 ulp of the
+ * correctly rounded value (a refined quotient and a Newton-refined inverse
+ * root).
  *
  * Source: prhub summary of sglang PR #34172 (LTX-2 quality=high fused
  * RMSNorm+modulate), section "key source snippet" (the eager expression
@@ -128,8 +130,9 @@ dit_status dit_rmsnorm_modulate(void* out, const void* x, const void* scale,
  *   residual_out = dit_residual_gate_add(hidden, update, gate)   (stored)
  *   modulated_out = dit_rmsnorm_modulate(residual_out, scale, shift, eps)
  * The statistic is taken over the residual as stored (rounded to the dtype),
- * so the two outputs are bitwise those of the two separate calls.  The
- * residual is never re-read from memory.
+ * with the same reduction order as dit_rmsnorm_modulate, so the two outputs
+ * are bitwise those of the two separate calls.  The residual is never re-read
+ * from memory.
  *
  * Source: the two operations above; the pages name the fused family member
  * (fused_gate_rmsnorm, prhub summary of sglang PR #34172, "implementation
@@ -144,6 +147,41 @@ dit_status dit_gate_add_rmsnorm_modulate(
     const void* update, const void* gate, const void* scale, const void* shift,
     int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
     dit_layout gate_layout, dit_layout mod_layout, dit_stream_t stream);
+
+/*
+ * Strided [B, 1, D] operands.  The same three operations, with one more
+ * argument: vec_stride, the distance in elements between the vectors of
+ * consecutive batches of every DIT_ROW_BCAST operand of the call (D for a
+ * contiguous [B, 1, D] tensor).  It lets a caller pass rows of an adaLN
+ * table directly: with a per-block table of shape [B, 9, D] (shift, scale,
+ * gate for each of the block's three modulation sites -- self-attention,
+ * prompt cross-attention, feed-forward: prhub summary of sglang PR #34172,
+ * "implementation breakdown" item 3), the site's vectors are
+ * table + i*D with vec_stride = 9*D, and no chunk is copied out.
+ *
+ * vec_stride must be >= D when B > 1 (DIT_ERR_BAD_SHAPE otherwise); it is
+ * unused for DIT_FULL operands.  Aliasing is checked over the whole span
+ * [p, p + ((B-1)*vec_stride + D) elements) of each strided operand.
+ */
+dit_status dit_residual_gate_add_strided(void* out, const void* hidden,
+                                         const void* update, const void* gate,
+                                         int64_t B, int64_t L, int64_t D,
+                                         dit_dtype dtype, dit_layout gate_layout,
+                                         int64_t vec_stride, dit_stream_t stream);
+
+dit_status dit_rmsnorm_modulate_strided(void* out, const void* x,
+                                        const void* scale, const void* shift,
+                                        int64_t B, int64_t L, int64_t D,
+                                        float eps, dit_dtype dtype,
+                                        dit_layout mod_layout, int64_t vec_stride,
+                                        dit_stream_t stream);
+
+dit_status dit_gate_add_rmsnorm_modulate_strided(
+    void* residual_out, void* modulated_out, const void* hidden,
+    const void* update, const void* gate, const void* scale, const void* shift,
+    int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+    dit_layout gate_layout, dit_layout mod_layout, int64_t vec_stride,
+    dit_stream_t stream);
 
 #ifdef __cplusplus
 }

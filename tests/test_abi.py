@@ -131,3 +131,20 @@ def test_valid_call_without_device_reports_no_device(lib):
     assert rga(lib) == NODEV
     assert mod(lib) == NODEV
     assert fused(lib) == NODEV
+
+
+def test_strided_vectors_validation(lib):
+    """vec_stride: >= D when B > 1; the strided span counts for aliasing."""
+    f = lib.dit_gate_add_rmsnorm_modulate_strided
+    B, L, D = 2, 4, 8
+    args = lambda r=O, m=O2, g=G, vs=9 * D: (r, m, H, U, g, S, SH, B, L, D, 1e-6, BF16, BCAST,
+                                              BCAST, vs, None)
+    assert f(*args(vs=D - 1)) == SHAPE
+    assert f(*args(vs=D)) in (NODEV, LAUNCH, OK)
+    assert f(*args(vs=9 * D)) in (NODEV, LAUNCH, OK)
+    # an output inside the gap of a strided operand's span is an alias
+    assert f(*args(r=G + 2 * D * 2)) == ALIAS
+    assert lib.dit_rmsnorm_modulate_strided(O, H, S, SH, B, L, D, 1e-6, BF16, BCAST, 3, None) == SHAPE
+    assert lib.dit_residual_gate_add_strided(O, H, U, G, 1, L, D, BF16, BCAST, 0, None) in (NODEV, LAUNCH, OK)
+    # full layouts ignore the stride
+    assert lib.dit_residual_gate_add_strided(O, H, U, G, B, L, D, BF16, FULL, 0, None) in (NODEV, LAUNCH, OK)

@@ -55,7 +55,7 @@ def _run(orc, B, L, D, rows):
     idx = rows.cuda()
     xs = x[:, idx, :].contiguous().cpu()
     us = [u[:, idx, :].contiguous().cpu() for u in updates]
-    ts = [{s: tuple(v.cpu() for v in tb[s]) for s in chain.SITES} for tb in tables]
+    ts = [{s: tuple(v.cpu().contiguous() for v in tb[s]) for s in chain.SITES} for tb in tables]
     got = []
 
     def on_site(j, xd, md):

@@ -239,3 +239,37 @@ def test_cpu_tensors_are_rejected():
     h = torch.zeros((1, 2, 8), dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         dit.residual_gate_add(h, h, h)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_strided_adaln_table(orc, dtype):
+    """Gate, scale and shift as [B, 1, D] rows of a [B, 9, D] adaLN table
+    (batch stride 9 * D): identical bits to contiguous copies, and to the
+    oracle."""
+    from diffusion_transformer_elementwise_gb300.synth import draw, seed_for
+    B, L, D = 3, 21, 3072
+    h, u, _ = rga_inputs(B, L, D, dtype, "bcast", tag="strided")
+    table = draw("mod", (B, 9, D), seed_for("strided", "table", dtype), dtype, "cuda")
+    sh_v, sc_v, g_v = table[:, 3:4], table[:, 4:5], table[:, 5:6]
+    assert not g_v.is_contiguous() and g_v.stride(0) == 9 * D
+    hd, ud = cuda(h, u)
+    out_s = dit.residual_gate_add(hd, ud, g_v)
+    out_c = dit.residual_gate_add(hd, ud, g_v.contiguous())
+    mod_s = dit.rmsnorm_modulate(hd, sc_v, sh_v, EPS)
+    mod_c = dit.rmsnorm_modulate(hd, sc_v.contiguous(), sh_v.contiguous(), EPS)
+    res_s, fm_s = dit.gate_add_rmsnorm_modulate(hd, ud, g_v, sc_v, sh_v, EPS)
+    res_c, fm_c = dit.gate_add_rmsnorm_modulate(hd, ud, g_v.contiguous(), sc_v.contiguous(),
+                                                sh_v.contiguous(), EPS)
+    torch.cuda.synchronize()
+    for a, b in ((out_s, out_c), (mod_s, mod_c), (res_s, res_c), (fm_s, fm_c)):
+        assert_bit_exact(a, b)
+    g, sc, sh = (v.cpu().contiguous() for v in (g_v, sc_v, sh_v))
+    assert_bit_exact(out_s, oracle_rga(orc, h, u, g, dtype, "bcast"))
+    ref, t = oracle_mod(orc, h, sc, sh, dtype, "bcast", EPS, with_t=True)
+    modulation_stats(mod_s, ref, t.numpy(), dtype, "strided modulation")
+    rref, mref, t2 = oracle_fused(orc, h, u, g, sc, sh, dtype, "bcast", "bcast", EPS, with_t=True)
+    assert_bit_exact(res_s, rref)
+    modulation_stats(fm_s, mref, t2.numpy(), dtype, "strided fused")
+    # the [B, 1, D] operands of one call must share their batch stride
+    with pytest.raises(ValueError):
+        dit.gate_add_rmsnorm_modulate(hd, ud, g_v, sc_v.contiguous(), sh_v, EPS)
