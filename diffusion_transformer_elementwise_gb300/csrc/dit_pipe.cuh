@@ -220,8 +220,14 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   uint32_t stage = base;
 
   // one group of RC rows starting at row0; CHECK: rows at or past rend are skipped
+#ifdef DIT_PIPE_KEEP_X  // tuning builds: pass two reuses pass one's fp32 values
+  constexpr bool kKeep = kReduce && !MFULL;
+#else
+  constexpr bool kKeep = false;
+#endif
   auto group = [&](int64_t row0, int64_t rend, auto check_tag) {
     constexpr bool CHECK = decltype(check_tag)::value;
+    F2 kept[kKeep ? RC : 1][kKeep ? VPT : 1][P];
     float ss[RC];
 #pragma unroll
     for (int j = 0; j < RC; ++j) {
@@ -255,6 +261,10 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
         if constexpr (kReduce) {
 #pragma unroll
           for (int i = 0; i < P; ++i) acc[i] = f2_fma(x[i], x[i], acc[i]);
+          if constexpr (kKeep) {
+#pragma unroll
+            for (int i = 0; i < P; ++i) kept[kKeep ? j : 0][kKeep ? k : 0][i] = x[i];
+          }
         }
       }
       if constexpr (kReduce) {
@@ -273,14 +283,17 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
       // lane l finishes row l % RC (lane-parallel), then broadcasts
       const int jr = lane % RC;
       const float4* pp = reinterpret_cast<const float4*>(&part[buf][jr][0]);
-      const float4 p0 = pp[0], p1 = pp[1], p2 = pp[2], p3 = pp[3];
-      const float tot = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
-                        (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
+      const float4 p0 = pp[0], p1 = pp[1];
+      float tot = ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w));
+      if (nwarps > 8) {  // uniform
+        const float4 p2 = pp[2], p3 = pp[3];
+        tot += ((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w));
+      }
       const float rl = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
       buf ^= 1;
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
-        const float r = __shfl_sync(0xFFFFFFFFu, rl, j);
+        const float r = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
         if (CHECK && row0 + j >= rend) continue;
         const int64_t rowoff = (row0 + j) * pitch;
         const F2 r2 = f2(r, r);
@@ -289,7 +302,12 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
           if (!cval[k]) continue;
           const uint32_t sl = stage + j * JS + k * KS;
           F2 x[P], y[P];
-          G::widen(lds16(sl + kX * OS), x);
+          if constexpr (kKeep) {
+#pragma unroll
+            for (int i = 0; i < P; ++i) x[i] = kept[kKeep ? j : 0][kKeep ? k : 0][i];
+          } else {
+            G::widen(lds16(sl + kX * OS), x);
+          }
           if constexpr (MFULL) {
             F2 sc[P], sh[P];
             G::widen(lds16(sl + kSc * OS), sc);
