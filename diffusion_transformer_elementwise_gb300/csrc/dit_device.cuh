@@ -372,17 +372,13 @@ __device__ __forceinline__ F2 residual_gate2(F2 h, F2 u, F2 g) {
   }
 }
 
-// fl(fl(n * one) + shift) per lane, n = x * r already formed.  A packed
-// multiply followed by a packed add may be contracted into one FMA, so the add
-// is written as an explicit FMA with multiplier 1 -- one rounding of t + shift,
-// with nothing left to contract (or, in tuning builds, as scalar adds).
+// fl(fl(n * one) + shift) per lane, n = x * r already formed: the product is
+// packed, the final add is the non-contractible scalar intrinsic.  (ptxas
+// contracts a packed multiply followed by a packed add -- or by an FMA with
+// multiplier 1 -- into one FMA; the bit-exact rounding-order test catches it.)
 __device__ __forceinline__ F2 modulate2(F2 n, F2 one, F2 shift) {
   const F2 t = f2_mul(n, one);
-#ifdef DIT_SCALAR_FINAL_ADD
   return f2(__fadd_rn(f2_lo(t), f2_lo(shift)), __fadd_rn(f2_hi(t), f2_hi(shift)));
-#else
-  return f2_fma(t, f2(1.0f, 1.0f), shift);
-#endif
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

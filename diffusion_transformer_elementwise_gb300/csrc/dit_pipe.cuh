@@ -220,14 +220,8 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   uint32_t stage = base;
 
   // one group of RC rows starting at row0; CHECK: rows at or past rend are skipped
-#ifdef DIT_PIPE_KEEP_X  // tuning builds: pass two reuses pass one's fp32 values
-  constexpr bool kKeep = kReduce && !MFULL;
-#else
-  constexpr bool kKeep = false;
-#endif
   auto group = [&](int64_t row0, int64_t rend, auto check_tag) {
     constexpr bool CHECK = decltype(check_tag)::value;
-    F2 kept[kKeep ? RC : 1][kKeep ? VPT : 1][P];
     float ss[RC];
 #pragma unroll
     for (int j = 0; j < RC; ++j) {
@@ -261,10 +255,6 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
         if constexpr (kReduce) {
 #pragma unroll
           for (int i = 0; i < P; ++i) acc[i] = f2_fma(x[i], x[i], acc[i]);
-          if constexpr (kKeep) {
-#pragma unroll
-            for (int i = 0; i < P; ++i) kept[kKeep ? j : 0][kKeep ? k : 0][i] = x[i];
-          }
         }
       }
       if constexpr (kReduce) {
@@ -302,12 +292,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
           if (!cval[k]) continue;
           const uint32_t sl = stage + j * JS + k * KS;
           F2 x[P], y[P];
-          if constexpr (kKeep) {
-#pragma unroll
-            for (int i = 0; i < P; ++i) x[i] = kept[kKeep ? j : 0][kKeep ? k : 0][i];
-          } else {
-            G::widen(lds16(sl + kX * OS), x);
-          }
+          G::widen(lds16(sl + kX * OS), x);
           if constexpr (MFULL) {
             F2 sc[P], sh[P];
             G::widen(lds16(sl + kSc * OS), sc);
