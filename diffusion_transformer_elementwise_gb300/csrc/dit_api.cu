@@ -64,23 +64,6 @@ int resident_ctas(const DeviceInfo& dev, const void* fn, int block, size_t smem)
   return n;
 }
 
-bool plan_rows(const DeviceInfo& dev, const void* fn, int block, int64_t B, int64_t L,
-               unsigned col_slices, RowPlan* plan, size_t smem) {
-  const int64_t target = (int64_t)dev.sm_count * resident_ctas(dev, fn, block, smem);
-  const int64_t per_chunk = B * (int64_t)col_slices;
-  int64_t chunks = (target + per_chunk - 1) / per_chunk;
-  if (chunks > L) chunks = L;
-  if (chunks < 1) chunks = 1;
-  const int64_t rpc = (L + chunks - 1) / chunks;
-  chunks = (L + rpc - 1) / rpc;
-  if (B * chunks > 0x7FFFFFFF) return false;
-  plan->grid = dim3((unsigned)(B * chunks), col_slices, 1);
-  plan->block = dim3((unsigned)block, 1, 1);
-  plan->rows_per_chunk = rpc;
-  plan->chunks_per_batch = chunks;
-  return true;
-}
-
 }  // namespace dit
 
 using dit::DeviceInfo;

@@ -41,13 +41,11 @@ struct RowArgs {
   int64_t D;          // elements per row
   int64_t rows;       // B * L
   int64_t vstride;    // bytes between batches of a [B, 1, D] operand (D * s when contiguous)
-  int64_t rows_per_chunk;
-  int64_t chunks_per_batch;
   int64_t nvec;       // vectors of the kernel's width per row
   float eps;
   float d_f;          // D as fp32
   float inv_d;        // fl(1 / D)
-  // grid-stride schedule of the staged kernels: groups of rows, never
+  // grid-stride schedule of the row kernels: groups of rows, never
   // straddling a batch; CTA c takes groups c, c + G, c + 2G, ...
   int64_t gpb;        // groups per batch
   int64_t ngroups;    // B * gpb
@@ -66,18 +64,6 @@ cudaError_t current_device(DeviceInfo* info);
 // How many CTAs of `fn` at `block` threads (and `smem` bytes of dynamic
 // shared memory) are resident per SM (cached).
 int resident_ctas(const DeviceInfo& dev, const void* fn, int block, size_t smem = 0);
-
-// Grid of the row kernels: (batch, row chunk) pairs on x, column slices on
-// y.  Chunks never straddle a batch, so a CTA loads its [B, 1, D] vectors
-// once.  Sized to one wave of resident CTAs.
-struct RowPlan {
-  dim3 grid;
-  dim3 block;
-  int64_t rows_per_chunk;
-  int64_t chunks_per_batch;
-};
-bool plan_rows(const DeviceInfo& dev, const void* fn, int block, int64_t B,
-               int64_t L, unsigned col_slices, RowPlan* plan, size_t smem = 0);
 
 // Widest power-of-two access (<= 32 bytes) that divides every address and
 // byte pitch in `bits` (the OR of them all).

@@ -1,9 +1,11 @@
 // dit_rows.cuh -- row-tiled kernels for the residual gate with a [B, 1, D]
 // gate, the adaLN RMSNorm-modulation and the fused op.
 //
-// Tiling.  A CTA owns a run of consecutive rows of one batch (so each
-// [B, 1, D] vector is loaded once per CTA, into registers, and reused for all
-// its rows, with no per-element index arithmetic) and a column slice of
+// Tiling.  A CTA takes groups of R consecutive rows of one batch, groups
+// c, c + G, c + 2G, ... of a one-wave grid (so the CTAs stream one moving
+// window of the tensors), keeps each [B, 1, D] vector in registers across its
+// rows (reloaded only when the batch changes; no per-element index
+// arithmetic), and owns a column slice of
 // blockDim.x * 32 bytes (16 for narrow accesses).  Thread t owns the 32/VB
 // (16/VB) vectors of VB bytes at
 // vector indices col0 + t + k * blockDim.x: each warp-wide access is
@@ -57,12 +59,7 @@ __global__ void DIT_ROW_BOUNDS row_kernel(RowArgs a) {
 
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
-  const int64_t b = blockIdx.x / a.chunks_per_batch;
-  const int64_t chunk = blockIdx.x - b * a.chunks_per_batch;
-  const int64_t r_begin = b * a.L + chunk * a.rows_per_chunk;
-  const int64_t r_stop = (b + 1) * a.L;
-  const int64_t r_end = r_begin + a.rows_per_chunk < r_stop ? r_begin + a.rows_per_chunk : r_stop;
-  if (r_begin >= r_end) return;  // uniform over the CTA
+  if ((int64_t)blockIdx.x >= a.ngroups) return;  // uniform over the CTA
 
   const int64_t pitch = a.D * (int64_t)sizeof(T);
   const int64_t col0 = (int64_t)blockIdx.y * nthr * VPT;
@@ -75,17 +72,19 @@ __global__ void DIT_ROW_BOUNDS row_kernel(RowArgs a) {
     coff[k] = cv * VB;
   }
 
-  // [B, 1, D] operands: loaded once for batch b.
+  // [B, 1, D] operands of the current batch, in registers
   Raw<VB> gb[VPT], scb[VPT], shb[VPT];
+  auto load_vectors = [&](int64_t b) {
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    if (!cval[k]) continue;
-    if constexpr (kHasGate && !GFULL) gb[k] = ld_bcast<VB>((const char*)a.g + b * a.vstride + coff[k]);
-    if constexpr (kReduce && !MFULL) {
-      scb[k] = ld_bcast<VB>((const char*)a.sc + b * a.vstride + coff[k]);
-      shb[k] = ld_bcast<VB>((const char*)a.sh + b * a.vstride + coff[k]);
+    for (int k = 0; k < VPT; ++k) {
+      if (!cval[k]) continue;
+      if constexpr (kHasGate && !GFULL) gb[k] = ld_bcast<VB>((const char*)a.g + b * a.vstride + coff[k]);
+      if constexpr (kReduce && !MFULL) {
+        scb[k] = ld_bcast<VB>((const char*)a.sc + b * a.vstride + coff[k]);
+        shb[k] = ld_bcast<VB>((const char*)a.sh + b * a.vstride + coff[k]);
+      }
     }
-  }
+  };
 
   __shared__ float part[2][R][32];
   int buf = 0;
@@ -93,7 +92,24 @@ __global__ void DIT_ROW_BOUNDS row_kernel(RowArgs a) {
   const int warp = tid >> 5;
   const int nwarps = nthr >> 5;
 
-  for (int64_t r0 = r_begin; r0 < r_end; r0 += R) {
+  // grid-stride over groups of R rows (never straddling a batch): CTA c takes
+  // groups c, c + G, c + 2G, ...
+  const int64_t nbatch = a.ngroups / a.gpb;
+  int64_t cb = (int64_t)blockIdx.x / a.gpb, cg = (int64_t)blockIdx.x - cb * a.gpb;
+  int64_t vec_b = -1;
+  for (; cb < nbatch;) {
+    if (cb != vec_b) {
+      load_vectors(cb);
+      vec_b = cb;
+    }
+    const int64_t r0 = cb * a.L + cg * R;
+    const int64_t r_end = r0 + R < (cb + 1) * a.L ? r0 + R : (cb + 1) * a.L;
+    cb += a.step_b;
+    cg += a.step_g;
+    if (cg >= a.gpb) {
+      cg -= a.gpb;
+      ++cb;
+    }
     Raw<VB> xv[R][VPT], uv[R][VPT], gv[R][VPT], scv[R][VPT], shv[R][VPT];
     bool rval[R];
 #pragma unroll
@@ -345,11 +361,16 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
       }
       block = (int)((threads_needed + 31) / 32 * 32);
     }
-    RowPlan plan;
-    if (!plan_rows(dev, fn, block, B, a.L, slices, &plan)) return cudaErrorInvalidConfiguration;
-    a.rows_per_chunk = plan.rows_per_chunk;
-    a.chunks_per_batch = plan.chunks_per_batch;
-    row_kernel<OP, T, VB, R, GFULL, MFULL><<<plan.grid, plan.block, 0, stream>>>(a);
+    a.gpb = (a.L + R - 1) / R;
+    a.ngroups = B * a.gpb;
+    int64_t G = (int64_t)dev.sm_count * resident_ctas(dev, fn, block);
+    if (G > a.ngroups) G = a.ngroups;
+    if (G < 1) G = 1;
+    if (G > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    a.step_b = G / a.gpb;
+    a.step_g = G - a.step_b * a.gpb;
+    row_kernel<OP, T, VB, R, GFULL, MFULL><<<dim3((unsigned)G, slices, 1), dim3((unsigned)block, 1, 1), 0,
+                                             stream>>>(a);
     return cudaGetLastError();
     }
   });
