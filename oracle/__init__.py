@@ -14,6 +14,9 @@ Operations (see dit_oracle.h for the passages each one follows):
   weightless RMSNorm per row over D.
 * :func:`gate_add_rmsnorm_modulate` -- both, the RMS taken over the stored
   (rounded) residual.
+* :func:`gelu_tanh` -- the FFN's tanh-approximated GELU (prhub summary of
+  sglang PR #34172, "implementation breakdown" item 3), in double, rounded
+  once.
 
 Arrays are numpy arrays or CPU torch tensors, contiguous, holding the raw
 storage of the dtype: 16-bit words for bf16 and fp16, ``float32`` for fp32.
@@ -83,6 +86,10 @@ def _bind(path):
     lib.orc_gate_add_rmsnorm_modulate.argtypes = [
         vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
     lib.orc_gate_add_rmsnorm_modulate.restype = ci
+    lib.orc_gelu_tanh.argtypes = [vp, vp, i64, ci]
+    lib.orc_gelu_tanh.restype = ci
+    lib.orc_store_double.argtypes = [vp, i64, ctypes.c_double, ci]
+    lib.orc_store_double.restype = None
     lib.orc_row_rms_inverse.argtypes = [vp, i64, fp, ci]
     lib.orc_row_rms_inverse.restype = fp
     lib.orc_residual_gate_add_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
@@ -200,6 +207,24 @@ def gate_add_rmsnorm_modulate(residual_out, modulated_out, hidden, update, gate,
     _check(rc, "gate_add_rmsnorm_modulate")
 
 
+def gelu_tanh(out, x, dtype="bf16"):
+    """out = gelu(x) with the tanh approximation, evaluated in double and
+    rounded once to dtype."""
+    n = int(x.numel() if hasattr(x, "numel") else x.size)
+    _check(_load().orc_gelu_tanh(_ptr(out), _ptr(x), n, DTYPES[dtype]), "gelu_tanh")
+
+
+def round_double(values, dtype):
+    """Storage words of doubles rounded once to dtype."""
+    import numpy as np
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float64)).ravel()
+    dst = np.empty(v.size, dtype=np.float32 if dtype == "fp32" else np.uint16)
+    lib = _load()
+    for i, x in enumerate(v.tolist()):
+        lib.orc_store_double(_ptr(dst), i, x, DTYPES[dtype])
+    return dst
+
+
 def row_rms_inverse(x_row, D, eps=1e-6, dtype="bf16") -> float:
     return _load().orc_row_rms_inverse(_ptr(x_row), D, float(eps), DTYPES[dtype])
 
@@ -213,7 +238,7 @@ def variant(lib_path: str):
     src = sys.modules[__name__]
     lib = _bind(lib_path)
     for name in ("decode", "encode", "residual_gate_add", "rmsnorm_modulate",
-                 "gate_add_rmsnorm_modulate", "row_rms_inverse"):
+                 "gate_add_rmsnorm_modulate", "row_rms_inverse", "gelu_tanh", "round_double"):
         fn = getattr(src, name)
         g = dict(fn.__globals__)
         g["_load"] = lambda lib=lib: lib

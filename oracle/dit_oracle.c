@@ -125,6 +125,27 @@ void orc_store(void* p, int64_t i, float v, int dtype) {
   }
 }
 
+/* One rounding of a double to the dtype.  fp32: the C conversion (round to
+ * nearest even).  bf16/fp16: first to fp32 by rounding to odd -- truncate
+ * toward zero, then set the last bit if anything was discarded -- then to the
+ * 16-bit format by round-to-nearest-even.  fp32 keeps at least two bits more
+ * than either 16-bit format, so the two steps give the correctly rounded
+ * result (Boldo and Melquiond, "When double rounding is odd", 2005). */
+void orc_store_double(void* p, int64_t i, double v, int dtype) {
+  if (dtype == ORC_FP32 || isnan(v) || isinf(v)) {
+    orc_store(p, i, (float)v, dtype);
+    return;
+  }
+  float f = (float)v;
+  if (fabs((double)f) > fabs(v)) f = nextafterf(f, 0.0f); /* toward zero */
+  if ((double)f != v && !isinf(f)) {
+    uint32_t b = f32_bits(f);
+    b |= 1u; /* sticky: odd */
+    f = bits_f32(b);
+  }
+  orc_store(p, i, f, dtype);
+}
+
 void orc_decode_array(float* dst_f32, const void* src, int64_t n, int dtype) {
   for (int64_t i = 0; i < n; ++i) dst_f32[i] = orc_load(src, i, dtype);
 }
@@ -187,6 +208,23 @@ static void rmsnorm_modulate_row(void* out, float* t_out, const void* x,
     if (t_out) t_out[r * D + d] = t;
     orc_store(out, r * D + d, y, dtype);
   }
+}
+
+/* gelu(x) = 0.5 * x * (1 + tanh(z)), z = sqrt(2/pi) * (x + 0.044715 * x^3),
+ * in double.  1 + tanh(z) = 2 / (1 + exp(-2z)) exactly, so the value is
+ * computed as x / (1 + exp(-2z)): the same function, without the cancellation
+ * of 1 + tanh(z) when tanh(z) is close to -1 (x below about -4), where even a
+ * double evaluation of the tanh form loses most of its digits. */
+int orc_gelu_tanh(void* out, const void* x, int64_t n, int dtype) {
+  if (n < 0 || (dtype != ORC_BF16 && dtype != ORC_FP16 && dtype != ORC_FP32)) return -1;
+  if (n > 0 && (!out || !x)) return -1;
+  const double k = sqrt(2.0 / 3.14159265358979323846);
+  for (int64_t i = 0; i < n; ++i) {
+    const double v = (double)orc_load(x, i, dtype);
+    const double z = k * (v + 0.044715 * v * v * v);
+    orc_store_double(out, i, v / (1.0 + exp(-2.0 * z)), dtype);
+  }
+  return 0;
 }
 
 /* ------------------------------------------------------------------------ */

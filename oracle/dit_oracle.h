@@ -83,6 +83,15 @@ int orc_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out,
                                   int dtype, int gate_layout, int mod_layout,
                                   const int64_t* rows, int64_t nrows);
 
+/* tanh-approximated GELU, elementwise over n elements:
+ *   gelu(x) = 0.5 * x * (1 + tanh(sqrt(2/pi) * (x + 0.044715 * x^3)))
+ * (the FFN activation of the LTX-2 blocks: prhub summary of sglang PR
+ * #34172, "implementation breakdown" item 3, LTX2FeedForward's tanh-GELU),
+ * evaluated in double and rounded once to the dtype. */
+int orc_gelu_tanh(void* out, const void* x, int64_t n, int dtype);
+/* one rounding of a double to the dtype (round-to-nearest-even) */
+void orc_store_double(void* p, int64_t i, double v, int dtype);
+
 /* The per-row statistic, exposed for the tests: r = 1/sqrt(mean(x^2) + eps)
  * for one row of D elements. */
 float orc_row_rms_inverse(const void* x_row, int64_t D, float eps, int dtype);

@@ -5,7 +5,8 @@ least one pin from the oracle test files fails on it.
 Mistakes planted: a wrong sign, a dropped term, a transposed or wrong
 operand, a wrong row index for a broadcast operand, eps outside the root or
 dropped, a wrong divisor in the mean, a fused multiply-add, wrong rounding of
-the storage dtype, and the fused op reading the unrounded residual.
+the storage dtype, the fused op reading the unrounded residual, and in the
+GELU a wrong coefficient, power, sign or scale, and double rounding.
 """
 import os
 import shutil
@@ -16,6 +17,7 @@ import pytest
 import oracle
 import test_oracle_codecs as pc
 import test_oracle_fused as pf
+import test_oracle_gelu as pg
 import test_oracle_modulate as pm
 import test_oracle_residual_gate as pr
 
@@ -44,6 +46,11 @@ MUTANTS = {
     "bf16_round_half_up": ("x += 0x7FFFu + lsb;", "x += 0x8000u; (void)lsb;"),
     "fp16_truncate": ("float m = nearbyintf(a / ldexpf(1.0f, E - 10));",
                       "float m = truncf(a / ldexpf(1.0f, E - 10));"),
+    "gelu_cubic_coeff": ("0.044715 * v * v * v", "0.04715 * v * v * v"),
+    "gelu_square": ("0.044715 * v * v * v", "0.044715 * v * v"),
+    "gelu_sign": ("v / (1.0 + exp(-2.0 * z))", "v / (1.0 + exp(2.0 * z))"),
+    "gelu_half_z": ("v / (1.0 + exp(-2.0 * z))", "v / (1.0 + exp(-z))"),
+    "double_rounding": ("    b |= 1u; /* sticky: odd */", "    (void)b;"),
     "fused_unrounded": (
         "      rmsnorm_modulate_row(j->out2, j->t_out, j->out, j->scale, j->shift, r,\n"
         "                           j->L, j->D, j->eps, j->dtype, j->layout2);",
@@ -82,6 +89,9 @@ PINS = [
     lambda o: pm.test_worked_examples_golden(o),
     lambda o: pm.test_bcast_equals_expanded_and_batches(o, "bf16"),
     lambda o: pf.test_exact_bruteforce(o, "bf16", (2, 2, 16)),
+    lambda o: pg.test_round_to_odd_avoids_double_rounding(o),
+    lambda o: pg.test_against_torch_float64(o, "bf16"),
+    lambda o: pg.test_against_50_digit_evaluation(o, "fp32"),
 ]
 
 
