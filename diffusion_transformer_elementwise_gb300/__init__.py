@@ -4,6 +4,7 @@ LTX-2-style video diffusion transformers.
 * :func:`residual_gate_add` -- ``hidden + update * gate`` (full or [B, 1, D] gate)
 * :func:`rmsnorm_modulate` -- ``rms_norm(x, eps) * (1 + scale) + shift``
 * :func:`gate_add_rmsnorm_modulate` -- both in one pass
+* :func:`gelu_tanh` -- the feed-forward's tanh-GELU
 
 Each call is one kernel of ``libdit_elementwise.so`` (C ABI in
 ``include/dit_elementwise.h``), launched on the current torch stream.  Build
@@ -12,6 +13,7 @@ the library with :func:`build`; without it every call raises.
 from ._binding import (  # noqa: F401
     DitError,
     gate_add_rmsnorm_modulate,
+    gelu_tanh,
     library,
     residual_gate_add,
     rmsnorm_modulate,

@@ -56,6 +56,8 @@ def library() -> ctypes.CDLL:
             lib.dit_gate_add_rmsnorm_modulate.argtypes = [
                 vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, cf, ci, ci, ci, vp]
             lib.dit_gate_add_rmsnorm_modulate.restype = ci
+            lib.dit_gelu_tanh.argtypes = [vp, vp, i64, ci, vp]
+            lib.dit_gelu_tanh.restype = ci
             lib.dit_residual_gate_add_strided.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci,
                                                           i64, vp]
             lib.dit_residual_gate_add_strided.restype = ci
@@ -215,3 +217,20 @@ def gate_add_rmsnorm_modulate(hidden, update, gate, scale, shift, eps=1e-6,
             float(eps), dt, glay, mlay, vs, _stream(dev, stream))
     check(st, "dit_gate_add_rmsnorm_modulate")
     return residual_out, modulated_out
+
+
+def gelu_tanh(x, out=None, stream=None):
+    """out = 0.5 * x * (1 + tanh(sqrt(2/pi) * (x + 0.044715 * x^3))),
+    elementwise over a contiguous tensor of any shape.  Pass out=x for the
+    in-place form.  Returns out."""
+    if out is None:
+        out = torch.empty_like(x)
+    dev = _cuda(("x", x), ("out", out))
+    dt = _dtype(x, ("out", out))
+    if out.shape != x.shape:
+        raise ValueError("out must have the shape of x")
+    with torch.cuda.device(dev):
+        st = library().dit_gelu_tanh(out.data_ptr(), x.data_ptr(), x.numel(), dt,
+                                     _stream(dev, stream))
+    check(st, "dit_gelu_tanh")
+    return out

@@ -308,6 +308,21 @@ dit_status dit_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out
                     dtype, gate_layout, mod_layout, D, stream);
 }
 
+dit_status dit_gelu_tanh(void* out, const void* x, int64_t n, dit_dtype dtype,
+                         dit_stream_t stream) {
+  if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
+  const int es = elem_size(dtype);
+  int64_t bytes;
+  if (n < 0 || __builtin_mul_overflow(n, (int64_t)es, &bytes)) return DIT_ERR_BAD_SHAPE;
+  if (n == 0) return DIT_OK;
+  if (!out || !x) return DIT_ERR_NULL_PTR;
+  if (misaligned(out, es) || misaligned(x, es)) return DIT_ERR_MISALIGNED;
+  if (out != x && overlaps(span(out, bytes), span(x, bytes))) return DIT_ERR_ALIAS;
+  DeviceInfo dev;
+  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
+  return launch_status(dit::launch_gelu(dev, dtype, out, x, n, (cudaStream_t)stream));
+}
+
 dit_status dit_residual_gate_add_strided(void* out, const void* hidden, const void* update,
                                          const void* gate, int64_t B, int64_t L, int64_t D,
                                          dit_dtype dtype, dit_layout gate_layout,

@@ -86,6 +86,8 @@ cudaError_t launch_rga_bcast(const DeviceInfo& dev, int dtype, int vb,
 cudaError_t launch_modulate(const DeviceInfo& dev, int dtype, int vb,
                             bool mod_full, const RowArgs& a, int64_t B,
                             cudaStream_t stream);
+cudaError_t launch_gelu(const DeviceInfo& dev, int dtype, void* out, const void* x,
+                        int64_t n, cudaStream_t stream);
 cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb,
                          bool gate_full, bool mod_full, const RowArgs& a,
                          int64_t B, cudaStream_t stream);

@@ -3,12 +3,13 @@
  * kernels for the memory-bound elementwise hot path of LTX-2-style video
  * diffusion transformers.
  *
- * Three operations, each one kernel launch on the caller's stream:
+ * Operations, each one kernel launch on the caller's stream:
  *
  *   dit_residual_gate_add          out = hidden + update * gate
  *   dit_rmsnorm_modulate           out = rms_norm(x, eps) * (1 + scale) + shift
  *   dit_gate_add_rmsnorm_modulate  both in one pass: writes the new residual
  *                                  and the modulated input of the next site
+ *   dit_gelu_tanh                  the feed-forward's tanh-GELU, elementwise
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -182,6 +183,24 @@ dit_status dit_gate_add_rmsnorm_modulate_strided(
     int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
     dit_layout gate_layout, dit_layout mod_layout, int64_t vec_stride,
     dit_stream_t stream);
+
+/*
+ * tanh-approximated GELU, elementwise over n contiguous elements:
+ *   out[i] = 0.5 * x[i] * (1 + tanh(z)),  z = sqrt(2/pi) * (x + 0.044715 x^3)
+ * evaluated in fp32 as x * sigmoid(2z) (the same function: 1 + tanh(z) =
+ * 2 / (1 + exp(-2z))), then rounded once to the dtype.  16-bit dtypes use
+ * the fast exp/divide intrinsics (relative error under 1e-4 before the
+ * rounding); fp32 uses expf and an IEEE division.
+ *
+ * Source: prhub summary of sglang PR #34172, "implementation breakdown"
+ * item 3 (LTX2FeedForward: proj_in, then the tanh-GELU act) and "functions
+ * and motivation" (the FFN GELU is the second elementwise chain that
+ * torch.compile fuses).
+ *
+ * out may be x (in place); any other overlap returns DIT_ERR_ALIAS.
+ */
+dit_status dit_gelu_tanh(void* out, const void* x, int64_t n, dit_dtype dtype,
+                         dit_stream_t stream);
 
 #ifdef __cplusplus
 }

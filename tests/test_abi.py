@@ -148,3 +148,14 @@ def test_strided_vectors_validation(lib):
     assert lib.dit_residual_gate_add_strided(O, H, U, G, 1, L, D, BF16, BCAST, 0, None) in (NODEV, LAUNCH, OK)
     # full layouts ignore the stride
     assert lib.dit_residual_gate_add_strided(O, H, U, G, B, L, D, BF16, FULL, 0, None) in (NODEV, LAUNCH, OK)
+
+
+def test_gelu_validation(lib):
+    f = lib.dit_gelu_tanh
+    assert f(O, H, -1, BF16, None) == SHAPE
+    assert f(O, H, 10, 5, None) == DTYPE
+    assert f(None, None, 0, BF16, None) == OK
+    assert f(None, H, 10, BF16, None) == NULLP
+    assert f(O + 1, H, 10, BF16, None) == MISALIGNED
+    assert f(H + 4, H, 10, BF16, None) == ALIAS          # partial overlap
+    assert f(H, H, 10, BF16, None) in (NODEV, LAUNCH, OK)  # in place
