@@ -243,7 +243,23 @@ def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16", only=None):
                   4 * N * es + 3 * vb, [h, u, g, sc, sh], [r, m],
                   sampler("fused", [h, u, g, sc, sh]))
 
+    def gelu_ffn():
+        # the feed-forward activation: [B, L, 4D]
+        x = draw("act", (B, L, 4 * D), seed_for("bench", "ffn"), dtype, device)
+        o = torch.empty_like(x)
+        n4 = 4 * N
+
+        def make(rows):
+            import oracle
+            host = x[:, :rows].contiguous().cpu()
+            res = torch.empty_like(host)
+            return lambda threads: oracle.gelu_tanh(res, host, dtype)
+        return Op("gelu_ffn", lambda: dit.gelu_tanh(x, out=o), 2 * n4 * es, [x], [o], make)
+
     builders = [rga_bcast, rga_bcast_inplace, rga_full, mod_bcast, fused_bcast]
+    extra = {"gelu_ffn": gelu_ffn}
+    if only in extra:
+        return [extra[only]()]
     if only is not None:
         builders = [f for f in builders if f.__name__ == only]
         if not builders:
@@ -466,7 +482,11 @@ def run_ours(args):
         dist.barrier()
     build()  # no-op when up to date
 
-    if args.workload == "chain":
+    if args.workload == "gelu":
+        ops = hotpath_ops(device, only="gelu_ffn")
+        workload = {"workload": "ltx2 feed-forward tanh-GELU on [1,32640,16384] bf16",
+                    "B": 1, "L": 32640, "D": 16384}
+    elif args.workload == "chain":
         ops = chain_ops(device)
         workload = {"workload": "ltx2_chain_b2_s32640_c4096: 8 DiT blocks x 3 sites "
                                 "(1 modulation + 23 fused + 1 residual gate per step)",
@@ -517,7 +537,7 @@ def run_ours(args):
                "ms_per_step": e_max / e_steps}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and args.workload != "chain":
+    if rank == 0 and world == 1 and not args.no_cpu and args.workload == "hotpath":
         cpu = cpu_baseline(ops)
 
     if dist is not None:
@@ -582,6 +602,10 @@ def run_shapes(args):
                   lambda: dit.gate_add_rmsnorm_modulate(h, u, g, sc, sh, EPS, residual_out=o,
                                                         modulated_out=o2),
                   4 * N * es + (3 * vbytes if lay == "bcast" else N * es + 2 * vbytes))]
+        if lay == "bcast" and dt == "bf16" and name.startswith(("ltx2", "flux2_bcast_s4608")):
+            xf = draw("act", (B, L, 4 * D), seed_for(name, "ffn"), dt, dev)
+            of = torch.empty_like(xf)
+            cases.append(("gelu_tanh_ffn_4D", lambda: dit.gelu_tanh(xf, out=of), 2 * 4 * N * es))
         for op, fn, nbytes in cases:
             for _ in range(10):
                 fn()
@@ -617,12 +641,12 @@ def main():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["hotpath", "chain", "shapes"], default="hotpath")
+    p.add_argument("--workload", choices=["hotpath", "chain", "shapes", "gelu"], default="hotpath")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--op", default=None,
                    help="time one op of the hot path only (rga_bcast, rga_bcast_inplace, "
-                        "rga_full, mod_bcast, fused_bcast): for profiling")
+                        "rga_full, mod_bcast, fused_bcast, gelu_ffn): for profiling")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
