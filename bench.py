@@ -162,7 +162,8 @@ def stored_traffic(kernel_key):
 # ---------------------------------------------------------------------------
 
 class Op:
-    def __init__(self, name, fn, nbytes, inputs, outputs, sample):
+    def __init__(self, name, fn, nbytes, inputs, outputs, sample, launches=1):
+        self.launches = launches  # kernels one call of fn launches
         self.name = name
         self.fn = fn            # enqueue the op on the current stream
         self.bytes = nbytes     # algorithmic bytes per call
@@ -267,8 +268,10 @@ def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16", only=None):
     return [f() for f in builders]
 
 
-def chain_ops(device, B=2, L=32640, D=4096, blocks=8, dtype="bf16"):
-    """The chain as one op per launch (so each kernel is timed)."""
+def chain_ops(device, B=2, L=32640, D=4096, blocks=8, dtype="bf16", graph=False):
+    """The chain as one op per launch (so each kernel is timed), or, with
+    graph=True, as one op that replays the whole chain captured in a CUDA
+    graph (timed as a whole)."""
     import torch
 
     import diffusion_transformer_elementwise_gb300 as dit
@@ -278,6 +281,11 @@ def chain_ops(device, B=2, L=32640, D=4096, blocks=8, dtype="bf16"):
     x, updates, tables = chain.make_inputs(B, L, D, blocks, dtype, device, seed_tag="bench")
     m = torch.empty_like(x)
     N, vb = B * L * D, B * D * es
+    if graph:
+        chain.run(x, updates, tables, EPS, m=m)  # first calls outside the capture
+        g, _ = chain.capture(x, updates, tables, EPS, m=m)
+        return [Op("chain_graph", g.replay, chain.algorithmic_bytes(B, L, D, blocks, es),
+                   [x] + updates, [x, m], None, launches=chain.launches(blocks))]
     sites = chain.site_list(blocks)
     ops = []
     s0 = tables[0][chain.SITES[0]]
@@ -487,10 +495,12 @@ def run_ours(args):
         workload = {"workload": "ltx2 feed-forward tanh-GELU on [1,32640,16384] bf16",
                     "B": 1, "L": 32640, "D": 16384}
     elif args.workload == "chain":
-        ops = chain_ops(device)
-        workload = {"workload": "ltx2_chain_b2_s32640_c4096: 8 DiT blocks x 3 sites "
-                                "(1 modulation + 23 fused + 1 residual gate per step)",
-                    "B": 2, "L": 32640, "D": 4096, "blocks": 8}
+        B, L, D = (int(v) for v in args.chain_shape.split(","))
+        ops = chain_ops(device, B, L, D, graph=args.graph)
+        workload = {"workload": f"ltx2_chain_b{B}_s{L}_c{D}: 8 DiT blocks x 3 sites "
+                                "(1 modulation + 23 fused + 1 residual gate per step)"
+                                + (", replayed as one CUDA graph" if args.graph else ""),
+                    "B": B, "L": L, "D": D, "blocks": 8}
     else:
         ops = hotpath_ops(device, only=args.op)
         workload = {"workload": "ltx2_bcast_s32640_c4096 hot path: rga_bcast, "
@@ -498,8 +508,10 @@ def run_ours(args):
                     "B": 1, "L": 32640, "D": 4096}
         if args.op:
             workload["workload"] = f"ltx2_bcast_s32640_c4096 {args.op} only (profiling)"
+    big = args.workload != "chain" or B * L * D * 2 > (129 << 20)
     workload["l2"] = ("no flush: every op reads its own inputs, each 267 MB or more, "
-                      "above the 129 MB L2")
+                      "above the 129 MB L2" if big else
+                      "no flush: the chain's buffers fit in the L2 (launch-bound case)")
     workload["eps"] = EPS
 
     with ClockSampler(local) as clk:
@@ -549,7 +561,8 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic", "config": workload, "roofline": roof,
                 "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": len(ops) * args.steps, "clocks": clocks, "per_op": table}
+                "gpu_launches": sum(op.launches for op in ops) * args.steps, "clocks": clocks,
+                "per_op": table}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -624,13 +637,30 @@ def run_shapes(args):
                 fn()
             e.record()
             torch.cuda.synchronize()
+            b2b = s.elapsed_time(e) / 20
+            # the same 20 calls captured in a CUDA graph: no host work per launch
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(20):
+                    fn()
+            torch.cuda.current_stream().wait_stream(side)
+            graph.replay()
+            s.record()
+            graph.replay()
+            e.record()
+            torch.cuda.synchronize()
+            graph_us = s.elapsed_time(e) / 20 * 1e3
+            del graph
             med = statistics.median(times)
             gbs = nbytes / (med * 1e-3) / 1e9
             print(json.dumps({"shape": name, "op": op, "dtype": dt, "B": B, "L": L, "D": D,
                               "bytes": nbytes, "median_us": med * 1e3,
                               "min_us": min(times) * 1e3, "GB_s": gbs,
                               "frac_of_peak": gbs / peak,
-                              "back_to_back_us": s.elapsed_time(e) / 20 * 1e3}), flush=True)
+                              "back_to_back_us": b2b * 1e3,
+                              "graph_us": graph_us}), flush=True)
         del h, u, g, o, o2
     return 0
 
@@ -642,6 +672,10 @@ def main():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["hotpath", "chain", "shapes", "gelu"], default="hotpath")
+    p.add_argument("--chain-shape", default="2,32640,4096",
+                   help="B,L,D of --workload chain (e.g. 1,126,2048: the audio stream)")
+    p.add_argument("--graph", action="store_true",
+                   help="--workload chain: replay the chain as one captured CUDA graph")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--op", default=None,

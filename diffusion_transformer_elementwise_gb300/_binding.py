@@ -36,6 +36,8 @@ class DitError(RuntimeError):
 def library() -> ctypes.CDLL:
     """The loaded C library (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB):
@@ -84,18 +86,19 @@ def _shape3(t: torch.Tensor, name: str):
 
 
 def _cuda(*tensors):
+    """Checks the tensors; returns the index of their (common) CUDA device."""
     dev = None
     for name, t in tensors:
-        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise TypeError(f"{name} must be a CUDA tensor (there is no CPU path)")
         vector = name in ("gate", "scale", "shift")
         if not t.is_contiguous() and not (vector and _strided_vector(t)):
             raise ValueError(f"{name} must be contiguous" +
                              (" (or a [B, 1, D] view with contiguous rows)" if vector else ""))
         if dev is None:
-            dev = t.device
-        elif t.device != dev:
-            raise ValueError(f"{name} is on {t.device}, expected {dev}")
+            dev = t.get_device()
+        elif t.get_device() != dev:
+            raise ValueError(f"{name} is on cuda:{t.get_device()}, expected cuda:{dev}")
     return dev
 
 
@@ -134,10 +137,25 @@ def layout_of(t: torch.Tensor, B: int, L: int, D: int, name: str) -> int:
     raise ValueError(f"{name} must be [{B}, {L}, {D}] or [{B}, 1, {D}], got {shape}")
 
 
-def _stream(device, stream):
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(dev: int, stream) -> int:
+    """The cudaStream_t to launch on: `stream` (a torch.cuda.Stream or a raw
+    handle), else torch's current stream of device `dev`."""
     if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        if _raw_stream is not None:
+            return _raw_stream(dev)
+        stream = torch.cuda.current_stream(dev)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _launch(dev: int, fn, *args) -> int:
+    """Calls the C entry point with `dev` as the current CUDA device."""
+    if torch.cuda.current_device() == dev:
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 def residual_gate_add(hidden, update, gate, out=None, stream=None):
@@ -152,10 +170,8 @@ def residual_gate_add(hidden, update, gate, out=None, stream=None):
         raise ValueError("update and out must have the shape of hidden")
     lay = layout_of(gate, B, L, D, "gate")
     vs = _vector_stride(D, gate) if lay == ROW_BCAST else D
-    with torch.cuda.device(dev):
-        st = library().dit_residual_gate_add_strided(out.data_ptr(), hidden.data_ptr(),
-                                                     update.data_ptr(), gate.data_ptr(), B, L, D,
-                                                     dt, lay, vs, _stream(dev, stream))
+    st = _launch(dev, library().dit_residual_gate_add_strided, out.data_ptr(), hidden.data_ptr(),
+                 update.data_ptr(), gate.data_ptr(), B, L, D, dt, lay, vs, _stream(dev, stream))
     check(st, "dit_residual_gate_add")
     return out
 
@@ -174,11 +190,9 @@ def rmsnorm_modulate(x, scale, shift, eps=1e-6, out=None, stream=None):
     if layout_of(shift, B, L, D, "shift") != lay:
         raise ValueError("scale and shift must have the same layout")
     vs = _vector_stride(D, scale, shift) if lay == ROW_BCAST else D
-    with torch.cuda.device(dev):
-        st = library().dit_rmsnorm_modulate_strided(out.data_ptr(), x.data_ptr(),
-                                                    scale.data_ptr(), shift.data_ptr(), B, L, D,
-                                                    float(eps), dt, lay, vs,
-                                                    _stream(dev, stream))
+    st = _launch(dev, library().dit_rmsnorm_modulate_strided, out.data_ptr(), x.data_ptr(),
+                 scale.data_ptr(), shift.data_ptr(), B, L, D, float(eps), dt, lay, vs,
+                 _stream(dev, stream))
     check(st, "dit_rmsnorm_modulate")
     return out
 
@@ -210,11 +224,10 @@ def gate_add_rmsnorm_modulate(hidden, update, gate, scale, shift, eps=1e-6,
         raise ValueError("scale and shift must have the same layout")
     vecs = ([gate] if glay == ROW_BCAST else []) + ([scale, shift] if mlay == ROW_BCAST else [])
     vs = _vector_stride(D, *vecs)
-    with torch.cuda.device(dev):
-        st = library().dit_gate_add_rmsnorm_modulate_strided(
-            residual_out.data_ptr(), modulated_out.data_ptr(), hidden.data_ptr(),
-            update.data_ptr(), gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D,
-            float(eps), dt, glay, mlay, vs, _stream(dev, stream))
+    st = _launch(dev, library().dit_gate_add_rmsnorm_modulate_strided,
+                 residual_out.data_ptr(), modulated_out.data_ptr(), hidden.data_ptr(),
+                 update.data_ptr(), gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D,
+                 float(eps), dt, glay, mlay, vs, _stream(dev, stream))
     check(st, "dit_gate_add_rmsnorm_modulate")
     return residual_out, modulated_out
 
@@ -229,8 +242,7 @@ def gelu_tanh(x, out=None, stream=None):
     dt = _dtype(x, ("out", out))
     if out.shape != x.shape:
         raise ValueError("out must have the shape of x")
-    with torch.cuda.device(dev):
-        st = library().dit_gelu_tanh(out.data_ptr(), x.data_ptr(), x.numel(), dt,
-                                     _stream(dev, stream))
+    st = _launch(dev, library().dit_gelu_tanh, out.data_ptr(), x.data_ptr(), x.numel(), dt,
+                 _stream(dev, stream))
     check(st, "dit_gelu_tanh")
     return out

@@ -83,6 +83,23 @@ def run(x, updates, tables, eps=1e-6, m=None, on_site=None, stream=None):
     return x, m
 
 
+def capture(x, updates, tables, eps=1e-6, m=None):
+    """Record one pass of the chain (1 + 3 * blocks launches on x, m and the
+    tables' buffers) in a CUDA graph.  Replaying the graph runs the same
+    kernels on the same buffers -- x is updated in place on every replay --
+    with no host work per launch.  Capturing runs nothing.  Returns (graph, m)."""
+    import torch
+    if m is None:
+        m = torch.empty_like(x)
+    side = torch.cuda.Stream(device=x.device)
+    side.wait_stream(torch.cuda.current_stream(x.device))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        run(x, updates, tables, eps, m=m)
+    torch.cuda.current_stream(x.device).wait_stream(side)
+    return graph, m
+
+
 def launches(blocks: int) -> int:
     return 1 + 3 * blocks
 

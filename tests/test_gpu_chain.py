@@ -84,3 +84,23 @@ def test_chain_full_size_sampled(orc):
 def test_chain_short_every_row(orc):
     B, L, D = 2, 64, 4096
     _run(orc, B, L, D, torch.arange(L))
+
+
+def test_chain_graph_replay_equals_eager():
+    """The chain captured in a CUDA graph and replayed twice gives, bit for
+    bit, what two eager passes give (x is updated in place by each pass).
+    Audio-stream shape [1, 126, 2048]: the launch-bound case a graph is for."""
+    B, L, D = 1, 126, 2048
+    xe, updates, tables = chain.make_inputs(B, L, D, 8, "bf16", "cuda", seed_tag="graph")
+    xg = xe.clone()
+    me = torch.empty_like(xe)
+    for _ in range(2):
+        chain.run(xe, updates, tables, EPS, m=me)
+    graph, mg = chain.capture(xg, updates, tables, EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(xg, chain.make_inputs(B, L, D, 8, "bf16", "cuda", seed_tag="graph")[0])
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(xg.view(torch.int16), xe.view(torch.int16))
+    assert torch.equal(mg.view(torch.int16), me.view(torch.int16))
