@@ -5,6 +5,8 @@ LTX-2-style video diffusion transformers.
 * :func:`rmsnorm_modulate` -- ``rms_norm(x, eps) * (1 + scale) + shift``
 * :func:`gate_add_rmsnorm_modulate` -- both in one pass
 * :func:`gelu_tanh` -- the feed-forward's tanh-GELU
+* ``*_grouped`` -- the first three over several problems (e.g. the video and
+  audio streams of a block) in one launch
 
 Each call is one kernel of ``libdit_elementwise.so`` (C ABI in
 ``include/dit_elementwise.h``), launched on the current torch stream.  Build
@@ -13,9 +15,12 @@ the library with :func:`build`; without it every call raises.
 from ._binding import (  # noqa: F401
     DitError,
     gate_add_rmsnorm_modulate,
+    gate_add_rmsnorm_modulate_grouped,
     gelu_tanh,
     library,
     residual_gate_add,
+    residual_gate_add_grouped,
     rmsnorm_modulate,
+    rmsnorm_modulate_grouped,
 )
 from .build import build  # noqa: F401

@@ -25,6 +25,19 @@ _lock = threading.Lock()
 _lib = None
 
 
+class Problem(ctypes.Structure):
+    """dit_problem of include/dit_elementwise.h."""
+    _fields_ = [("out", ctypes.c_void_p), ("out2", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("update", ctypes.c_void_p), ("gate", ctypes.c_void_p),
+                ("scale", ctypes.c_void_p), ("shift", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("L", ctypes.c_int64), ("D", ctypes.c_int64),
+                ("vec_stride", ctypes.c_int64)]
+
+
+OP_RESIDUAL_GATE, OP_RMSNORM_MODULATE, OP_GATE_ADD_RMSNORM_MODULATE = 0, 1, 2
+MAX_GROUP = 8
+
+
 class DitError(RuntimeError):
     """A dit_* call returned a status other than DIT_OK."""
 
@@ -69,6 +82,8 @@ def library() -> ctypes.CDLL:
             lib.dit_gate_add_rmsnorm_modulate_strided.argtypes = [
                 vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, cf, ci, ci, ci, i64, vp]
             lib.dit_gate_add_rmsnorm_modulate_strided.restype = ci
+            lib.dit_grouped.argtypes = [ci, ctypes.POINTER(Problem), ci, cf, ci, ci, ci, vp]
+            lib.dit_grouped.restype = ci
             _lib = lib
     return _lib
 
@@ -246,3 +261,118 @@ def gelu_tanh(x, out=None, stream=None):
                  _stream(dev, stream))
     check(st, "dit_gelu_tanh")
     return out
+
+
+# ---------------------------------------------------------------------------
+# grouped launches (dit_grouped): one operation over several problems
+# ---------------------------------------------------------------------------
+
+def _group_call(op, problems, eps, dt, glay, mlay, dev, stream, what):
+    if len(problems) > MAX_GROUP:
+        raise ValueError(f"at most {MAX_GROUP} problems per grouped call")
+    arr = (Problem * max(1, len(problems)))(*problems)
+    st = _launch(dev, library().dit_grouped, op, arr, len(problems), float(eps), dt, glay, mlay,
+                 _stream(dev, stream))
+    check(st, what)
+
+
+def _common(values, what):
+    vals = set(values)
+    if len(vals) > 1:
+        raise ValueError(f"the problems of one grouped call must share their {what}")
+    return vals.pop()
+
+
+def residual_gate_add_grouped(problems, stream=None):
+    """out = hidden + update * gate for each (hidden, update, gate[, out]) of
+    `problems` (out None or missing: allocated; out=hidden: in place), in one
+    launch when the problems allow it (dit_grouped).  All problems share the
+    dtype and the gate layout.  Returns the list of outputs."""
+    if not problems:
+        return []
+    descs, outs, devs, dts, lays = [], [], [], [], []
+    for hidden, update, gate, *rest in problems:
+        out = rest[0] if rest and rest[0] is not None else torch.empty_like(hidden)
+        B, L, D = _shape3(hidden, "hidden")
+        devs.append(_cuda(("hidden", hidden), ("update", update), ("gate", gate), ("out", out)))
+        dts.append(_dtype(hidden, ("update", update), ("gate", gate), ("out", out)))
+        if tuple(update.shape) != (B, L, D) or tuple(out.shape) != (B, L, D):
+            raise ValueError("update and out must have the shape of hidden")
+        lay = layout_of(gate, B, L, D, "gate")
+        lays.append(lay)
+        vs = _vector_stride(D, gate) if lay == ROW_BCAST else D
+        descs.append(Problem(out.data_ptr(), None, hidden.data_ptr(), update.data_ptr(),
+                             gate.data_ptr(), None, None, B, L, D, vs))
+        outs.append(out)
+    dev, dt, lay = _common(devs, "device"), _common(dts, "dtype"), _common(lays, "gate layout")
+    _group_call(OP_RESIDUAL_GATE, descs, 0.0, dt, lay, FULL, dev, stream,
+                "dit_grouped(residual gate)")
+    return outs
+
+
+def rmsnorm_modulate_grouped(problems, eps=1e-6, stream=None):
+    """out = rms_norm(x, eps) * (1 + scale) + shift for each
+    (x, scale, shift[, out]) of `problems`, in one launch when the problems
+    allow it (dit_grouped).  All problems share the dtype and the layout of
+    scale/shift.  Returns the list of outputs."""
+    if not problems:
+        return []
+    descs, outs, devs, dts, lays = [], [], [], [], []
+    for x, scale, shift, *rest in problems:
+        out = rest[0] if rest and rest[0] is not None else torch.empty_like(x)
+        B, L, D = _shape3(x, "x")
+        devs.append(_cuda(("x", x), ("scale", scale), ("shift", shift), ("out", out)))
+        dts.append(_dtype(x, ("scale", scale), ("shift", shift), ("out", out)))
+        if tuple(out.shape) != (B, L, D):
+            raise ValueError("out must have the shape of x")
+        lay = layout_of(scale, B, L, D, "scale")
+        if layout_of(shift, B, L, D, "shift") != lay:
+            raise ValueError("scale and shift must have the same layout")
+        lays.append(lay)
+        vs = _vector_stride(D, scale, shift) if lay == ROW_BCAST else D
+        descs.append(Problem(out.data_ptr(), None, x.data_ptr(), None, None, scale.data_ptr(),
+                             shift.data_ptr(), B, L, D, vs))
+        outs.append(out)
+    dev, dt, lay = _common(devs, "device"), _common(dts, "dtype"), _common(lays, "scale layout")
+    _group_call(OP_RMSNORM_MODULATE, descs, eps, dt, FULL, lay, dev, stream,
+                "dit_grouped(modulation)")
+    return outs
+
+
+def gate_add_rmsnorm_modulate_grouped(problems, eps=1e-6, stream=None):
+    """The fused op for each (hidden, update, gate, scale, shift[,
+    residual_out[, modulated_out]]) of `problems`, in one launch when the
+    problems allow it (dit_grouped).  All problems share the dtype, the gate
+    layout and the scale/shift layout.  Returns the list of
+    (residual_out, modulated_out)."""
+    if not problems:
+        return []
+    descs, outs, devs, dts, glays, mlays = [], [], [], [], [], []
+    for hidden, update, gate, scale, shift, *rest in problems:
+        r = rest[0] if len(rest) > 0 and rest[0] is not None else torch.empty_like(hidden)
+        m = rest[1] if len(rest) > 1 and rest[1] is not None else torch.empty_like(hidden)
+        B, L, D = _shape3(hidden, "hidden")
+        devs.append(_cuda(("hidden", hidden), ("update", update), ("gate", gate),
+                          ("scale", scale), ("shift", shift), ("residual_out", r),
+                          ("modulated_out", m)))
+        dts.append(_dtype(hidden, ("update", update), ("gate", gate), ("scale", scale),
+                          ("shift", shift), ("residual_out", r), ("modulated_out", m)))
+        for name, t in (("update", update), ("residual_out", r), ("modulated_out", m)):
+            if tuple(t.shape) != (B, L, D):
+                raise ValueError(f"{name} must have the shape of hidden")
+        glay = layout_of(gate, B, L, D, "gate")
+        mlay = layout_of(scale, B, L, D, "scale")
+        if layout_of(shift, B, L, D, "shift") != mlay:
+            raise ValueError("scale and shift must have the same layout")
+        glays.append(glay)
+        mlays.append(mlay)
+        vecs = ([gate] if glay == ROW_BCAST else []) + ([scale, shift] if mlay == ROW_BCAST else [])
+        descs.append(Problem(r.data_ptr(), m.data_ptr(), hidden.data_ptr(), update.data_ptr(),
+                             gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D,
+                             _vector_stride(D, *vecs)))
+        outs.append((r, m))
+    dev, dt = _common(devs, "device"), _common(dts, "dtype")
+    glay, mlay = _common(glays, "gate layout"), _common(mlays, "scale layout")
+    _group_call(OP_GATE_ADD_RMSNORM_MODULATE, descs, eps, dt, glay, mlay, dev, stream,
+                "dit_grouped(fused)")
+    return outs

@@ -118,6 +118,8 @@ const char* dit_status_string(dit_status s) {
     case DIT_ERR_LAUNCH: return "DIT_ERR_LAUNCH: the CUDA runtime rejected the launch";
     case DIT_ERR_MISALIGNED: return "DIT_ERR_MISALIGNED: a pointer is not aligned to the element size";
     case DIT_ERR_NO_DEVICE: return "DIT_ERR_NO_DEVICE: no current CUDA device";
+    case DIT_ERR_BAD_GROUP:
+      return "DIT_ERR_BAD_GROUP: op is not a dit_op value, or count is outside [0, DIT_MAX_GROUP]";
   }
   return "unknown dit_status";
 }
@@ -138,9 +140,26 @@ bool valid_vector_stride(int64_t B, int64_t D, int64_t vs, int es) {
   return !__builtin_mul_overflow(B - 1, vs, &t) && !__builtin_mul_overflow(t + D, (int64_t)es, &t);
 }
 
-dit_status residual_gate_impl(void* out, const void* hidden, const void* update, const void* gate,
-                              int64_t B, int64_t L, int64_t D, dit_dtype dtype,
-                              dit_layout gate_layout, int64_t vs, dit_stream_t stream) {
+// A validated call of one operation: its kernel arguments, its access width
+// and the byte spans it writes and reads (for the aliasing checks of grouped
+// calls).
+struct Prepared {
+  int op;
+  bool empty;
+  int64_t B;
+  int64_t n;  // B * L * D
+  RowArgs a;
+  int vb;  // widest access dividing every row pointer, the pitch and the stride
+  bool gate_full, mod_full;
+  Span writes[2];
+  int nwrites;
+  Span reads[5];
+  int nreads;
+};
+
+dit_status prepare_rga(void* out, const void* hidden, const void* update, const void* gate,
+                       int64_t B, int64_t L, int64_t D, dit_dtype dtype, dit_layout gate_layout,
+                       int64_t vs, Prepared* p) {
   if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
   if (!valid_layout(gate_layout)) return DIT_ERR_BAD_LAYOUT;
   const int es = elem_size(dtype);
@@ -148,24 +167,25 @@ dit_status residual_gate_impl(void* out, const void* hidden, const void* update,
   if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
   const bool full = gate_layout == DIT_FULL;
   if (!full && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
-  if (n == 0) return DIT_OK;
+  *p = Prepared{};
+  p->op = dit::OP_RGA;
+  p->empty = n == 0;
+  if (p->empty) return DIT_OK;
   if (!out || !hidden || !update || !gate) return DIT_ERR_NULL_PTR;
   if (misaligned(out, es) || misaligned(hidden, es) || misaligned(update, es) ||
       misaligned(gate, es))
     return DIT_ERR_MISALIGNED;
   const int64_t bytes = n * es;
   const Span so = span(out, bytes);
-  if (overlaps(so, span(update, bytes)) ||
-      overlaps(so, span(gate, full ? bytes : vector_span(B, D, vs, es))) ||
+  const Span sg = span(gate, full ? bytes : vector_span(B, D, vs, es));
+  if (overlaps(so, span(update, bytes)) || overlaps(so, sg) ||
       (out != hidden && overlaps(so, span(hidden, bytes))))
     return DIT_ERR_ALIAS;
 
-  DeviceInfo dev;
-  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (full) return launch_status(dit::launch_rga_full(dev, dtype, out, hidden, update, gate, n, s));
-
-  RowArgs a = {};
+  p->B = B;
+  p->n = n;
+  p->gate_full = full;
+  RowArgs& a = p->a;
   a.out = out;
   a.x = hidden;
   a.u = update;
@@ -173,15 +193,22 @@ dit_status residual_gate_impl(void* out, const void* hidden, const void* update,
   a.L = L;
   a.D = D;
   a.rows = B * L;
-  a.vstride = (B > 1 ? vs : D) * es;
+  a.vstride = (B > 1 && !full ? vs : D) * es;
   const uint64_t bits = (uintptr_t)out | (uintptr_t)hidden | (uintptr_t)update |
                         (uintptr_t)gate | (uint64_t)(D * es) | (uint64_t)a.vstride;
-  return launch_status(dit::launch_rga_bcast(dev, dtype, dit::widest_access(bits), a, B, s));
+  p->vb = dit::widest_access(bits);
+  p->writes[0] = so;
+  p->nwrites = 1;
+  p->reads[0] = span(hidden, bytes);
+  p->reads[1] = span(update, bytes);
+  p->reads[2] = sg;
+  p->nreads = 3;
+  return DIT_OK;
 }
 
-dit_status modulate_impl(void* out, const void* x, const void* scale, const void* shift,
-                         int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
-                         dit_layout mod_layout, int64_t vs, dit_stream_t stream) {
+dit_status prepare_modulate(void* out, const void* x, const void* scale, const void* shift,
+                            int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+                            dit_layout mod_layout, int64_t vs, Prepared* p) {
   if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
   if (!valid_layout(mod_layout)) return DIT_ERR_BAD_LAYOUT;
   const int es = elem_size(dtype);
@@ -190,7 +217,10 @@ dit_status modulate_impl(void* out, const void* x, const void* scale, const void
   const bool full = mod_layout == DIT_FULL;
   if (!full && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
   if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
-  if (n == 0) return DIT_OK;
+  *p = Prepared{};
+  p->op = dit::OP_MOD;
+  p->empty = n == 0;
+  if (p->empty) return DIT_OK;
   if (!out || !x || !scale || !shift) return DIT_ERR_NULL_PTR;
   if (misaligned(out, es) || misaligned(x, es) || misaligned(scale, es) || misaligned(shift, es))
     return DIT_ERR_MISALIGNED;
@@ -201,9 +231,10 @@ dit_status modulate_impl(void* out, const void* x, const void* scale, const void
       overlaps(so, span(shift, vbytes)))
     return DIT_ERR_ALIAS;
 
-  DeviceInfo dev;
-  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
-  RowArgs a = {};
+  p->B = B;
+  p->n = n;
+  p->mod_full = full;
+  RowArgs& a = p->a;
   a.out = out;
   a.x = x;
   a.sc = scale;
@@ -217,15 +248,21 @@ dit_status modulate_impl(void* out, const void* x, const void* scale, const void
   a.inv_d = 1.0f / (float)D;
   const uint64_t bits = (uintptr_t)out | (uintptr_t)x | (uintptr_t)scale | (uintptr_t)shift |
                         (uint64_t)(D * es) | (uint64_t)a.vstride;
-  return launch_status(dit::launch_modulate(dev, dtype, dit::widest_access(bits), full, a, B,
-                                            (cudaStream_t)stream));
+  p->vb = dit::widest_access(bits);
+  p->writes[0] = so;
+  p->nwrites = 1;
+  p->reads[0] = span(x, bytes);
+  p->reads[1] = span(scale, vbytes);
+  p->reads[2] = span(shift, vbytes);
+  p->nreads = 3;
+  return DIT_OK;
 }
 
-dit_status fused_impl(void* residual_out, void* modulated_out, const void* hidden,
-                      const void* update, const void* gate, const void* scale, const void* shift,
-                      int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
-                      dit_layout gate_layout, dit_layout mod_layout, int64_t vs,
-                      dit_stream_t stream) {
+dit_status prepare_fused(void* residual_out, void* modulated_out, const void* hidden,
+                         const void* update, const void* gate, const void* scale,
+                         const void* shift, int64_t B, int64_t L, int64_t D, float eps,
+                         dit_dtype dtype, dit_layout gate_layout, dit_layout mod_layout,
+                         int64_t vs, Prepared* p) {
   if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
   if (!valid_layout(gate_layout) || !valid_layout(mod_layout)) return DIT_ERR_BAD_LAYOUT;
   const int es = elem_size(dtype);
@@ -234,7 +271,10 @@ dit_status fused_impl(void* residual_out, void* modulated_out, const void* hidde
   const bool any_bcast = gate_layout == DIT_ROW_BCAST || mod_layout == DIT_ROW_BCAST;
   if (any_bcast && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
   if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
-  if (n == 0) return DIT_OK;
+  *p = Prepared{};
+  p->op = dit::OP_FUSED;
+  p->empty = n == 0;
+  if (p->empty) return DIT_OK;
   if (!residual_out || !modulated_out || !hidden || !update || !gate || !scale || !shift)
     return DIT_ERR_NULL_PTR;
   if (misaligned(residual_out, es) || misaligned(modulated_out, es) || misaligned(hidden, es) ||
@@ -256,9 +296,11 @@ dit_status fused_impl(void* residual_out, void* modulated_out, const void* hidde
     if (overlaps(sr, inputs[i])) return DIT_ERR_ALIAS;
   }
 
-  DeviceInfo dev;
-  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
-  RowArgs a = {};
+  p->B = B;
+  p->n = n;
+  p->gate_full = gate_layout == DIT_FULL;
+  p->mod_full = mod_layout == DIT_FULL;
+  RowArgs& a = p->a;
   a.out = residual_out;
   a.out2 = modulated_out;
   a.x = hidden;
@@ -276,9 +318,62 @@ dit_status fused_impl(void* residual_out, void* modulated_out, const void* hidde
   const uint64_t bits = (uintptr_t)residual_out | (uintptr_t)modulated_out | (uintptr_t)hidden |
                         (uintptr_t)update | (uintptr_t)gate | (uintptr_t)scale |
                         (uintptr_t)shift | (uint64_t)(D * es) | (uint64_t)a.vstride;
-  return launch_status(dit::launch_fused(dev, dtype, dit::widest_access(bits),
-                                         gate_layout == DIT_FULL, mod_layout == DIT_FULL, a, B,
-                                         (cudaStream_t)stream));
+  p->vb = dit::widest_access(bits);
+  p->writes[0] = sr;
+  p->writes[1] = sm;
+  p->nwrites = 2;
+  for (int i = 0; i < 5; ++i) p->reads[i] = inputs[i];
+  p->nreads = 5;
+  return DIT_OK;
+}
+
+// One kernel for one prepared, non-empty call.
+cudaError_t launch_one(const DeviceInfo& dev, int dtype, const Prepared& p, cudaStream_t s) {
+  switch (p.op) {
+    case dit::OP_RGA:
+      if (p.gate_full)
+        return dit::launch_rga_full(dev, dtype, p.a.out, p.a.x, p.a.u, p.a.g, p.n, s);
+      return dit::launch_rga_bcast(dev, dtype, p.vb, p.a, p.B, s);
+    case dit::OP_MOD:
+      return dit::launch_modulate(dev, dtype, p.vb, p.mod_full, p.a, p.B, s);
+    default:
+      return dit::launch_fused(dev, dtype, p.vb, p.gate_full, p.mod_full, p.a, p.B, s);
+  }
+}
+
+dit_status run_one(dit_status st, int dtype, const Prepared& p, dit_stream_t stream) {
+  if (st != DIT_OK || p.empty) return st;
+  DeviceInfo dev;
+  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
+  return launch_status(launch_one(dev, dtype, p, (cudaStream_t)stream));
+}
+
+dit_status residual_gate_impl(void* out, const void* hidden, const void* update, const void* gate,
+                              int64_t B, int64_t L, int64_t D, dit_dtype dtype,
+                              dit_layout gate_layout, int64_t vs, dit_stream_t stream) {
+  Prepared p;
+  const dit_status st = prepare_rga(out, hidden, update, gate, B, L, D, dtype, gate_layout, vs, &p);
+  return run_one(st, dtype, p, stream);
+}
+
+dit_status modulate_impl(void* out, const void* x, const void* scale, const void* shift,
+                         int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+                         dit_layout mod_layout, int64_t vs, dit_stream_t stream) {
+  Prepared p;
+  const dit_status st =
+      prepare_modulate(out, x, scale, shift, B, L, D, eps, dtype, mod_layout, vs, &p);
+  return run_one(st, dtype, p, stream);
+}
+
+dit_status fused_impl(void* residual_out, void* modulated_out, const void* hidden,
+                      const void* update, const void* gate, const void* scale, const void* shift,
+                      int64_t B, int64_t L, int64_t D, float eps, dit_dtype dtype,
+                      dit_layout gate_layout, dit_layout mod_layout, int64_t vs,
+                      dit_stream_t stream) {
+  Prepared p;
+  const dit_status st = prepare_fused(residual_out, modulated_out, hidden, update, gate, scale,
+                                      shift, B, L, D, eps, dtype, gate_layout, mod_layout, vs, &p);
+  return run_one(st, dtype, p, stream);
 }
 
 }  // namespace
@@ -345,6 +440,78 @@ dit_status dit_gate_add_rmsnorm_modulate_strided(
     int64_t vec_stride, dit_stream_t stream) {
   return fused_impl(residual_out, modulated_out, hidden, update, gate, scale, shift, B, L, D, eps,
                     dtype, gate_layout, mod_layout, vec_stride, stream);
+}
+
+dit_status dit_grouped(dit_op op, const dit_problem* problems, int count, float eps,
+                       dit_dtype dtype, dit_layout gate_layout, dit_layout mod_layout,
+                       dit_stream_t stream) {
+  if (op != DIT_OP_RESIDUAL_GATE && op != DIT_OP_RMSNORM_MODULATE &&
+      op != DIT_OP_GATE_ADD_RMSNORM_MODULATE)
+    return DIT_ERR_BAD_GROUP;
+  if (count < 0 || count > DIT_MAX_GROUP) return DIT_ERR_BAD_GROUP;
+  if (count > 0 && !problems) return DIT_ERR_NULL_PTR;
+  Prepared prep[DIT_MAX_GROUP];
+  for (int i = 0; i < count; ++i) {
+    const dit_problem& q = problems[i];
+    dit_status st;
+    if (op == DIT_OP_RESIDUAL_GATE)
+      st = prepare_rga(q.out, q.x, q.update, q.gate, q.B, q.L, q.D, dtype, gate_layout,
+                       q.vec_stride, &prep[i]);
+    else if (op == DIT_OP_RMSNORM_MODULATE)
+      st = prepare_modulate(q.out, q.x, q.scale, q.shift, q.B, q.L, q.D, eps, dtype, mod_layout,
+                            q.vec_stride, &prep[i]);
+    else
+      st = prepare_fused(q.out, q.out2, q.x, q.update, q.gate, q.scale, q.shift, q.B, q.L, q.D,
+                         eps, dtype, gate_layout, mod_layout, q.vec_stride, &prep[i]);
+    if (st != DIT_OK) return st;
+  }
+  // the problems run concurrently: none may write what another reads or writes
+  for (int i = 0; i < count; ++i) {
+    if (prep[i].empty) continue;
+    for (int j = 0; j < count; ++j) {
+      if (j == i || prep[j].empty) continue;
+      for (int w = 0; w < prep[i].nwrites; ++w) {
+        for (int k = 0; k < prep[j].nwrites; ++k)
+          if (overlaps(prep[i].writes[w], prep[j].writes[k])) return DIT_ERR_ALIAS;
+        for (int k = 0; k < prep[j].nreads; ++k)
+          if (overlaps(prep[i].writes[w], prep[j].reads[k])) return DIT_ERR_ALIAS;
+      }
+    }
+  }
+  int live[DIT_MAX_GROUP];
+  int nlive = 0;
+  for (int i = 0; i < count; ++i)
+    if (!prep[i].empty) live[nlive++] = i;
+  if (nlive == 0) return DIT_OK;
+
+  DeviceInfo dev;
+  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool rows_op = !(op == DIT_OP_RESIDUAL_GATE && gate_layout == DIT_FULL);
+  bool staged = nlive > 1 && rows_op;
+  for (int i = 0; i < nlive; ++i) staged = staged && prep[live[i]].vb >= 16;
+  if (staged) {
+    RowArgs a[DIT_MAX_GROUP];
+    int64_t B[DIT_MAX_GROUP];
+    for (int i = 0; i < nlive; ++i) {
+      a[i] = prep[live[i]].a;
+      B[i] = prep[live[i]].B;
+    }
+    cudaError_t e;
+    if (op == DIT_OP_RESIDUAL_GATE)
+      e = dit::launch_rga_grouped(dev, dtype, a, B, nlive, s);
+    else if (op == DIT_OP_RMSNORM_MODULATE)
+      e = dit::launch_modulate_grouped(dev, dtype, mod_layout == DIT_FULL, a, B, nlive, s);
+    else
+      e = dit::launch_fused_grouped(dev, dtype, gate_layout == DIT_FULL, mod_layout == DIT_FULL,
+                                    a, B, nlive, s);
+    if (e != cudaErrorNotSupported) return launch_status(e);
+  }
+  for (int i = 0; i < nlive; ++i) {
+    const cudaError_t e = launch_one(dev, dtype, prep[live[i]], s);
+    if (e != cudaSuccess) return DIT_ERR_LAUNCH;
+  }
+  return DIT_OK;
 }
 
 }  // extern "C"

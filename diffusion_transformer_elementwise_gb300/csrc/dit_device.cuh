@@ -278,13 +278,13 @@ __device__ __forceinline__ F2 f2(float lo, float hi) {
   return r;
 }
 __device__ __forceinline__ float f2_lo(F2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  float lo;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0,t}, %1;\n\t}" : "=f"(lo) : "l"(a.v));
   return lo;
 }
 __device__ __forceinline__ float f2_hi(F2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  float hi;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t,%0}, %1;\n\t}" : "=f"(hi) : "l"(a.v));
   return hi;
 }
 __device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {

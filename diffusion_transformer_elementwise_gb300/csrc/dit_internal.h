@@ -14,6 +14,9 @@ namespace dit {
 
 enum Op { OP_RGA = 0, OP_MOD = 1, OP_FUSED = 2 };
 
+// Most problems one grouped launch takes (DIT_MAX_GROUP of the C ABI).
+constexpr int kMaxGroup = 8;
+
 // Arguments of the flat (full-gate) residual-gate kernel.  Elements
 // [0, n_head) and the n_tail elements after the vector body are handled one
 // at a time; the body is n_vec vectors of the kernel's width.
@@ -91,6 +94,19 @@ cudaError_t launch_gelu(const DeviceInfo& dev, int dtype, void* out, const void*
 cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb,
                          bool gate_full, bool mod_full, const RowArgs& a,
                          int64_t B, cudaStream_t stream);
+
+// Grouped launches of the staged row kernel: `count` problems of one
+// operation, dtype and layout, each with 16-byte aligned rows.  Return
+// cudaErrorNotSupported, having launched nothing, when a problem cannot take
+// the staged kernel (the caller then launches the problems one by one).
+cudaError_t launch_rga_grouped(const DeviceInfo& dev, int dtype, const RowArgs* a,
+                               const int64_t* B, int count, cudaStream_t stream);
+cudaError_t launch_modulate_grouped(const DeviceInfo& dev, int dtype, bool mod_full,
+                                    const RowArgs* a, const int64_t* B, int count,
+                                    cudaStream_t stream);
+cudaError_t launch_fused_grouped(const DeviceInfo& dev, int dtype, bool gate_full,
+                                 bool mod_full, const RowArgs* a, const int64_t* B, int count,
+                                 cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // compile-time dispatch over (dtype, access width)

@@ -107,8 +107,10 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[RC]) {
 #else
 #define DIT_PIPE_BOUNDS __launch_bounds__(512)
 #endif
+// The body of one CTA: CTA `cta` of the problem's grid-stride schedule, on
+// column slice `slice` of the row.
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS>
-__global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
+__device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, const int64_t slice) {
   using G = Granule<T>;
   constexpr int P = G::P;  // fp32 pairs per 16-byte granule
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
@@ -125,11 +127,11 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   const int warp = tid >> 5;
   const int nwarps = nthr >> 5;
 
-  if ((int64_t)blockIdx.x >= a.ngroups) return;  // uniform over the CTA
+  if (cta >= a.ngroups) return;  // uniform over the CTA
   const int64_t pitch = a.D * (int64_t)sizeof(T);
 
   // this thread's granules: t + k * T (+ the column slice of the residual gate)
-  const int64_t g0 = (int64_t)blockIdx.y * nthr * VPT + tid;
+  const int64_t g0 = slice * nthr * VPT + tid;
   bool cval[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) cval[k] = ALLCOLS || g0 + (int64_t)k * nthr < a.nvec;
@@ -176,7 +178,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   const int64_t nbatch = a.ngroups / a.gpb;  // B
   // group position (batch, group within batch) of the next group to issue
   uint32_t issue_stage = base;
-  int64_t ib = (int64_t)blockIdx.x / a.gpb, ig = (int64_t)blockIdx.x - ib * a.gpb;
+  int64_t ib = cta / a.gpb, ig = cta - ib * a.gpb;
   auto advance = [&](int64_t& bb, int64_t& gg) {
     bb += a.step_b;
     gg += a.step_g;
@@ -227,7 +229,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
     for (int j = 0; j < RC; ++j) {
       ss[j] = 0.0f;
       if (CHECK && row0 + j >= rend) continue;
-      const int64_t rowoff = (row0 + j) * pitch;
+      [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch;
       F2 acc[P];  // independent accumulators: no serial FMA chain
 #pragma unroll
       for (int i = 0; i < P; ++i) acc[i] = f2(0.0f, 0.0f);
@@ -310,7 +312,7 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
     }
   };
 
-  int64_t cb = (int64_t)blockIdx.x / a.gpb, cg = (int64_t)blockIdx.x - cb * a.gpb;
+  int64_t cb = cta / a.gpb, cg = cta - cb * a.gpb;
   int64_t vec_b = -1;  // batch whose vectors are in registers
   while (cb < nbatch) {
     cp_async_wait<S - 2>();  // this thread's copies of this group have landed
@@ -329,6 +331,32 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
     advance(cb, cg);
   }
   cp_async_wait<0>();  // no copy may outlive the CTA's shared memory
+}
+
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS>
+__global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
+  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS>(a, blockIdx.x, blockIdx.y);
+}
+
+// Several problems of one operation in one launch: problem p owns the CTAs
+// [begin[p], begin[p+1]), slices[p] per schedule position (column slices of
+// the residual gate's long rows; 1 otherwise).  Every problem runs the same
+// body with the launch's common block size; threads past a problem's
+// narrower row own no granules.
+struct GroupArgs {
+  RowArgs p[kMaxGroup];
+  int64_t begin[kMaxGroup + 1];
+  int32_t slices[kMaxGroup];
+  int32_t count;
+};
+
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL>
+__global__ void DIT_PIPE_BOUNDS pipe_group_kernel(const __grid_constant__ GroupArgs ga) {
+  int p = 0;
+  while (p + 1 < ga.count && (int64_t)blockIdx.x >= ga.begin[p + 1]) ++p;  // uniform
+  const int64_t local = (int64_t)blockIdx.x - ga.begin[p];
+  const int64_t sl = ga.slices[p];
+  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, false>(ga.p[p], local / sl, local - (local / sl) * sl);
 }
 
 // Stages and rows per stage of each operation (tuning builds may override).
@@ -454,6 +482,95 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       if constexpr (SD > 3)
         if (S == 3) return by_cols(std::integral_constant<int, 3>{});
       return by_cols(std::integral_constant<int, 2>{});
+    }
+  });
+}
+
+// Several problems of operation OP in one launch of pipe_group_kernel.  Every
+// problem must take the staged path (16-byte aligned rows; for the reducing
+// operations, rows of at most kPipeBlockMax * VPT granules); returns
+// cudaErrorNotSupported otherwise, having launched nothing.  The block is the
+// widest problem's; one wave of resident CTAs is split over the problems in
+// proportion to their bytes (at least one schedule position each).
+template <int OP, bool GFULL, bool MFULL>
+cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs* args,
+                                const int64_t* B, int count, cudaStream_t stream) {
+  constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
+  constexpr int RC = pipe_rows<OP>();
+  constexpr int VPT = pipe_vpt<OP>();
+  if (count < 1 || count > kMaxGroup) return cudaErrorInvalidValue;
+  const int64_t es = dtype == 2 ? 4 : 2;
+  int block = 32;
+  for (int p = 0; p < count; ++p) {
+    const int64_t nvec = args[p].D * es / 16;
+    const int64_t threads_needed = (nvec + VPT - 1) / VPT;
+    int64_t bp = threads_needed;
+    if (OP == OP_RGA) {
+      if (bp > 256) bp = 256;
+    } else if (bp > kPipeBlockMax) {
+      return cudaErrorNotSupported;
+    }
+    bp = (bp + 31) / 32 * 32;
+    if (bp > block) block = (int)bp;
+  }
+  const size_t per_stage = (size_t)RC * NS * VPT * block * 16;
+  const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
+  constexpr int SD = pipe_stages<OP>();
+  const int S = per_stage * SD <= limit ? SD : 2;
+  if (per_stage * S > limit) return cudaErrorNotSupported;
+
+  return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
+    using T = typename decltype(tt)::type;
+    auto go = [&](auto stages) -> cudaError_t {
+      constexpr int SS_ = decltype(stages)::value;
+      auto kern = pipe_group_kernel<OP, T, VPT, SS_, RC, GFULL, MFULL>;
+      const size_t smem = SS_ * per_stage;
+      static size_t configured[64];
+      const bool cached = dev.device >= 0 && dev.device < 64;
+      if (smem + kStaticSmemReserve > 48 * 1024 && (!cached || configured[dev.device] < smem)) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) {
+          (void)cudaGetLastError();
+          return e;
+        }
+        if (cached) configured[dev.device] = smem;
+      }
+      const int64_t wave = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
+      GroupArgs ga;
+      ga.count = count;
+      ga.begin[0] = 0;
+      double total = 0.0;
+      for (int p = 0; p < count; ++p) total += (double)(B[p] * args[p].L) * (double)args[p].D;
+      for (int p = 0; p < count; ++p) {
+        RowArgs a = args[p];
+        a.nvec = a.D * es / 16;
+        const int64_t sl = OP == OP_RGA ? (a.nvec + (int64_t)block * VPT - 1) / ((int64_t)block * VPT) : 1;
+        a.gpb = (a.L + RC - 1) / RC;
+        a.ngroups = B[p] * a.gpb;
+        const double share = (double)(B[p] * a.L) * (double)a.D / total;
+        int64_t g = (int64_t)((double)wave * share / (double)sl);
+        if (g > a.ngroups) g = a.ngroups;
+        if (g < 1) g = 1;
+        a.step_b = g / a.gpb;
+        a.step_g = g - a.step_b * a.gpb;
+        ga.p[p] = a;
+        ga.slices[p] = (int32_t)sl;
+        ga.begin[p + 1] = ga.begin[p] + g * sl;
+      }
+      for (int p = count; p < kMaxGroup; ++p) {
+        ga.p[p] = RowArgs{};
+        ga.slices[p] = 1;
+        ga.begin[p + 1] = ga.begin[count];
+      }
+      if (ga.begin[count] > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+      kern<<<(unsigned)ga.begin[count], block, smem, stream>>>(ga);
+      return cudaGetLastError();
+    };
+    if constexpr (SD == 2) {
+      return go(std::integral_constant<int, 2>{});
+    } else {
+      return S == SD ? go(std::integral_constant<int, SD>{}) : go(std::integral_constant<int, 2>{});
     }
   });
 }

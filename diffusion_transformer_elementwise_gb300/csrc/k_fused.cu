@@ -20,4 +20,14 @@ cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb, bool gate_ful
                   : launch_row_op<OP_FUSED, false, false>(dev, dtype, vb, a, B, stream);
 }
 
+cudaError_t launch_fused_grouped(const DeviceInfo& dev, int dtype, bool gate_full,
+                                 bool mod_full, const RowArgs* a, const int64_t* B, int count,
+                                 cudaStream_t stream) {
+  if (gate_full)
+    return mod_full ? launch_pipe_grouped<OP_FUSED, true, true>(dev, dtype, a, B, count, stream)
+                    : launch_pipe_grouped<OP_FUSED, true, false>(dev, dtype, a, B, count, stream);
+  return mod_full ? launch_pipe_grouped<OP_FUSED, false, true>(dev, dtype, a, B, count, stream)
+                  : launch_pipe_grouped<OP_FUSED, false, false>(dev, dtype, a, B, count, stream);
+}
+
 }  // namespace dit

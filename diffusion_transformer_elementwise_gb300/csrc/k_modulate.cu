@@ -18,4 +18,11 @@ cudaError_t launch_modulate(const DeviceInfo& dev, int dtype, int vb, bool mod_f
                   : launch_row_op<OP_MOD, false, false>(dev, dtype, vb, a, B, stream);
 }
 
+cudaError_t launch_modulate_grouped(const DeviceInfo& dev, int dtype, bool mod_full,
+                                    const RowArgs* a, const int64_t* B, int count,
+                                    cudaStream_t stream) {
+  return mod_full ? launch_pipe_grouped<OP_MOD, false, true>(dev, dtype, a, B, count, stream)
+                  : launch_pipe_grouped<OP_MOD, false, false>(dev, dtype, a, B, count, stream);
+}
+
 }  // namespace dit

@@ -115,4 +115,9 @@ cudaError_t launch_rga_bcast(const DeviceInfo& dev, int dtype, int vb, const Row
   return launch_row_op<OP_RGA, false, false>(dev, dtype, vb, a, B, stream);
 }
 
+cudaError_t launch_rga_grouped(const DeviceInfo& dev, int dtype, const RowArgs* a,
+                               const int64_t* B, int count, cudaStream_t stream) {
+  return launch_pipe_grouped<OP_RGA, false, false>(dev, dtype, a, B, count, stream);
+}
+
 }  // namespace dit

@@ -10,6 +10,9 @@
  *   dit_gate_add_rmsnorm_modulate  both in one pass: writes the new residual
  *                                  and the modulated input of the next site
  *   dit_gelu_tanh                  the feed-forward's tanh-GELU, elementwise
+ *   dit_grouped                    one of the first three over several
+ *                                  problems (e.g. video and audio streams)
+ *                                  in one launch
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -25,7 +28,8 @@
  * Ownership.  The caller owns all memory.  The library allocates nothing,
  *   keeps no per-call state and never synchronises: each call validates its
  *   arguments on the host, enqueues one kernel on `stream` (0 = the legacy
- *   default stream) and returns.  Outputs are complete once the stream
+ *   default stream; dit_grouped: one kernel, or one per problem as stated
+ *   there) and returns.  Outputs are complete once the stream
  *   reaches that point.
  * Aliasing.  out == hidden (exactly the same pointer) is allowed, as is
  *   residual_out == hidden; any other overlap between an output and another
@@ -72,11 +76,13 @@ typedef enum {
   DIT_ERR_BAD_EPS = 6,      /* eps is negative, infinite or NaN               */
   DIT_ERR_LAUNCH = 7,       /* the CUDA runtime rejected the launch           */
   DIT_ERR_MISALIGNED = 8,   /* a pointer is not aligned to the element size   */
-  DIT_ERR_NO_DEVICE = 9     /* no current CUDA device could be queried        */
+  DIT_ERR_NO_DEVICE = 9,    /* no current CUDA device could be queried        */
+  DIT_ERR_BAD_GROUP = 10    /* dit_grouped: op is not a dit_op value, or count
+                               is outside [0, DIT_MAX_GROUP]                  */
 } dit_status;
 
 /* Version of this interface; bumped on any incompatible change. */
-#define DIT_ABI_VERSION 1
+#define DIT_ABI_VERSION 2
 int dit_abi_version(void);
 
 /* A static, human-readable name for a status code. */
@@ -189,8 +195,8 @@ dit_status dit_gate_add_rmsnorm_modulate_strided(
  *   out[i] = 0.5 * x[i] * (1 + tanh(z)),  z = sqrt(2/pi) * (x + 0.044715 x^3)
  * evaluated in fp32 as x * sigmoid(2z) (the same function: 1 + tanh(z) =
  * 2 / (1 + exp(-2z))), then rounded once to the dtype.  16-bit dtypes use
- * the fast exp/divide intrinsics (relative error under 1e-4 before the
- * rounding); fp32 uses expf and an IEEE division.
+ * the hardware approximations of 2^v and 1/v (each within about 2^-22
+ * relative); fp32 uses expf and an IEEE division.
  *
  * Source: prhub summary of sglang PR #34172, "implementation breakdown"
  * item 3 (LTX2FeedForward: proj_in, then the tanh-GELU act) and "functions
@@ -201,6 +207,62 @@ dit_status dit_gate_add_rmsnorm_modulate_strided(
  */
 dit_status dit_gelu_tanh(void* out, const void* x, int64_t n, dit_dtype dtype,
                          dit_stream_t stream);
+
+/*
+ * Grouped launches: one operation over up to DIT_MAX_GROUP independent
+ * problems of one dtype and layout, each with its own pointers, B, L, D and
+ * vec_stride.  An LTX-2 block applies each of its adaLN modulations to the
+ * video stream (hidden size 4096) and to the audio stream (hidden size 2048)
+ * -- prhub summary of sglang PR #34172, "implementation breakdown" item 3
+ * (the six sites: video/audio self-attention, prompt cross-attention and
+ * feed-forward) and the test section (hidden 4096 = video, 2048 = audio) --
+ * so one grouped call covers both streams of a site.
+ *
+ * Each problem computes exactly what the single call of the same operation
+ * computes: the residual is bitwise that of dit_residual_gate_add, and the
+ * modulated output is within the same bound of the exact statistic (its
+ * fp32 sum of squares may be reduced in another tree order than a single
+ * call's, as the launch's block is that of the widest problem).
+ *
+ * Launch: when every non-empty problem has 16-byte aligned pointers, pitch
+ * and vec_stride and (for the modulating operations) rows of at most 8192
+ * 16-bit or 4096 fp32 elements, the call enqueues ONE kernel on `stream`
+ * that covers all of them, with the CTAs split in proportion to the
+ * problems' sizes.  Otherwise, and for a DIT_FULL gate of the residual gate
+ * (whose flat kernel has no rows), it enqueues one kernel per non-empty
+ * problem, in order.  No problem may write memory that another problem
+ * reads or writes (DIT_ERR_ALIAS), since they run concurrently.
+ *
+ * problems: a HOST array of `count` descriptors (0 <= count <= DIT_MAX_GROUP;
+ * NULL allowed when count == 0), read during the call only.  Validation is
+ * that of the single calls, per problem, before anything is launched; the
+ * first failing problem's status is returned.
+ */
+#define DIT_MAX_GROUP 8
+
+typedef enum {
+  DIT_OP_RESIDUAL_GATE = 0,          /* out = hidden + update * gate */
+  DIT_OP_RMSNORM_MODULATE = 1,       /* out = rms_norm(x) * (1 + scale) + shift */
+  DIT_OP_GATE_ADD_RMSNORM_MODULATE = 2 /* both, fused */
+} dit_op;
+
+typedef struct {
+  void* out;          /* residual gate: out; modulation: out; fused: residual_out */
+  void* out2;         /* fused: modulated_out; NULL otherwise */
+  const void* x;      /* residual gate, fused: hidden; modulation: x */
+  const void* update; /* residual gate, fused */
+  const void* gate;   /* residual gate, fused */
+  const void* scale;  /* modulation, fused */
+  const void* shift;  /* modulation, fused */
+  int64_t B, L, D;
+  int64_t vec_stride; /* as in the _strided calls (elements; D if contiguous) */
+} dit_problem;
+
+/* gate_layout is read by the residual gate and the fused op, mod_layout by
+ * the modulation and the fused op; eps by the modulating operations. */
+dit_status dit_grouped(dit_op op, const dit_problem* problems, int count,
+                       float eps, dit_dtype dtype, dit_layout gate_layout,
+                       dit_layout mod_layout, dit_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -14,7 +14,7 @@ from diffusion_transformer_elementwise_gb300.build import build
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
                       "dit_elementwise.h")
 
-OK, NULLP, SHAPE, DTYPE, LAYOUT, ALIAS, EPS, LAUNCH, MISALIGNED, NODEV = range(10)
+OK, NULLP, SHAPE, DTYPE, LAYOUT, ALIAS, EPS, LAUNCH, MISALIGNED, NODEV, BADGROUP = range(11)
 BF16, FP16, FP32 = 0, 1, 2
 FULL, BCAST = 0, 1
 
@@ -44,7 +44,7 @@ def test_version_and_status_strings(lib):
     m = re.search(r"#define DIT_ABI_VERSION (\d+)", open(HEADER).read())
     assert lib.dit_abi_version() == int(m.group(1))
     seen = set()
-    for code in range(10):
+    for code in range(11):
         s = lib.dit_status_string(code).decode()
         assert s.startswith("DIT_") and s not in seen
         seen.add(s)
@@ -159,3 +159,49 @@ def test_gelu_validation(lib):
     assert f(O + 1, H, 10, BF16, None) == MISALIGNED
     assert f(H + 4, H, 10, BF16, None) == ALIAS          # partial overlap
     assert f(H, H, 10, BF16, None) in (NODEV, LAUNCH, OK)  # in place
+
+
+def test_grouped_validation(lib):
+    from diffusion_transformer_elementwise_gb300._binding import Problem
+    f = lib.dit_grouped
+    RGA, MOD, FUSED = 0, 1, 2
+
+    def probs(*ps):
+        return (Problem * max(1, len(ps)))(*ps)
+
+    n4, n2 = 4 * 8 * 2, 3 * 4 * 2  # bytes of [1,4,8] and [1,3,4] bf16
+    video = Problem(O, O2, H, U, G, S, SH, 1, 4, 8, 8)
+    audio = Problem(O + 4096, O2 + 4096, H + 4096, U + 4096, G + 4096, S + 4096, SH + 4096,
+                    1, 3, 4, 4)
+    assert f(3, probs(video), 1, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
+    assert f(-1, probs(video), 1, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
+    assert f(RGA, probs(video), 9, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
+    assert f(RGA, probs(video), -1, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
+    assert f(RGA, None, 2, 1e-6, BF16, BCAST, BCAST, None) == NULLP
+    assert f(RGA, None, 0, 1e-6, BF16, BCAST, BCAST, None) == OK
+    assert f(FUSED, probs(video, audio), 2, -1.0, BF16, BCAST, BCAST, None) == EPS
+    assert f(FUSED, probs(video, audio), 2, 1e-6, 7, BCAST, BCAST, None) == DTYPE
+    assert f(FUSED, probs(video, audio), 2, 1e-6, BF16, 5, BCAST, None) == LAYOUT
+    # the single-call checks, per problem: the first failing problem's status
+    bad = Problem(O, O2, H, U, G, S, SH, 1, -4, 8, 8)
+    assert f(FUSED, probs(video, bad), 2, 1e-6, BF16, BCAST, BCAST, None) == SHAPE
+    assert f(FUSED, probs(Problem(O, None, H, U, G, S, SH, 1, 4, 8, 8)), 1, 1e-6, BF16,
+             BCAST, BCAST, None) == NULLP
+    assert f(RGA, probs(Problem(O, None, H, U, G, None, None, 1, 4, 8, 8)), 1, 1e-6, BF16,
+             BCAST, BCAST, None) in (NODEV, LAUNCH, OK)  # out2, scale, shift unused
+    # across problems: no output may overlap another problem's tensors
+    clash = Problem(H + 2, O2 + 4096, H + 4096, U + 4096, G + 4096, S + 4096, SH + 4096,
+                    1, 3, 4, 4)  # writes into video's hidden
+    assert f(FUSED, probs(video, clash), 2, 1e-6, BF16, BCAST, BCAST, None) == ALIAS
+    clash2 = Problem(O + 4096, O2 + 8, H + 4096, U + 4096, G + 4096, S + 4096, SH + 4096,
+                     1, 3, 4, 4)  # its modulated output inside video's
+    assert f(FUSED, probs(video, clash2), 2, 1e-6, BF16, BCAST, BCAST, None) == ALIAS
+    # reading the same tensor from two problems is fine (e.g. a shared gate)
+    share = Problem(O + 4096, O2 + 4096, H + 4096, U + 4096, G, S, SH, 1, 3, 4, 4)
+    assert f(FUSED, probs(video, share), 2, 1e-6, BF16, BCAST, BCAST, None) in (NODEV, LAUNCH, OK)
+    # empty problems need no pointers
+    empty = Problem(None, None, None, None, None, None, None, 0, 3, 4, 4)
+    assert f(MOD, probs(empty, empty), 2, 1e-6, BF16, BCAST, BCAST, None) == OK
+    import torch
+    if not torch.cuda.is_available():
+        assert f(FUSED, probs(video, audio), 2, 1e-6, BF16, BCAST, BCAST, None) == NODEV
