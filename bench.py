@@ -309,6 +309,33 @@ def chain_ops(device, B=2, L=32640, D=4096, blocks=8, dtype="bf16", graph=False)
     return ops
 
 
+def chain_av_ops(device, video, audio, blocks=8, dtype="bf16", graph=False, grouped=True):
+    """The chain over a video and an audio stream as ONE op per step: the
+    grouped launches (1 + 3 * blocks kernels) or one launch per stream and
+    site (twice as many), eager or replayed as a CUDA graph."""
+    import torch
+
+    from diffusion_transformer_elementwise_gb300 import chain
+
+    es = 2 if dtype != "fp32" else 4
+    streams = [chain.make_inputs(*shape, blocks, dtype, device, seed_tag=f"bench-av{i}")
+               for i, shape in enumerate((video, audio))]
+    ms = [torch.empty_like(x) for x, _, _ in streams]
+    nbytes = sum(chain.algorithmic_bytes(*shape, blocks, es) for shape in (video, audio))
+    n_launch = chain.launches(blocks) * (1 if grouped else 2)
+    chain.run_streams(streams, EPS, ms=ms, grouped=grouped)  # first calls outside any capture
+    if graph:
+        g, _ = chain.capture_streams(streams, EPS, ms=ms, grouped=grouped)
+        fn = g.replay
+    else:
+        def fn():
+            chain.run_streams(streams, EPS, ms=ms, grouped=grouped)
+    name = "chain_av_" + ("grouped" if grouped else "separate") + ("_graph" if graph else "")
+    ins = [t for x, us, _ in streams for t in [x] + us]
+    outs = [t for x, _, _ in streams for t in [x]] + ms
+    return [Op(name, fn, nbytes, ins, outs, None, launches=n_launch)]
+
+
 # ---------------------------------------------------------------------------
 # timing
 # ---------------------------------------------------------------------------
@@ -494,6 +521,17 @@ def run_ours(args):
         ops = hotpath_ops(device, only="gelu_ffn")
         workload = {"workload": "ltx2 feed-forward tanh-GELU on [1,32640,16384] bf16",
                     "B": 1, "L": 32640, "D": 16384}
+    elif args.workload == "chain_av":
+        video = tuple(int(v) for v in args.chain_shape.split(","))
+        audio = tuple(int(v) for v in args.audio_shape.split(","))
+        ops = chain_av_ops(device, video, audio, graph=args.graph, grouped=not args.separate)
+        B, L, D = video
+        workload = {"workload": f"ltx2 video {list(video)} + audio {list(audio)} bf16 chain: "
+                                f"8 DiT blocks x 3 sites, "
+                                + ("one launch per stream and site" if args.separate else
+                                   "one grouped launch per site for both streams")
+                                + (", replayed as one CUDA graph" if args.graph else ""),
+                    "video": list(video), "audio": list(audio), "blocks": 8}
     elif args.workload == "chain":
         B, L, D = (int(v) for v in args.chain_shape.split(","))
         ops = chain_ops(device, B, L, D, graph=args.graph)
@@ -508,7 +546,7 @@ def run_ours(args):
                     "B": 1, "L": 32640, "D": 4096}
         if args.op:
             workload["workload"] = f"ltx2_bcast_s32640_c4096 {args.op} only (profiling)"
-    big = args.workload != "chain" or B * L * D * 2 > (129 << 20)
+    big = args.workload not in ("chain", "chain_av") or B * L * D * 2 > (129 << 20)
     workload["l2"] = ("no flush: every op reads its own inputs, each 267 MB or more, "
                       "above the 129 MB L2" if big else
                       "no flush: the chain's buffers fit in the L2 (launch-bound case)")
@@ -671,11 +709,16 @@ def main():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["hotpath", "chain", "shapes", "gelu"], default="hotpath")
+    p.add_argument("--workload", choices=["hotpath", "chain", "chain_av", "shapes", "gelu"], default="hotpath")
     p.add_argument("--chain-shape", default="2,32640,4096",
                    help="B,L,D of --workload chain (e.g. 1,126,2048: the audio stream)")
+    p.add_argument("--audio-shape", default="1,126,2048",
+                   help="B,L,D of the audio stream of --workload chain_av")
     p.add_argument("--graph", action="store_true",
-                   help="--workload chain: replay the chain as one captured CUDA graph")
+                   help="--workload chain / chain_av: replay the chain as one captured CUDA graph")
+    p.add_argument("--separate", action="store_true",
+                   help="--workload chain_av: one launch per stream and site instead of "
+                        "one grouped launch per site")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--op", default=None,

@@ -276,8 +276,16 @@ def _group_call(op, problems, eps, dt, glay, mlay, dev, stream, what):
     check(st, what)
 
 
+def _either(layout, L, B, D, vs):
+    """None where both layouts read the same memory (one row per batch and
+    contiguous vectors), so the problem takes the group's layout."""
+    return None if L == 1 and (B <= 1 or vs == D) else layout
+
+
 def _common(values, what):
-    vals = set(values)
+    vals = set(v for v in values if v is not None)
+    if not vals:
+        return FULL
     if len(vals) > 1:
         raise ValueError(f"the problems of one grouped call must share their {what}")
     return vals.pop()
@@ -299,8 +307,8 @@ def residual_gate_add_grouped(problems, stream=None):
         if tuple(update.shape) != (B, L, D) or tuple(out.shape) != (B, L, D):
             raise ValueError("update and out must have the shape of hidden")
         lay = layout_of(gate, B, L, D, "gate")
-        lays.append(lay)
         vs = _vector_stride(D, gate) if lay == ROW_BCAST else D
+        lays.append(_either(lay, L, B, D, vs))
         descs.append(Problem(out.data_ptr(), None, hidden.data_ptr(), update.data_ptr(),
                              gate.data_ptr(), None, None, B, L, D, vs))
         outs.append(out)
@@ -328,8 +336,8 @@ def rmsnorm_modulate_grouped(problems, eps=1e-6, stream=None):
         lay = layout_of(scale, B, L, D, "scale")
         if layout_of(shift, B, L, D, "shift") != lay:
             raise ValueError("scale and shift must have the same layout")
-        lays.append(lay)
         vs = _vector_stride(D, scale, shift) if lay == ROW_BCAST else D
+        lays.append(_either(lay, L, B, D, vs))
         descs.append(Problem(out.data_ptr(), None, x.data_ptr(), None, None, scale.data_ptr(),
                              shift.data_ptr(), B, L, D, vs))
         outs.append(out)
@@ -364,12 +372,12 @@ def gate_add_rmsnorm_modulate_grouped(problems, eps=1e-6, stream=None):
         mlay = layout_of(scale, B, L, D, "scale")
         if layout_of(shift, B, L, D, "shift") != mlay:
             raise ValueError("scale and shift must have the same layout")
-        glays.append(glay)
-        mlays.append(mlay)
         vecs = ([gate] if glay == ROW_BCAST else []) + ([scale, shift] if mlay == ROW_BCAST else [])
+        vs = _vector_stride(D, *vecs)
+        glays.append(_either(glay, L, B, D, vs))
+        mlays.append(_either(mlay, L, B, D, vs))
         descs.append(Problem(r.data_ptr(), m.data_ptr(), hidden.data_ptr(), update.data_ptr(),
-                             gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D,
-                             _vector_stride(D, *vecs)))
+                             gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D, vs))
         outs.append((r, m))
     dev, dt = _common(devs, "device"), _common(dts, "dtype")
     glay, mlay = _common(glays, "gate layout"), _common(mlays, "scale layout")

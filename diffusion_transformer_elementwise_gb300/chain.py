@@ -23,7 +23,14 @@ activations (N = B * L * D elements of s bytes) plus the small vectors.
 """
 from __future__ import annotations
 
-from ._binding import gate_add_rmsnorm_modulate, residual_gate_add, rmsnorm_modulate
+from ._binding import (
+    gate_add_rmsnorm_modulate,
+    gate_add_rmsnorm_modulate_grouped,
+    residual_gate_add,
+    residual_gate_add_grouped,
+    rmsnorm_modulate,
+    rmsnorm_modulate_grouped,
+)
 from .synth import draw, seed_for
 
 SITES = ("sa", "ca", "ff")
@@ -98,6 +105,74 @@ def capture(x, updates, tables, eps=1e-6, m=None):
         run(x, updates, tables, eps, m=m)
     torch.cuda.current_stream(x.device).wait_stream(side)
     return graph, m
+
+
+def run_streams(streams, eps=1e-6, ms=None, grouped=True, stream=None):
+    """The chain over several streams at once -- the video and audio streams
+    of LTX-2 blocks, whose six adaLN sites each modulate both (prhub summary
+    of sglang PR #34172, "implementation breakdown" item 3).  streams: a list
+    of (x, updates, tables) as make_inputs returns, with the same number of
+    blocks.  grouped=True: one grouped launch per site for all streams
+    (1 + 3 * blocks launches); False: one launch per stream and site.
+    Each x is updated in place; returns the list of (x, m)."""
+    import torch
+    blocks = len(streams[0][2])
+    sites = site_list(blocks)
+    if ms is None:
+        ms = [torch.empty_like(x) for x, _, _ in streams]
+
+    def vectors(tables, blk, k):
+        return tables[blk][SITES[k]]
+
+    first = []
+    for (x, _, tables), m in zip(streams, ms):
+        shift, scale, _ = vectors(tables, 0, 0)
+        first.append((x, scale, shift, m))
+    if grouped:
+        rmsnorm_modulate_grouped(first, eps, stream=stream)
+    else:
+        for x, scale, shift, m in first:
+            rmsnorm_modulate(x, scale, shift, eps, out=m, stream=stream)
+    for j, (blk, k) in enumerate(sites):
+        last = j + 1 == len(sites)
+        calls = []
+        for (x, updates, tables), m in zip(streams, ms):
+            gate = vectors(tables, blk, k)[2]
+            if last:
+                calls.append((x, updates[k], gate, x))
+            else:
+                nb, nk = sites[j + 1]
+                shift, scale, _ = vectors(tables, nb, nk)
+                calls.append((x, updates[k], gate, scale, shift, x, m))
+        if grouped:
+            if last:
+                residual_gate_add_grouped(calls, stream=stream)
+            else:
+                gate_add_rmsnorm_modulate_grouped(calls, eps, stream=stream)
+        else:
+            for c in calls:
+                if last:
+                    residual_gate_add(c[0], c[1], c[2], out=c[3], stream=stream)
+                else:
+                    gate_add_rmsnorm_modulate(c[0], c[1], c[2], c[3], c[4], eps, residual_out=c[5],
+                                              modulated_out=c[6], stream=stream)
+    return [(x, m) for (x, _, _), m in zip(streams, ms)]
+
+
+def capture_streams(streams, eps=1e-6, ms=None, grouped=True):
+    """run_streams recorded in a CUDA graph (nothing runs while capturing).
+    Returns (graph, ms)."""
+    import torch
+    x0 = streams[0][0]
+    if ms is None:
+        ms = [torch.empty_like(x) for x, _, _ in streams]
+    side = torch.cuda.Stream(device=x0.device)
+    side.wait_stream(torch.cuda.current_stream(x0.device))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        run_streams(streams, eps, ms=ms, grouped=grouped)
+    torch.cuda.current_stream(x0.device).wait_stream(side)
+    return graph, ms
 
 
 def launches(blocks: int) -> int:

@@ -342,7 +342,12 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
 // [begin[p], begin[p+1]), slices[p] per schedule position (column slices of
 // the residual gate's long rows; 1 otherwise).  Every problem runs the same
 // body with the launch's common block size; threads past a problem's
-// narrower row own no granules.
+// narrower row own no granules.  Problem 0 is the largest: its CTAs read
+// their arguments as constant-bank operands, exactly as the single-problem
+// kernel does (ALLCOLS0: its rows fill every thread's granules); the other
+// problems' CTAs first copy their arguments to shared memory, since a kernel
+// parameter selected by a runtime index is not a constant-bank operand and
+// the body reads some of them for every row group.
 struct GroupArgs {
   RowArgs p[kMaxGroup];
   int64_t begin[kMaxGroup + 1];
@@ -350,13 +355,34 @@ struct GroupArgs {
   int32_t count;
 };
 
-template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL>
-__global__ void DIT_PIPE_BOUNDS pipe_group_kernel(const __grid_constant__ GroupArgs ga) {
-  int p = 0;
+// Two bodies are inlined; the register bound keeps the modulation at the
+// occupancy of its single-problem kernel (<= 64 registers: four 256-thread
+// CTAs per SM).  The residual gate's ring (RC rows per stage) and the fused
+// op's registers hold them at fewer CTAs per SM anyway.
+template <int OP>
+constexpr int group_min_blocks() { return OP == OP_MOD ? 2 : 1; }
+
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS0>
+__global__ void __launch_bounds__(512, group_min_blocks<OP>())
+    pipe_group_kernel(const __grid_constant__ GroupArgs ga) {
+  if ((int64_t)blockIdx.x < ga.begin[1]) {  // uniform over the CTA
+    const int64_t sl = ga.slices[0];
+    const int64_t cta = (int64_t)blockIdx.x / sl;
+    pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS0>(ga.p[0], cta, (int64_t)blockIdx.x - cta * sl);
+    return;
+  }
+  int p = 1;
   while (p + 1 < ga.count && (int64_t)blockIdx.x >= ga.begin[p + 1]) ++p;  // uniform
   const int64_t local = (int64_t)blockIdx.x - ga.begin[p];
   const int64_t sl = ga.slices[p];
-  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, false>(ga.p[p], local / sl, local - (local / sl) * sl);
+  static_assert(sizeof(RowArgs) % 8 == 0, "RowArgs is copied in 8-byte words");
+  __shared__ __align__(16) RowArgs sa;
+  if (threadIdx.x < sizeof(RowArgs) / 8)
+    reinterpret_cast<uint64_t*>(&sa)[threadIdx.x] =
+        reinterpret_cast<const uint64_t*>(&ga.p[p])[threadIdx.x];
+  __syncthreads();
+  const int64_t cta = local / sl;
+  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, false>(sa, cta, local - cta * sl);
 }
 
 // Stages and rows per stage of each operation (tuning builds may override).
@@ -491,15 +517,29 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
 // operations, rows of at most kPipeBlockMax * VPT granules); returns
 // cudaErrorNotSupported otherwise, having launched nothing.  The block is the
 // widest problem's; one wave of resident CTAs is split over the problems in
-// proportion to their bytes (at least one schedule position each).
+// proportion to their row groups (at least one schedule position each).
 template <int OP, bool GFULL, bool MFULL>
-cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs* args,
-                                const int64_t* B, int count, cudaStream_t stream) {
+cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs* args_in,
+                                const int64_t* B_in, int count, cudaStream_t stream) {
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
   constexpr int RC = pipe_rows<OP>();
   constexpr int VPT = pipe_vpt<OP>();
   if (count < 1 || count > kMaxGroup) return cudaErrorInvalidValue;
   const int64_t es = dtype == 2 ? 4 : 2;
+  // the largest problem (most elements) first; the others keep their order
+  RowArgs args[kMaxGroup];
+  int64_t B[kMaxGroup];
+  int first = 0;
+  for (int p = 1; p < count; ++p)
+    if (B_in[p] * args_in[p].L * args_in[p].D > B_in[first] * args_in[first].L * args_in[first].D)
+      first = p;
+  args[0] = args_in[first];
+  B[0] = B_in[first];
+  for (int p = 0, q = 1; p < count; ++p)
+    if (p != first) {
+      args[q] = args_in[p];
+      B[q++] = B_in[p];
+    }
   int block = 32;
   for (int p = 0; p < count; ++p) {
     const int64_t nvec = args[p].D * es / 16;
@@ -518,12 +558,20 @@ cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs*
   constexpr int SD = pipe_stages<OP>();
   const int S = per_stage * SD <= limit ? SD : 2;
   if (per_stage * S > limit) return cudaErrorNotSupported;
+  int64_t sl[kMaxGroup], units[kMaxGroup], total = 0;
+  for (int p = 0; p < count; ++p) {
+    const int64_t nvec = args[p].D * es / 16;
+    sl[p] = OP == OP_RGA ? (nvec + (int64_t)block * VPT - 1) / ((int64_t)block * VPT) : 1;
+    units[p] = B[p] * ((args[p].L + RC - 1) / RC) * sl[p];
+    total += units[p];
+  }
+  const bool allcols0 = (int64_t)block * VPT * sl[0] == args[0].D * es / 16;
 
   return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
     using T = typename decltype(tt)::type;
-    auto go = [&](auto stages) -> cudaError_t {
+    auto go = [&](auto stages, auto cols) -> cudaError_t {
       constexpr int SS_ = decltype(stages)::value;
-      auto kern = pipe_group_kernel<OP, T, VPT, SS_, RC, GFULL, MFULL>;
+      auto kern = pipe_group_kernel<OP, T, VPT, SS_, RC, GFULL, MFULL, decltype(cols)::value>;
       const size_t smem = SS_ * per_stage;
       static size_t configured[64];
       const bool cached = dev.device >= 0 && dev.device < 64;
@@ -537,26 +585,43 @@ cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs*
         if (cached) configured[dev.device] = smem;
       }
       const int64_t wave = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
+      // Work units: (row group, column slice) pairs.  A CTA streams its
+      // groups one after another, about one per memory round trip, so every
+      // problem gets CTAs in proportion to its units -- each CTA then takes
+      // about the same number of groups, and a small problem (a short audio
+      // stream) is not left to a few CTAs that finish last: units * wave /
+      // total schedule positions, at least one and at most the problem's
+      // groups.  The largest problem gives back what the minimums
+      // take, so the grid stays within one wave (a CTA past the wave would
+      // start only when another finishes).  The smaller problems round up:
+      // their CTAs must not be the last to finish.
+      int64_t cps[kMaxGroup], used = 0;
+      for (int p = 0; p < count; ++p) {
+        const int64_t ng = B[p] * ((args[p].L + RC - 1) / RC);
+        const double want = (double)units[p] * (double)wave / (double)total / (double)sl[p];
+        int64_t g = p == 0 ? (int64_t)want : (int64_t)ceil(want);
+        if (g > ng) g = ng;
+        if (g < 1) g = 1;
+        cps[p] = g;
+        used += g * sl[p];
+      }
+      if (used > wave) {
+        const int64_t give = (used - wave + sl[0] - 1) / sl[0];
+        cps[0] = cps[0] > give ? cps[0] - give : 1;
+      }
       GroupArgs ga;
       ga.count = count;
       ga.begin[0] = 0;
-      double total = 0.0;
-      for (int p = 0; p < count; ++p) total += (double)(B[p] * args[p].L) * (double)args[p].D;
       for (int p = 0; p < count; ++p) {
         RowArgs a = args[p];
         a.nvec = a.D * es / 16;
-        const int64_t sl = OP == OP_RGA ? (a.nvec + (int64_t)block * VPT - 1) / ((int64_t)block * VPT) : 1;
         a.gpb = (a.L + RC - 1) / RC;
         a.ngroups = B[p] * a.gpb;
-        const double share = (double)(B[p] * a.L) * (double)a.D / total;
-        int64_t g = (int64_t)((double)wave * share / (double)sl);
-        if (g > a.ngroups) g = a.ngroups;
-        if (g < 1) g = 1;
-        a.step_b = g / a.gpb;
-        a.step_g = g - a.step_b * a.gpb;
+        a.step_b = cps[p] / a.gpb;
+        a.step_g = cps[p] - a.step_b * a.gpb;
         ga.p[p] = a;
-        ga.slices[p] = (int32_t)sl;
-        ga.begin[p + 1] = ga.begin[p] + g * sl;
+        ga.slices[p] = (int32_t)sl[p];
+        ga.begin[p + 1] = ga.begin[p] + cps[p] * sl[p];
       }
       for (int p = count; p < kMaxGroup; ++p) {
         ga.p[p] = RowArgs{};
@@ -567,10 +632,14 @@ cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs*
       kern<<<(unsigned)ga.begin[count], block, smem, stream>>>(ga);
       return cudaGetLastError();
     };
+    auto by_cols = [&](auto stages) -> cudaError_t {
+      return allcols0 ? go(stages, std::true_type{}) : go(stages, std::false_type{});
+    };
     if constexpr (SD == 2) {
-      return go(std::integral_constant<int, 2>{});
+      return by_cols(std::integral_constant<int, 2>{});
     } else {
-      return S == SD ? go(std::integral_constant<int, SD>{}) : go(std::integral_constant<int, 2>{});
+      return S == SD ? by_cols(std::integral_constant<int, SD>{})
+                     : by_cols(std::integral_constant<int, 2>{});
     }
   });
 }
