@@ -7,6 +7,8 @@ LTX-2-style video diffusion transformers.
 * :func:`gelu_tanh` -- the feed-forward's tanh-GELU
 * ``*_grouped`` -- the first three over several problems (e.g. the video and
   audio streams of a block) in one launch
+* :func:`selfcheck` / :func:`ensure_checked` -- bit-for-bit check of one
+  runtime key (op, dtype, layouts, D) on the GPU
 
 Each call is one kernel of ``libdit_elementwise.so`` (C ABI in
 ``include/dit_elementwise.h``), launched on the current torch stream.  Build
@@ -14,6 +16,7 @@ the library with :func:`build`; without it every call raises.
 """
 from ._binding import (  # noqa: F401
     DitError,
+    ensure_checked,
     gate_add_rmsnorm_modulate,
     gate_add_rmsnorm_modulate_grouped,
     gelu_tanh,
@@ -22,5 +25,7 @@ from ._binding import (  # noqa: F401
     residual_gate_add_grouped,
     rmsnorm_modulate,
     rmsnorm_modulate_grouped,
+    selfcheck,
+    set_first_use_check,
 )
 from .build import build  # noqa: F401

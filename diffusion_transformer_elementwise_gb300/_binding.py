@@ -84,6 +84,10 @@ def library() -> ctypes.CDLL:
             lib.dit_gate_add_rmsnorm_modulate_strided.restype = ci
             lib.dit_grouped.argtypes = [ci, ctypes.POINTER(Problem), ci, cf, ci, ci, ci, vp]
             lib.dit_grouped.restype = ci
+            lib.dit_selfcheck_workspace_bytes.argtypes = [ci, ci, i64]
+            lib.dit_selfcheck_workspace_bytes.restype = i64
+            lib.dit_selfcheck.argtypes = [ci, ci, ci, ci, i64, vp, i64, vp, vp]
+            lib.dit_selfcheck.restype = ci
             _lib = lib
     return _lib
 
@@ -185,6 +189,8 @@ def residual_gate_add(hidden, update, gate, out=None, stream=None):
         raise ValueError("update and out must have the shape of hidden")
     lay = layout_of(gate, B, L, D, "gate")
     vs = _vector_stride(D, gate) if lay == ROW_BCAST else D
+    if _first_use:
+        _first_use_check("residual_gate", hidden.dtype, lay, ROW_BCAST, D, dev)
     st = _launch(dev, library().dit_residual_gate_add_strided, out.data_ptr(), hidden.data_ptr(),
                  update.data_ptr(), gate.data_ptr(), B, L, D, dt, lay, vs, _stream(dev, stream))
     check(st, "dit_residual_gate_add")
@@ -205,6 +211,8 @@ def rmsnorm_modulate(x, scale, shift, eps=1e-6, out=None, stream=None):
     if layout_of(shift, B, L, D, "shift") != lay:
         raise ValueError("scale and shift must have the same layout")
     vs = _vector_stride(D, scale, shift) if lay == ROW_BCAST else D
+    if _first_use:
+        _first_use_check("rmsnorm_modulate", x.dtype, ROW_BCAST, lay, D, dev)
     st = _launch(dev, library().dit_rmsnorm_modulate_strided, out.data_ptr(), x.data_ptr(),
                  scale.data_ptr(), shift.data_ptr(), B, L, D, float(eps), dt, lay, vs,
                  _stream(dev, stream))
@@ -239,6 +247,8 @@ def gate_add_rmsnorm_modulate(hidden, update, gate, scale, shift, eps=1e-6,
         raise ValueError("scale and shift must have the same layout")
     vecs = ([gate] if glay == ROW_BCAST else []) + ([scale, shift] if mlay == ROW_BCAST else [])
     vs = _vector_stride(D, *vecs)
+    if _first_use:
+        _first_use_check("gate_add_rmsnorm_modulate", hidden.dtype, glay, mlay, D, dev)
     st = _launch(dev, library().dit_gate_add_rmsnorm_modulate_strided,
                  residual_out.data_ptr(), modulated_out.data_ptr(), hidden.data_ptr(),
                  update.data_ptr(), gate.data_ptr(), scale.data_ptr(), shift.data_ptr(), B, L, D,
@@ -384,3 +394,78 @@ def gate_add_rmsnorm_modulate_grouped(problems, eps=1e-6, stream=None):
     _group_call(OP_GATE_ADD_RMSNORM_MODULATE, descs, eps, dt, glay, mlay, dev, stream,
                 "dit_grouped(fused)")
     return outs
+
+
+# ---------------------------------------------------------------------------
+# self-check of runtime keys (dit_selfcheck)
+# ---------------------------------------------------------------------------
+
+OPS = {"residual_gate": OP_RESIDUAL_GATE, "rmsnorm_modulate": OP_RMSNORM_MODULATE,
+       "gate_add_rmsnorm_modulate": OP_GATE_ADD_RMSNORM_MODULATE}
+LAYOUTS = {"full": FULL, "bcast": ROW_BCAST}
+_NAMES = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
+_CODES = {"bf16": 0, "fp16": 1, "fp32": 2}
+
+
+def selfcheck(op, dtype, gate_layout="bcast", mod_layout="bcast", D=4096, device=None,
+              stream=None, return_workspace=False):
+    """Run dit_selfcheck for the key (op, dtype, gate_layout, mod_layout, D)
+    on a [2, 7, D] problem and return the number of output words that differ
+    from their one correct value (0: the key's path computes the
+    definition).  Synchronises the stream to read the count.  op: a key of
+    OPS; dtype: "bf16", "fp16" or "fp32" (or a torch dtype); layouts: "full"
+    or "bcast".  return_workspace=True also returns the workspace (a uint8
+    device tensor laid out as include/dit_elementwise.h states)."""
+    opc = OPS[op] if isinstance(op, str) else int(op)
+    dt = _CODES[_NAMES.get(dtype, dtype)]
+    dev = torch.cuda.current_device() if device is None else torch.device(device).index
+    nbytes = library().dit_selfcheck_workspace_bytes(opc, dt, int(D))
+    if nbytes < 0:
+        raise ValueError(f"no self-check for op={op!r} dtype={dtype!r} D={D}")
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=f"cuda:{dev}")
+    off = (-ws.data_ptr()) % 256
+    work = ws[off:off + nbytes]
+    count = torch.zeros(1, dtype=torch.int32, device=f"cuda:{dev}")
+    st = _launch(dev, library().dit_selfcheck, opc, dt, LAYOUTS[gate_layout],
+                 LAYOUTS[mod_layout], int(D), work.data_ptr(), nbytes, count.data_ptr(),
+                 _stream(dev, stream))
+    check(st, "dit_selfcheck")
+    n = int(count.item())
+    return (n, work) if return_workspace else n
+
+
+_checked: set = set()
+_first_use = False
+
+
+def ensure_checked(op, dtype, gate_layout="bcast", mod_layout="bcast", D=4096, device=None):
+    """Self-check the key once per process (the pages' first-use guard,
+    without a fallback).  Raises DitError with status -1 if any output word
+    differs (the key is then not recorded); returns True if the check ran
+    now, False if the key had passed before.  The check covers the kernel
+    the library picks for 256-byte aligned tensors of row width D."""
+    dt = _NAMES.get(dtype, dtype)
+    dev = torch.cuda.current_device() if device is None else torch.device(device).index
+    key = (op, dt, gate_layout, mod_layout, int(D), dev)
+    if key in _checked:
+        return False
+    n = selfcheck(op, dt, gate_layout, mod_layout, D, device=dev)
+    if n:
+        raise DitError(-1, f"self-check failed for {key}: {n} output words differ")
+    _checked.add(key)
+    return True
+
+
+def set_first_use_check(enabled: bool) -> None:
+    """When enabled, the first call of each runtime key (op, dtype, layouts,
+    D, device) through residual_gate_add, rmsnorm_modulate and
+    gate_add_rmsnorm_modulate runs ensure_checked first (one synchronisation
+    per new key).  Off by default."""
+    global _first_use
+    _first_use = bool(enabled)
+
+
+def _first_use_check(op, dtype, glay, mlay, D, dev):
+    if _first_use:
+        names = {FULL: "full", ROW_BCAST: "bcast"}
+        ensure_checked(op, dtype, names[glay], names[mlay], D, device=dev)

@@ -118,8 +118,10 @@ const char* dit_status_string(dit_status s) {
     case DIT_ERR_LAUNCH: return "DIT_ERR_LAUNCH: the CUDA runtime rejected the launch";
     case DIT_ERR_MISALIGNED: return "DIT_ERR_MISALIGNED: a pointer is not aligned to the element size";
     case DIT_ERR_NO_DEVICE: return "DIT_ERR_NO_DEVICE: no current CUDA device";
-    case DIT_ERR_BAD_GROUP:
-      return "DIT_ERR_BAD_GROUP: op is not a dit_op value, or count is outside [0, DIT_MAX_GROUP]";
+    case DIT_ERR_BAD_OP:
+      return "DIT_ERR_BAD_OP: op is not a dit_op value, or count is outside [0, DIT_MAX_GROUP]";
+    case DIT_ERR_WORKSPACE:
+      return "DIT_ERR_WORKSPACE: workspace NULL, too small or not 256-byte aligned";
   }
   return "unknown dit_status";
 }
@@ -447,8 +449,8 @@ dit_status dit_grouped(dit_op op, const dit_problem* problems, int count, float 
                        dit_stream_t stream) {
   if (op != DIT_OP_RESIDUAL_GATE && op != DIT_OP_RMSNORM_MODULATE &&
       op != DIT_OP_GATE_ADD_RMSNORM_MODULATE)
-    return DIT_ERR_BAD_GROUP;
-  if (count < 0 || count > DIT_MAX_GROUP) return DIT_ERR_BAD_GROUP;
+    return DIT_ERR_BAD_OP;
+  if (count < 0 || count > DIT_MAX_GROUP) return DIT_ERR_BAD_OP;
   if (count > 0 && !problems) return DIT_ERR_NULL_PTR;
   Prepared prep[DIT_MAX_GROUP];
   for (int i = 0; i < count; ++i) {
@@ -512,6 +514,104 @@ dit_status dit_grouped(dit_op op, const dit_problem* problems, int count, float 
     if (e != cudaSuccess) return DIT_ERR_LAUNCH;
   }
   return DIT_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// self-check of one runtime key
+// ---------------------------------------------------------------------------
+
+namespace {
+constexpr int kCheckB = 2, kCheckL = 7;  // rows: 7 per batch (ragged for 4-row groups)
+constexpr int64_t kCheckAlign = 256;
+
+bool valid_op(int op) {
+  return op == DIT_OP_RESIDUAL_GATE || op == DIT_OP_RMSNORM_MODULATE ||
+         op == DIT_OP_GATE_ADD_RMSNORM_MODULATE;
+}
+
+// bytes of one workspace tensor (N = 14 * D elements, rounded up to 256);
+// -1 on overflow or a bad size
+int64_t check_slot_bytes(dit_dtype dtype, int64_t D) {
+  if (D <= 0 || !valid_dtype(dtype)) return -1;
+  int64_t n;
+  if (!element_count(kCheckB, kCheckL, D, elem_size(dtype), &n)) return -1;
+  const int64_t bytes = n * elem_size(dtype);
+  if (bytes > ((int64_t)1 << 40)) return -1;
+  return (bytes + kCheckAlign - 1) / kCheckAlign * kCheckAlign;
+}
+}  // namespace
+
+extern "C" {
+
+int64_t dit_selfcheck_workspace_bytes(dit_op op, dit_dtype dtype, int64_t D) {
+  if (!valid_op(op)) return -1;
+  const int64_t slot = check_slot_bytes(dtype, D);
+  if (slot < 0) return -1;
+  return 9 * slot + kCheckAlign;  // nine tensors, then the row statistics
+}
+
+dit_status dit_selfcheck(dit_op op, dit_dtype dtype, dit_layout gate_layout,
+                         dit_layout mod_layout, int64_t D, void* workspace,
+                         int64_t workspace_bytes, unsigned int* mismatches,
+                         dit_stream_t stream) {
+  if (!valid_op(op)) return DIT_ERR_BAD_OP;
+  if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
+  if (!valid_layout(gate_layout) || !valid_layout(mod_layout)) return DIT_ERR_BAD_LAYOUT;
+  const int64_t slot = check_slot_bytes(dtype, D);
+  if (slot < 0) return DIT_ERR_BAD_SHAPE;
+  if (!mismatches) return DIT_ERR_NULL_PTR;
+  if (((uintptr_t)mismatches & 3) != 0) return DIT_ERR_MISALIGNED;
+  if (!workspace || ((uintptr_t)workspace & (uintptr_t)(kCheckAlign - 1)) != 0 ||
+      workspace_bytes < 9 * slot + kCheckAlign)
+    return DIT_ERR_WORKSPACE;
+  const Span sw = span(workspace, 9 * slot + kCheckAlign);
+  if (overlaps(sw, span(mismatches, 4))) return DIT_ERR_ALIAS;
+
+  dit::SelfcheckArgs a = {};
+  for (int i = 0; i < 9; ++i) a.t[i] = (char*)workspace + i * slot;
+  a.rstat = (float*)((char*)workspace + 9 * slot);
+  a.D = D;
+  a.B = kCheckB;
+  a.L = kCheckL;
+  a.dtype = dtype;
+  a.eps = 0.75f;
+  a.gate_full = gate_layout == DIT_FULL;
+  a.mod_full = mod_layout == DIT_FULL;
+
+  // the operation through the public call's own validation
+  Prepared p;
+  dit_status st;
+  if (op == DIT_OP_RESIDUAL_GATE) {
+    a.op = dit::OP_RGA;
+    a.mod_full = false;
+    st = prepare_rga(a.t[5], a.t[0], a.t[1], a.t[2], kCheckB, kCheckL, D, dtype, gate_layout, D,
+                     &p);
+  } else if (op == DIT_OP_RMSNORM_MODULATE) {
+    a.op = dit::OP_MOD;
+    a.gate_full = false;
+    st = prepare_modulate(a.t[5], a.t[0], a.t[3], a.t[4], kCheckB, kCheckL, D, a.eps, dtype,
+                          mod_layout, D, &p);
+  } else {
+    a.op = dit::OP_FUSED;
+    st = prepare_fused(a.t[5], a.t[6], a.t[0], a.t[1], a.t[2], a.t[3], a.t[4], kCheckB, kCheckL,
+                       D, a.eps, dtype, gate_layout, mod_layout, D, &p);
+  }
+  if (st != DIT_OK) return st;
+
+  DeviceInfo dev;
+  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(mismatches, 0, sizeof(unsigned int), s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return DIT_ERR_LAUNCH;
+  }
+  cudaError_t e = dit::launch_selfcheck_fill(a, s);
+  if (e == cudaSuccess) e = launch_one(dev, dtype, p, s);
+  if (e == cudaSuccess) e = dit::launch_selfcheck_reference(a, s);
+  if (e == cudaSuccess) e = dit::launch_selfcheck_compare(a, mismatches, s);
+  return launch_status(e);
 }
 
 }  // extern "C"

@@ -108,6 +108,26 @@ cudaError_t launch_fused_grouped(const DeviceInfo& dev, int dtype, bool gate_ful
                                  bool mod_full, const RowArgs* a, const int64_t* B, int count,
                                  cudaStream_t stream);
 
+// The self-check of one runtime key (dit_selfcheck): nine tensors of a
+// [B, L, D] problem in the caller's workspace -- x (hidden), update, gate,
+// scale, shift, out, out2, expected, expected2 -- and B * L row statistics.
+struct SelfcheckArgs {
+  void* t[9];
+  float* rstat;
+  int64_t D;
+  int B, L;
+  int dtype;
+  int op;  // Op
+  bool gate_full, mod_full;
+  float eps;
+};
+// seeded inputs; the plain reference outputs; the count of differing output
+// words added to *mismatches (k_selfcheck.cu)
+cudaError_t launch_selfcheck_fill(const SelfcheckArgs& a, cudaStream_t s);
+cudaError_t launch_selfcheck_reference(const SelfcheckArgs& a, cudaStream_t s);
+cudaError_t launch_selfcheck_compare(const SelfcheckArgs& a, unsigned int* mismatches,
+                                     cudaStream_t s);
+
 // ---------------------------------------------------------------------------
 // compile-time dispatch over (dtype, access width)
 // ---------------------------------------------------------------------------

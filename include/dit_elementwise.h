@@ -13,6 +13,7 @@
  *   dit_grouped                    one of the first three over several
  *                                  problems (e.g. video and audio streams)
  *                                  in one launch
+ *   dit_selfcheck                  bit-for-bit check of one runtime key
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -77,8 +78,11 @@ typedef enum {
   DIT_ERR_LAUNCH = 7,       /* the CUDA runtime rejected the launch           */
   DIT_ERR_MISALIGNED = 8,   /* a pointer is not aligned to the element size   */
   DIT_ERR_NO_DEVICE = 9,    /* no current CUDA device could be queried        */
-  DIT_ERR_BAD_GROUP = 10    /* dit_grouped: op is not a dit_op value, or count
+  DIT_ERR_BAD_OP = 10,      /* op is not a dit_op value, or (dit_grouped) count
                                is outside [0, DIT_MAX_GROUP]                  */
+  DIT_ERR_WORKSPACE = 11    /* dit_selfcheck: workspace NULL, smaller than
+                               dit_selfcheck_workspace_bytes or not 256-byte
+                               aligned                                        */
 } dit_status;
 
 /* Version of this interface; bumped on any incompatible change. */
@@ -263,6 +267,44 @@ typedef struct {
 dit_status dit_grouped(dit_op op, const dit_problem* problems, int count,
                        float eps, dit_dtype dtype, dit_layout gate_layout,
                        dit_layout mod_layout, dit_stream_t stream);
+
+/*
+ * Self-check of one runtime key: (op, dtype, gate_layout, mod_layout, D).
+ *
+ * The pages' integration checks every runtime key of its pointwise fusions
+ * bit for bit on first use and falls back to the model's math on a mismatch
+ * or a launch failure (vllm-omni PR #7350, "[Kernel] Enable LTX DiffVAE
+ * fusions on SM100 and SM103", section Purpose).  This library has no
+ * fallback; dit_selfcheck gives the caller the check itself.  It enqueues on
+ * `stream`, in order:
+ *   1. seeded inputs of a [2, 7, D] problem, written into `workspace`;
+ *   2. the operation, through the same validation and launch path as the
+ *      public call of that op, dtype and layouts (so the kernel the library
+ *      picks for 256-byte aligned tensors with rows of D elements);
+ *   3. the expected outputs from plain one-thread-per-element kernels;
+ *   4. the count of output words that differ from the expected ones, added
+ *      to *mismatches after the call has set it to zero.
+ * Every output has exactly one correct value: the residual gate is defined
+ * to the bit, and the inputs of the modulating ops make the row statistic
+ * exact in any summation order (every normalised value is +-1/2, eps = 3/4,
+ * so r = 1).  Zero mismatches: the key's path computes the definition.
+ *
+ * workspace: device memory of at least dit_selfcheck_workspace_bytes(op,
+ * dtype, D) bytes, 256-byte aligned, owned by the caller and free for the
+ * call's duration; on return it holds, from offset 0, nine tensors of
+ * N = 14 * D elements each starting on a 256-byte boundary -- x (hidden),
+ * update, gate, scale, shift (a [2, 1, D] operand fills its first 2 * D
+ * elements), out, out2, expected, expected2 -- then 14 fp32 row statistics.
+ * mismatches: device pointer to one unsigned int (4-byte aligned).
+ * eps is fixed (3/4) and not an argument.  The call does not synchronise:
+ * read *mismatches after the stream has reached it.
+ */
+int64_t dit_selfcheck_workspace_bytes(dit_op op, dit_dtype dtype, int64_t D);
+
+dit_status dit_selfcheck(dit_op op, dit_dtype dtype, dit_layout gate_layout,
+                         dit_layout mod_layout, int64_t D, void* workspace,
+                         int64_t workspace_bytes, unsigned int* mismatches,
+                         dit_stream_t stream);
 
 #ifdef __cplusplus
 }

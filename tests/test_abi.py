@@ -14,7 +14,8 @@ from diffusion_transformer_elementwise_gb300.build import build
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
                       "dit_elementwise.h")
 
-OK, NULLP, SHAPE, DTYPE, LAYOUT, ALIAS, EPS, LAUNCH, MISALIGNED, NODEV, BADGROUP = range(11)
+OK, NULLP, SHAPE, DTYPE, LAYOUT, ALIAS, EPS, LAUNCH, MISALIGNED, NODEV, BADOP, WORKSPACE = \
+    range(12)
 BF16, FP16, FP32 = 0, 1, 2
 FULL, BCAST = 0, 1
 
@@ -44,7 +45,7 @@ def test_version_and_status_strings(lib):
     m = re.search(r"#define DIT_ABI_VERSION (\d+)", open(HEADER).read())
     assert lib.dit_abi_version() == int(m.group(1))
     seen = set()
-    for code in range(11):
+    for code in range(12):
         s = lib.dit_status_string(code).decode()
         assert s.startswith("DIT_") and s not in seen
         seen.add(s)
@@ -173,10 +174,10 @@ def test_grouped_validation(lib):
     video = Problem(O, O2, H, U, G, S, SH, 1, 4, 8, 8)
     audio = Problem(O + 4096, O2 + 4096, H + 4096, U + 4096, G + 4096, S + 4096, SH + 4096,
                     1, 3, 4, 4)
-    assert f(3, probs(video), 1, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
-    assert f(-1, probs(video), 1, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
-    assert f(RGA, probs(video), 9, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
-    assert f(RGA, probs(video), -1, 1e-6, BF16, BCAST, BCAST, None) == BADGROUP
+    assert f(3, probs(video), 1, 1e-6, BF16, BCAST, BCAST, None) == BADOP
+    assert f(-1, probs(video), 1, 1e-6, BF16, BCAST, BCAST, None) == BADOP
+    assert f(RGA, probs(video), 9, 1e-6, BF16, BCAST, BCAST, None) == BADOP
+    assert f(RGA, probs(video), -1, 1e-6, BF16, BCAST, BCAST, None) == BADOP
     assert f(RGA, None, 2, 1e-6, BF16, BCAST, BCAST, None) == NULLP
     assert f(RGA, None, 0, 1e-6, BF16, BCAST, BCAST, None) == OK
     assert f(FUSED, probs(video, audio), 2, -1.0, BF16, BCAST, BCAST, None) == EPS
@@ -205,3 +206,30 @@ def test_grouped_validation(lib):
     import torch
     if not torch.cuda.is_available():
         assert f(FUSED, probs(video, audio), 2, 1e-6, BF16, BCAST, BCAST, None) == NODEV
+
+
+def test_selfcheck_validation(lib):
+    f, wb = lib.dit_selfcheck, lib.dit_selfcheck_workspace_bytes
+    RGA, MOD, FUSED = 0, 1, 2
+    # nine tensors of 14 * D elements rounded up to 256 bytes, then 256 bytes
+    assert wb(RGA, BF16, 4096) == 9 * 14 * 4096 * 2 + 256
+    assert wb(FUSED, FP32, 3) == 9 * 256 + 256
+    assert wb(MOD, FP16, 3077) == 9 * ((14 * 3077 * 2 + 255) // 256 * 256) + 256
+    assert wb(3, BF16, 64) == -1 and wb(MOD, 9, 64) == -1 and wb(MOD, BF16, 0) == -1
+    assert wb(MOD, BF16, 1 << 60) == -1
+    W, CNT = A * 64, A * 1024
+    n = wb(FUSED, BF16, 64)
+    assert f(7, BF16, BCAST, BCAST, 64, W, n, CNT, None) == BADOP
+    assert f(FUSED, 5, BCAST, BCAST, 64, W, n, CNT, None) == DTYPE
+    assert f(FUSED, BF16, 2, BCAST, 64, W, n, CNT, None) == LAYOUT
+    assert f(FUSED, BF16, BCAST, BCAST, 0, W, n, CNT, None) == SHAPE
+    assert f(FUSED, BF16, BCAST, BCAST, -5, W, n, CNT, None) == SHAPE
+    assert f(FUSED, BF16, BCAST, BCAST, 64, W, n, None, None) == NULLP
+    assert f(FUSED, BF16, BCAST, BCAST, 64, W, n, CNT + 2, None) == MISALIGNED
+    assert f(FUSED, BF16, BCAST, BCAST, 64, None, n, CNT, None) == WORKSPACE
+    assert f(FUSED, BF16, BCAST, BCAST, 64, W + 16, n, CNT, None) == WORKSPACE
+    assert f(FUSED, BF16, BCAST, BCAST, 64, W, n - 1, CNT, None) == WORKSPACE
+    assert f(FUSED, BF16, BCAST, BCAST, 64, W, n, W + 512, None) == ALIAS
+    import torch
+    if not torch.cuda.is_available():
+        assert f(FUSED, BF16, BCAST, BCAST, 64, W, n, CNT, None) == NODEV
