@@ -306,6 +306,35 @@ dit_status dit_selfcheck(dit_op op, dit_dtype dtype, dit_layout gate_layout,
                          int64_t workspace_bytes, unsigned int* mismatches,
                          dit_stream_t stream);
 
+/*
+ * dit_selfcheck_static: the same check, with no workspace argument and no
+ * allocation.  The pages have no counterpart; this entry point exists for
+ * callers that cannot allocate device memory when they want the check -- a
+ * process whose device memory is all held by a framework's caching
+ * allocator, or a latency-critical loop that must not call cudaMalloc or
+ * cudaFree (both may synchronise the device).
+ *
+ * The workspace is a static device array of DIT_SELFCHECK_STATIC_BYTES
+ * (4 MiB) inside the library, which every GPU that loads the library keeps
+ * until the process exits.  That covers bf16/fp16 keys up to D = 16384 and
+ * fp32 keys up to D = 8192; a key whose dit_selfcheck_workspace_bytes is
+ * larger returns DIT_ERR_WORKSPACE.  The caller passes `mismatches` (device,
+ * one unsigned int) as for dit_selfcheck; the call allocates nothing.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current), so make that first call before anything that must
+ * not see such a runtime query.  All calls share the one array, and nothing
+ * in it needs to start at zero; calls whose work overlaps on the GPU (other
+ * streams, other host threads) race on its contents, so order them -- one
+ * stream, or a synchronisation between them.
+ */
+#define DIT_SELFCHECK_STATIC_BYTES (4u << 20)
+
+dit_status dit_selfcheck_static(dit_op op, dit_dtype dtype,
+                                dit_layout gate_layout, dit_layout mod_layout,
+                                int64_t D, unsigned int* mismatches,
+                                dit_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
