@@ -17,6 +17,10 @@ Operations (see dit_oracle.h for the passages each one follows):
 * :func:`gelu_tanh` -- the FFN's tanh-approximated GELU (prhub summary of
   sglang PR #34172, "implementation breakdown" item 3), in double, rounded
   once.
+* :func:`rmsnorm_modulate_fp8`, :func:`gate_add_rmsnorm_modulate_fp8` -- the
+  modulated output quantised to OCP E4M3 with a per-tensor scale (the
+  RMSNorm + FP8 quantisation family named among the prhub summary's related
+  PRs); :func:`e4m3_decode`, :func:`e4m3_encode` -- the E4M3 codec.
 
 Arrays are numpy arrays or CPU torch tensors, contiguous, holding the raw
 storage of the dtype: 16-bit words for bf16 and fp16, ``float32`` for fp32.
@@ -101,6 +105,16 @@ def _bind(path):
     lib.orc_gate_add_rmsnorm_modulate_mt.argtypes = [
         ci, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, vp, i64]
     lib.orc_gate_add_rmsnorm_modulate_mt.restype = ci
+    lib.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_to_f32.restype = fp
+    lib.orc_f32_to_e4m3.argtypes = [fp]
+    lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.orc_rmsnorm_modulate_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci,
+                                             fp, vp, i64]
+    lib.orc_rmsnorm_modulate_fp8.restype = ci
+    lib.orc_gate_add_rmsnorm_modulate_fp8.argtypes = [
+        vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, fp, ci, ci, ci, fp, vp, i64]
+    lib.orc_gate_add_rmsnorm_modulate_fp8.restype = ci
     return lib
 
 
@@ -214,6 +228,46 @@ def gelu_tanh(out, x, dtype="bf16"):
     _check(_load().orc_gelu_tanh(_ptr(out), _ptr(x), n, DTYPES[dtype]), "gelu_tanh")
 
 
+def e4m3_decode(codes):
+    """fp32 values (numpy) of E4M3 codes (any iterable of 0..255)."""
+    import numpy as np
+    lib = _load()
+    return np.array([lib.orc_e4m3_to_f32(int(c)) for c in codes], dtype=np.float32)
+
+
+def e4m3_encode(values):
+    """E4M3 codes (numpy uint8) of fp32 values, each rounded once."""
+    import numpy as np
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.orc_f32_to_e4m3(float(x)) for x in v.tolist()], dtype=np.uint8)
+
+
+def rmsnorm_modulate_fp8(out, x, scale, shift, B, L, D, eps=1e-6, dtype="bf16",
+                         mod_layout="bcast", quant_scale=1.0, rows=None, t_out=None):
+    """out (uint8, one E4M3 code per element) = e4m3(fl(y * fl(1 / quant_scale)))
+    of the fp32 modulation value y."""
+    rp, n, keep = _rows(rows)
+    rc = _load().orc_rmsnorm_modulate_fp8(_ptr(out), _ptr(t_out), _ptr(x), _ptr(scale),
+                                          _ptr(shift), B, L, D, float(eps), DTYPES[dtype],
+                                          LAYOUTS[mod_layout], float(quant_scale), rp, n)
+    del keep
+    _check(rc, "rmsnorm_modulate_fp8")
+
+
+def gate_add_rmsnorm_modulate_fp8(residual_out, out, hidden, update, gate, scale, shift,
+                                  B, L, D, eps=1e-6, dtype="bf16", gate_layout="bcast",
+                                  mod_layout="bcast", quant_scale=1.0, rows=None,
+                                  t_out=None):
+    rp, n, keep = _rows(rows)
+    rc = _load().orc_gate_add_rmsnorm_modulate_fp8(
+        _ptr(residual_out), _ptr(out), _ptr(t_out), _ptr(hidden), _ptr(update), _ptr(gate),
+        _ptr(scale), _ptr(shift), B, L, D, float(eps), DTYPES[dtype], LAYOUTS[gate_layout],
+        LAYOUTS[mod_layout], float(quant_scale), rp, n)
+    del keep
+    _check(rc, "gate_add_rmsnorm_modulate_fp8")
+
+
 def round_double(values, dtype):
     """Storage words of doubles rounded once to dtype."""
     import numpy as np
@@ -238,7 +292,9 @@ def variant(lib_path: str):
     src = sys.modules[__name__]
     lib = _bind(lib_path)
     for name in ("decode", "encode", "residual_gate_add", "rmsnorm_modulate",
-                 "gate_add_rmsnorm_modulate", "row_rms_inverse", "gelu_tanh", "round_double"):
+                 "gate_add_rmsnorm_modulate", "row_rms_inverse", "gelu_tanh", "round_double",
+                 "e4m3_decode", "e4m3_encode", "rmsnorm_modulate_fp8",
+                 "gate_add_rmsnorm_modulate_fp8"):
         fn = getattr(src, name)
         g = dict(fn.__globals__)
         g["_load"] = lambda lib=lib: lib

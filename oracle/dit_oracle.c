@@ -26,6 +26,13 @@
  *   R5  a [B, 1, D] operand serves rows b*L .. b*L+L-1 of batch b.
  *   R6  fp32 -> bf16/fp16 rounding is round-to-nearest-even, overflow gives
  *       +-inf, subnormals are kept, NaN stays NaN.
+ *   R7  FP8 output (the RMSNorm + FP8 quantisation family the prhub summary
+ *       of sglang PR #34172 names among its related PRs): OCP E4M3 with no
+ *       infinities (bias 7, 3 fraction bits, largest finite 448); a static
+ *       per-tensor scale s, applied as q = fl(y * fl(1 / s)) to the fp32
+ *       modulation value y (before any rounding to the activation dtype);
+ *       q rounded to nearest-even on the E4M3 grid, saturating at +-448
+ *       (infinities included), NaN stays NaN.
  */
 #include "dit_oracle.h"
 
@@ -154,6 +161,46 @@ void orc_encode_array(void* dst, const float* src_f32, int64_t n, int dtype) {
   for (int64_t i = 0; i < n; ++i) orc_store(dst, i, src_f32[i], dtype);
 }
 
+/* OCP E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; no
+ * infinities; exponent 15 with fraction 7 is NaN.  Codes 0..7 are
+ * subnormal, k * 2^-9. */
+float orc_e4m3_to_f32(uint8_t b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  float v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexpf((float)m, -9);
+  else
+    v = ldexpf((float)(8 + m), e - 10);
+  return (b & 0x80) ? -v : v;
+}
+
+/* Reading R7.  |f| is rounded to the E4M3 grid of its binade with
+ * nearbyint (round to nearest, ties to even, in the default rounding mode):
+ * spacing 2^-9 below 2^-6 (subnormals), 2^(E-3) in [2^E, 2^(E+1)).  The
+ * grid multiple k then maps to the code directly: codes grow with the value,
+ * and a binade's 8 steps are the 8 fraction values. */
+uint8_t orc_f32_to_e4m3(float f) {
+  if (isnan(f)) return 0x7F;
+  const uint8_t sign = signbit(f) ? 0x80 : 0;
+  const double a = fabs((double)f);
+  if (a >= 448.0) return sign | 0x7E; /* saturate, infinities included */
+  if (a < ldexp(1.0, -6)) {
+    const double k = nearbyint(a / ldexp(1.0, -9)); /* 0..8; 8 is 2^-6 */
+    return sign | (uint8_t)k;
+  }
+  int E;
+  (void)frexp(a, &E); /* a = m * 2^E with m in [0.5, 1): binade 2^(E-1) */
+  E -= 1;
+  double k = nearbyint(a / ldexp(1.0, E - 3)); /* 8..16 */
+  int ex = E + 7;
+  if (k == 16.0) {
+    k = 8.0;
+    ex += 1;
+  }
+  return sign | (uint8_t)((ex << 3) | ((int)k - 8));
+}
+
 /* ------------------------------------------------------------------------ */
 /* one row of each operation                                                 */
 /* ------------------------------------------------------------------------ */
@@ -191,7 +238,7 @@ float orc_row_rms_inverse(const void* x_row, int64_t D, float eps, int dtype) {
 static void rmsnorm_modulate_row(void* out, float* t_out, const void* x,
                                  const void* scale, const void* shift,
                                  int64_t r, int64_t L, int64_t D, float eps,
-                                 int dtype, int mod_layout) {
+                                 int dtype, int mod_layout, int fp8, float qinv) {
   if (D == 0) return;
   const size_t esize = (dtype == ORC_FP32) ? 4 : 2;
   const void* x_row = (const char*)x + (size_t)(r * D) * esize;
@@ -206,7 +253,10 @@ static void rmsnorm_modulate_row(void* out, float* t_out, const void* x,
     float t = n * one;
     float y = t + sh;
     if (t_out) t_out[r * D + d] = t;
-    orc_store(out, r * D + d, y, dtype);
+    if (fp8) /* reading R7 */
+      ((uint8_t*)out)[r * D + d] = orc_f32_to_e4m3(y * qinv);
+    else
+      orc_store(out, r * D + d, y, dtype);
   }
 }
 
@@ -263,6 +313,8 @@ typedef struct {
   int64_t B, L, D;
   float eps;
   int dtype, layout1, layout2;
+  int fp8;    /* modulated output in E4M3 (reading R7) */
+  float qinv; /* fl(1 / quant_scale) */
   const int64_t* rows;
   int64_t begin, end; /* positions in the row selection */
 } orc_job;
@@ -275,13 +327,13 @@ static void run_job(const orc_job* j) {
                         j->dtype, j->layout1);
     } else if (j->op == 1) {
       rmsnorm_modulate_row(j->out, j->t_out, j->hidden, j->scale, j->shift, r,
-                           j->L, j->D, j->eps, j->dtype, j->layout1);
+                           j->L, j->D, j->eps, j->dtype, j->layout1, j->fp8, j->qinv);
     } else {
       /* reading R4: the stored (rounded) residual is the modulation input */
       residual_gate_row(j->out, j->hidden, j->update, j->gate, r, j->L, j->D,
                         j->dtype, j->layout1);
       rmsnorm_modulate_row(j->out2, j->t_out, j->out, j->scale, j->shift, r,
-                           j->L, j->D, j->eps, j->dtype, j->layout2);
+                           j->L, j->D, j->eps, j->dtype, j->layout2, j->fp8, j->qinv);
     }
   }
 }
@@ -360,13 +412,16 @@ int orc_residual_gate_add(void* out, const void* hidden, const void* update,
 static int modulate_impl(int nthreads, void* out, float* t_out, const void* x,
                          const void* scale, const void* shift, int64_t B,
                          int64_t L, int64_t D, float eps, int dtype,
-                         int mod_layout, const int64_t* rows, int64_t nrows) {
+                         int mod_layout, const int64_t* rows, int64_t nrows,
+                         int fp8, float qinv) {
   if (bad_common(B, L, D, dtype, rows, nrows) || bad_layout(mod_layout)) return -1;
   if (B * L * D > 0 && (!out || !x || !scale || !shift)) return -1;
   orc_job j = {0};
   j.op = 1;
   j.out = out;
   j.t_out = t_out;
+  j.fp8 = fp8;
+  j.qinv = qinv;
   j.hidden = x;
   j.scale = scale;
   j.shift = shift;
@@ -386,7 +441,7 @@ int orc_rmsnorm_modulate(void* out, float* t_out, const void* x,
                          int64_t L, int64_t D, float eps, int dtype,
                          int mod_layout, const int64_t* rows, int64_t nrows) {
   return modulate_impl(1, out, t_out, x, scale, shift, B, L, D, eps, dtype,
-                       mod_layout, rows, nrows);
+                       mod_layout, rows, nrows, 0, 1.0f);
 }
 
 int orc_rmsnorm_modulate_mt(int nthreads, void* out, const void* x,
@@ -394,7 +449,7 @@ int orc_rmsnorm_modulate_mt(int nthreads, void* out, const void* x,
                             int64_t L, int64_t D, float eps, int dtype,
                             int mod_layout, const int64_t* rows, int64_t nrows) {
   return modulate_impl(nthreads, out, NULL, x, scale, shift, B, L, D, eps,
-                       dtype, mod_layout, rows, nrows);
+                       dtype, mod_layout, rows, nrows, 0, 1.0f);
 }
 
 static int fused_impl(int nthreads, void* residual_out, void* modulated_out,
@@ -402,7 +457,7 @@ static int fused_impl(int nthreads, void* residual_out, void* modulated_out,
                       const void* gate, const void* scale, const void* shift,
                       int64_t B, int64_t L, int64_t D, float eps, int dtype,
                       int gate_layout, int mod_layout, const int64_t* rows,
-                      int64_t nrows) {
+                      int64_t nrows, int fp8, float qinv) {
   if (bad_common(B, L, D, dtype, rows, nrows) || bad_layout(gate_layout) ||
       bad_layout(mod_layout))
     return -1;
@@ -414,6 +469,8 @@ static int fused_impl(int nthreads, void* residual_out, void* modulated_out,
   j.out = residual_out;
   j.out2 = modulated_out;
   j.t_out = t_out;
+  j.fp8 = fp8;
+  j.qinv = qinv;
   j.hidden = hidden;
   j.update = update;
   j.gate = gate;
@@ -440,7 +497,7 @@ int orc_gate_add_rmsnorm_modulate(void* residual_out, void* modulated_out,
                                   const int64_t* rows, int64_t nrows) {
   return fused_impl(1, residual_out, modulated_out, t_out, hidden, update, gate,
                     scale, shift, B, L, D, eps, dtype, gate_layout, mod_layout,
-                    rows, nrows);
+                    rows, nrows, 0, 1.0f);
 }
 
 int orc_gate_add_rmsnorm_modulate_mt(int nthreads, void* residual_out,
@@ -452,5 +509,31 @@ int orc_gate_add_rmsnorm_modulate_mt(int nthreads, void* residual_out,
                                      const int64_t* rows, int64_t nrows) {
   return fused_impl(nthreads, residual_out, modulated_out, NULL, hidden, update,
                     gate, scale, shift, B, L, D, eps, dtype, gate_layout,
-                    mod_layout, rows, nrows);
+                    mod_layout, rows, nrows, 0, 1.0f);
+}
+
+/* Reading R7: the modulation (or the fused op) with its modulated output in
+ * E4M3, q = fl(y * fl(1 / quant_scale)). */
+int orc_rmsnorm_modulate_fp8(uint8_t* out, float* t_out, const void* x,
+                             const void* scale, const void* shift, int64_t B,
+                             int64_t L, int64_t D, float eps, int dtype,
+                             int mod_layout, float quant_scale,
+                             const int64_t* rows, int64_t nrows) {
+  const float qinv = 1.0f / quant_scale;
+  return modulate_impl(1, out, t_out, x, scale, shift, B, L, D, eps, dtype,
+                       mod_layout, rows, nrows, 1, qinv);
+}
+
+int orc_gate_add_rmsnorm_modulate_fp8(void* residual_out, uint8_t* out,
+                                      float* t_out, const void* hidden,
+                                      const void* update, const void* gate,
+                                      const void* scale, const void* shift,
+                                      int64_t B, int64_t L, int64_t D, float eps,
+                                      int dtype, int gate_layout, int mod_layout,
+                                      float quant_scale, const int64_t* rows,
+                                      int64_t nrows) {
+  const float qinv = 1.0f / quant_scale;
+  return fused_impl(1, residual_out, out, t_out, hidden, update, gate, scale,
+                    shift, B, L, D, eps, dtype, gate_layout, mod_layout, rows,
+                    nrows, 1, qinv);
 }

@@ -92,6 +92,31 @@ int orc_gelu_tanh(void* out, const void* x, int64_t n, int dtype);
 /* one rounding of a double to the dtype (round-to-nearest-even) */
 void orc_store_double(void* p, int64_t i, double v, int dtype);
 
+/* OCP E4M3 (no infinities, largest finite 448): exact decoding, and one
+ * rounding of an fp32 value to nearest-even with saturation at +-448; NaN
+ * gives 0x7F. */
+float   orc_e4m3_to_f32(uint8_t b);
+uint8_t orc_f32_to_e4m3(float f);
+
+/* The modulation and the fused op with the modulated output quantised to
+ * E4M3: q = fl(y * fl(1 / quant_scale)) of the fp32 value y, rounded once
+ * to E4M3 (RMSNorm + FP8 quantisation: the fusion family that the prhub
+ * summary of sglang PR #34172 lists among its related PRs).  `out` holds
+ * one byte per element. */
+int orc_rmsnorm_modulate_fp8(uint8_t* out, float* t_out, const void* x,
+                             const void* scale, const void* shift, int64_t B,
+                             int64_t L, int64_t D, float eps, int dtype,
+                             int mod_layout, float quant_scale,
+                             const int64_t* rows, int64_t nrows);
+int orc_gate_add_rmsnorm_modulate_fp8(void* residual_out, uint8_t* out,
+                                      float* t_out, const void* hidden,
+                                      const void* update, const void* gate,
+                                      const void* scale, const void* shift,
+                                      int64_t B, int64_t L, int64_t D, float eps,
+                                      int dtype, int gate_layout, int mod_layout,
+                                      float quant_scale, const int64_t* rows,
+                                      int64_t nrows);
+
 /* The per-row statistic, exposed for the tests: r = 1/sqrt(mean(x^2) + eps)
  * for one row of D elements. */
 float orc_row_rms_inverse(const void* x_row, int64_t D, float eps, int dtype);

@@ -6,7 +6,9 @@ Mistakes planted: a wrong sign, a dropped term, a transposed or wrong
 operand, a wrong row index for a broadcast operand, eps outside the root or
 dropped, a wrong divisor in the mean, a fused multiply-add, wrong rounding of
 the storage dtype, the fused op reading the unrounded residual, and in the
-GELU a wrong coefficient, power, sign or scale, and double rounding.
+GELU a wrong coefficient, power, sign or scale, and double rounding; in the
+FP8 output the scale applied the wrong way, no saturation, ties away from
+zero and a wrong subnormal spacing.
 """
 import os
 import shutil
@@ -16,6 +18,7 @@ import pytest
 
 import oracle
 import test_oracle_codecs as pc
+import test_oracle_fp8 as p8
 import test_oracle_fused as pf
 import test_oracle_gelu as pg
 import test_oracle_modulate as pm
@@ -46,6 +49,13 @@ MUTANTS = {
     "bf16_round_half_up": ("x += 0x7FFFu + lsb;", "x += 0x8000u; (void)lsb;"),
     "fp16_truncate": ("float m = nearbyintf(a / ldexpf(1.0f, E - 10));",
                       "float m = truncf(a / ldexpf(1.0f, E - 10));"),
+    "fp8_scale_inverted": ("orc_f32_to_e4m3(y * qinv)", "orc_f32_to_e4m3(y / qinv)"),
+    "fp8_no_saturation": ("if (a >= 448.0) return sign | 0x7E;",
+                          "if (a >= 464.0) return sign | 0x7F;"),
+    "fp8_ties_away": ("double k = nearbyint(a / ldexp(1.0, E - 3));",
+                      "double k = round(a / ldexp(1.0, E - 3));"),
+    "fp8_subnormal_spacing": ("const double k = nearbyint(a / ldexp(1.0, -9));",
+                              "const double k = nearbyint(a / ldexp(1.0, -10));"),
     "gelu_cubic_coeff": ("0.044715 * v * v * v", "0.04715 * v * v * v"),
     "gelu_square": ("0.044715 * v * v * v", "0.044715 * v * v"),
     "gelu_sign": ("v / (1.0 + exp(-2.0 * z))", "v / (1.0 + exp(2.0 * z))"),
@@ -53,7 +63,7 @@ MUTANTS = {
     "double_rounding": ("    b |= 1u; /* sticky: odd */", "    (void)b;"),
     "fused_unrounded": (
         "      rmsnorm_modulate_row(j->out2, j->t_out, j->out, j->scale, j->shift, r,\n"
-        "                           j->L, j->D, j->eps, j->dtype, j->layout2);",
+        "                           j->L, j->D, j->eps, j->dtype, j->layout2, j->fp8, j->qinv);",
         # modulate the fp32 sums instead of the stored (rounded) residual
         "      { float* xr = malloc(sizeof(float) * (size_t)j->D); double sum = 0;\n"
         "        int64_t gr = j->layout1 == ORC_FULL ? r : r / j->L;\n"
@@ -92,6 +102,9 @@ PINS = [
     lambda o: pg.test_round_to_odd_avoids_double_rounding(o),
     lambda o: pg.test_against_torch_float64(o, "bf16"),
     lambda o: pg.test_against_50_digit_evaluation(o, "fp32"),
+    lambda o: p8.test_ties_golden(o),
+    lambda o: p8.test_encode_against_torch(o),
+    lambda o: p8.test_modulate_fp8_is_quantised_fp32_modulation(o, "bf16", 0.005),
 ]
 
 
