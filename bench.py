@@ -257,8 +257,31 @@ def hotpath_ops(device, B=1, L=32640, D=4096, dtype="bf16", only=None):
             return lambda threads: oracle.gelu_tanh(res, host, dtype)
         return Op("gelu_ffn", lambda: dit.gelu_tanh(x, out=o), 2 * n4 * es, [x], [o], make)
 
+    def mod_fp8():
+        # the modulation with its output in E4M3 (the input of an FP8 GEMM)
+        x = draw("act", (B, L, D), seed_for("bench", "x8"), dtype, device)
+        sc = draw("mod", (B, 1, D), seed_for("bench", "sc8"), dtype, device)
+        sh = draw("mod", (B, 1, D), seed_for("bench", "sh8"), dtype, device)
+        qs = torch.full((1,), 0.05, dtype=torch.float32, device=device)
+        o = torch.empty((B, L, D), dtype=torch.uint8, device=device)
+        return Op("mod_fp8", lambda: dit.rmsnorm_modulate_fp8(x, sc, sh, qs, EPS, out=o),
+                  N * es + N + 2 * vb, [x], [o], None)
+
+    def fused_fp8():
+        h = draw("act", (B, L, D), seed_for("bench", "h8"), dtype, device)
+        u = draw("act", (B, L, D), seed_for("bench", "u8"), dtype, device)
+        g = draw("gate", (B, 1, D), seed_for("bench", "g8"), dtype, device)
+        sc = draw("mod", (B, 1, D), seed_for("bench", "sc8f"), dtype, device)
+        sh = draw("mod", (B, 1, D), seed_for("bench", "sh8f"), dtype, device)
+        qs = torch.full((1,), 0.05, dtype=torch.float32, device=device)
+        r = torch.empty_like(h)
+        o = torch.empty((B, L, D), dtype=torch.uint8, device=device)
+        return Op("fused_fp8", lambda: dit.gate_add_rmsnorm_modulate_fp8(
+            h, u, g, sc, sh, qs, EPS, residual_out=r, out=o),
+            3 * N * es + N + 3 * vb, [h, u], [r, o], None)
+
     builders = [rga_bcast, rga_bcast_inplace, rga_full, mod_bcast, fused_bcast]
-    extra = {"gelu_ffn": gelu_ffn}
+    extra = {"gelu_ffn": gelu_ffn, "mod_fp8": mod_fp8, "fused_fp8": fused_fp8}
     if only in extra:
         return [extra[only]()]
     if only is not None:
@@ -517,7 +540,12 @@ def run_ours(args):
         dist.barrier()
     build()  # no-op when up to date
 
-    if args.workload == "gelu":
+    if args.workload == "fp8":
+        ops = hotpath_ops(device, only="mod_fp8") + hotpath_ops(device, only="fused_fp8")
+        workload = {"workload": "ltx2_bcast_s32640_c4096 modulation and fused op with an E4M3 "
+                                "(FP8) modulated output, per-tensor scale",
+                    "B": 1, "L": 32640, "D": 4096}
+    elif args.workload == "gelu":
         ops = hotpath_ops(device, only="gelu_ffn")
         workload = {"workload": "ltx2 feed-forward tanh-GELU on [1,32640,16384] bf16",
                     "B": 1, "L": 32640, "D": 16384}
@@ -709,7 +737,8 @@ def main():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["hotpath", "chain", "chain_av", "shapes", "gelu"], default="hotpath")
+    p.add_argument("--workload", choices=["hotpath", "chain", "chain_av", "shapes", "gelu", "fp8"],
+                   default="hotpath")
     p.add_argument("--chain-shape", default="2,32640,4096",
                    help="B,L,D of --workload chain (e.g. 1,126,2048: the audio stream)")
     p.add_argument("--audio-shape", default="1,126,2048",
@@ -723,7 +752,8 @@ def main():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--op", default=None,
                    help="time one op of the hot path only (rga_bcast, rga_bcast_inplace, "
-                        "rga_full, mod_bcast, fused_bcast, gelu_ffn): for profiling")
+                        "rga_full, mod_bcast, fused_bcast, gelu_ffn, mod_fp8, fused_fp8): "
+                        "for profiling")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -84,6 +84,12 @@ def library() -> ctypes.CDLL:
             lib.dit_gate_add_rmsnorm_modulate_strided.restype = ci
             lib.dit_grouped.argtypes = [ci, ctypes.POINTER(Problem), ci, cf, ci, ci, ci, vp]
             lib.dit_grouped.restype = ci
+            lib.dit_rmsnorm_modulate_fp8.argtypes = [vp, vp, vp, vp, i64, i64, i64, cf, ci, ci,
+                                                     i64, vp, vp]
+            lib.dit_rmsnorm_modulate_fp8.restype = ci
+            lib.dit_gate_add_rmsnorm_modulate_fp8.argtypes = [
+                vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, cf, ci, ci, ci, i64, vp, vp]
+            lib.dit_gate_add_rmsnorm_modulate_fp8.restype = ci
             lib.dit_selfcheck_workspace_bytes.argtypes = [ci, ci, i64]
             lib.dit_selfcheck_workspace_bytes.restype = i64
             lib.dit_selfcheck.argtypes = [ci, ci, ci, ci, i64, vp, i64, vp, vp]
@@ -469,3 +475,81 @@ def _first_use_check(op, dtype, glay, mlay, D, dev):
     if _first_use:
         names = {FULL: "full", ROW_BCAST: "bcast"}
         ensure_checked(op, dtype, names[glay], names[mlay], D, device=dev)
+
+
+# ---------------------------------------------------------------------------
+# modulated output in FP8 (OCP E4M3)
+# ---------------------------------------------------------------------------
+
+_FP8 = getattr(torch, "float8_e4m3fn", None)
+
+
+def _fp8_out(out, like, name="out"):
+    """The E4M3 output tensor: float8_e4m3fn (allocated if None) or uint8."""
+    if out is None:
+        return torch.empty(like.shape, dtype=_FP8 or torch.uint8, device=like.device)
+    if out.dtype not in tuple(t for t in (_FP8, torch.uint8) if t is not None):
+        raise TypeError(f"{name} must be float8_e4m3fn or uint8, got {out.dtype}")
+    if tuple(out.shape) != tuple(like.shape):
+        raise ValueError(f"{name} must have the shape {tuple(like.shape)}")
+    return out
+
+
+def _quant_scale(qs, dev):
+    if (not isinstance(qs, torch.Tensor) or not qs.is_cuda or qs.dtype != torch.float32
+            or qs.numel() != 1 or qs.get_device() != dev):
+        raise TypeError("quant_scale must be a one-element float32 CUDA tensor on the "
+                        "tensors' device (read by the kernel)")
+    return qs
+
+
+def rmsnorm_modulate_fp8(x, scale, shift, quant_scale, eps=1e-6, out=None, stream=None):
+    """out = e4m3(fl(y * fl(1 / quant_scale))) with y = rms_norm(x, eps) *
+    (1 + scale) + shift in fp32 (dit_rmsnorm_modulate_fp8): OCP E4M3,
+    nearest-even, saturating at +-448.  quant_scale: one-element float32
+    CUDA tensor.  Returns out (float8_e4m3fn, or the uint8 tensor given)."""
+    B, L, D = _shape3(x, "x")
+    out = _fp8_out(out, x)
+    dev = _cuda(("x", x), ("scale", scale), ("shift", shift), ("out", out))
+    dt = _dtype(x, ("scale", scale), ("shift", shift))
+    lay = layout_of(scale, B, L, D, "scale")
+    if layout_of(shift, B, L, D, "shift") != lay:
+        raise ValueError("scale and shift must have the same layout")
+    vs = _vector_stride(D, scale, shift) if lay == ROW_BCAST else D
+    qs = _quant_scale(quant_scale, dev)
+    st = _launch(dev, library().dit_rmsnorm_modulate_fp8, out.data_ptr(), x.data_ptr(),
+                 scale.data_ptr(), shift.data_ptr(), B, L, D, float(eps), dt, lay, vs,
+                 qs.data_ptr(), _stream(dev, stream))
+    check(st, "dit_rmsnorm_modulate_fp8")
+    return out
+
+
+def gate_add_rmsnorm_modulate_fp8(hidden, update, gate, scale, shift, quant_scale, eps=1e-6,
+                                  residual_out=None, out=None, stream=None):
+    """residual_out = hidden + update * gate (dtype of hidden); out = the E4M3
+    modulation of residual_out (dit_gate_add_rmsnorm_modulate_fp8).  Returns
+    (residual_out, out)."""
+    B, L, D = _shape3(hidden, "hidden")
+    if residual_out is None:
+        residual_out = torch.empty_like(hidden)
+    out = _fp8_out(out, hidden)
+    dev = _cuda(("hidden", hidden), ("update", update), ("gate", gate), ("scale", scale),
+                ("shift", shift), ("residual_out", residual_out), ("out", out))
+    dt = _dtype(hidden, ("update", update), ("gate", gate), ("scale", scale), ("shift", shift),
+                ("residual_out", residual_out))
+    for name, t in (("update", update), ("residual_out", residual_out)):
+        if tuple(t.shape) != (B, L, D):
+            raise ValueError(f"{name} must have the shape of hidden")
+    glay = layout_of(gate, B, L, D, "gate")
+    mlay = layout_of(scale, B, L, D, "scale")
+    if layout_of(shift, B, L, D, "shift") != mlay:
+        raise ValueError("scale and shift must have the same layout")
+    vecs = ([gate] if glay == ROW_BCAST else []) + ([scale, shift] if mlay == ROW_BCAST else [])
+    vs = _vector_stride(D, *vecs)
+    qs = _quant_scale(quant_scale, dev)
+    st = _launch(dev, library().dit_gate_add_rmsnorm_modulate_fp8, residual_out.data_ptr(),
+                 out.data_ptr(), hidden.data_ptr(), update.data_ptr(), gate.data_ptr(),
+                 scale.data_ptr(), shift.data_ptr(), B, L, D, float(eps), dt, glay, mlay, vs,
+                 qs.data_ptr(), _stream(dev, stream))
+    check(st, "dit_gate_add_rmsnorm_modulate_fp8")
+    return residual_out, out

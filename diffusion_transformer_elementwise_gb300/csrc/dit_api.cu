@@ -615,3 +615,136 @@ dit_status dit_selfcheck(dit_op op, dit_dtype dtype, dit_layout gate_layout,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// modulated output in OCP E4M3
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Shape and alignment rules of the E4M3-output calls: the staged row kernel
+// only -- 16-byte aligned inputs, rows and vector strides of a multiple of
+// 16 bytes, rows of at most 16 KB; the E4M3 output aligned to the bytes of
+// its per-granule store (8 for 16-bit inputs, 4 for fp32).
+dit_status fp8_rules(int64_t D, int es, int64_t vs_bytes, const void* out8,
+                     const void* const* inputs, int ninputs) {
+  if (D * es > 16384) return DIT_ERR_BAD_SHAPE;
+  if ((D * es) % 16 != 0 || vs_bytes % 16 != 0) return DIT_ERR_MISALIGNED;
+  for (int i = 0; i < ninputs; ++i)
+    if (((uintptr_t)inputs[i] & 15) != 0) return DIT_ERR_MISALIGNED;
+  if (((uintptr_t)out8 & (uintptr_t)(16 / es - 1)) != 0) return DIT_ERR_MISALIGNED;
+  return DIT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dit_status dit_rmsnorm_modulate_fp8(void* out, const void* x, const void* scale,
+                                    const void* shift, int64_t B, int64_t L, int64_t D,
+                                    float eps, dit_dtype dtype, dit_layout mod_layout,
+                                    int64_t vec_stride, const float* quant_scale,
+                                    dit_stream_t stream) {
+  if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
+  if (!valid_layout(mod_layout)) return DIT_ERR_BAD_LAYOUT;
+  const int es = elem_size(dtype);
+  int64_t n;
+  if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
+  const bool full = mod_layout == DIT_FULL;
+  if (!full && !valid_vector_stride(B, D, vec_stride, es)) return DIT_ERR_BAD_SHAPE;
+  if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
+  if (n == 0) return DIT_OK;
+  if (!out || !x || !scale || !shift || !quant_scale) return DIT_ERR_NULL_PTR;
+  const int64_t vs = B > 1 && !full ? vec_stride : D;
+  const void* ins[3] = {x, scale, shift};
+  const dit_status rule = fp8_rules(D, es, vs * es, out, ins, 3);
+  if (rule != DIT_OK) return rule;
+  if (((uintptr_t)quant_scale & 3) != 0) return DIT_ERR_MISALIGNED;
+  const int64_t bytes = n * es;
+  const int64_t vbytes = full ? bytes : vector_span(B, D, vs, es);
+  const Span so = span(out, n);  // one byte per element
+  if (overlaps(so, span(x, bytes)) || overlaps(so, span(scale, vbytes)) ||
+      overlaps(so, span(shift, vbytes)) || overlaps(so, span(quant_scale, 4)))
+    return DIT_ERR_ALIAS;
+
+  DeviceInfo dev;
+  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
+  RowArgs a = {};
+  a.out = out;
+  a.x = x;
+  a.sc = scale;
+  a.sh = shift;
+  a.L = L;
+  a.D = D;
+  a.rows = B * L;
+  a.vstride = vs * es;
+  a.eps = eps;
+  a.d_f = (float)D;
+  a.inv_d = 1.0f / (float)D;
+  a.qscale = quant_scale;
+  const cudaError_t e = dit::launch_modulate_fp8(dev, dtype, full, a, B, (cudaStream_t)stream);
+  return e == cudaErrorNotSupported ? DIT_ERR_BAD_SHAPE : launch_status(e);
+}
+
+dit_status dit_gate_add_rmsnorm_modulate_fp8(
+    void* residual_out, void* out, const void* hidden, const void* update, const void* gate,
+    const void* scale, const void* shift, int64_t B, int64_t L, int64_t D, float eps,
+    dit_dtype dtype, dit_layout gate_layout, dit_layout mod_layout, int64_t vec_stride,
+    const float* quant_scale, dit_stream_t stream) {
+  if (!valid_dtype(dtype)) return DIT_ERR_BAD_DTYPE;
+  if (!valid_layout(gate_layout) || !valid_layout(mod_layout)) return DIT_ERR_BAD_LAYOUT;
+  const int es = elem_size(dtype);
+  int64_t n;
+  if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
+  const bool any_bcast = gate_layout == DIT_ROW_BCAST || mod_layout == DIT_ROW_BCAST;
+  if (any_bcast && !valid_vector_stride(B, D, vec_stride, es)) return DIT_ERR_BAD_SHAPE;
+  if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
+  if (n == 0) return DIT_OK;
+  if (!residual_out || !out || !hidden || !update || !gate || !scale || !shift || !quant_scale)
+    return DIT_ERR_NULL_PTR;
+  const int64_t vs = B > 1 && any_bcast ? vec_stride : D;
+  const void* ins[6] = {residual_out, hidden, update, gate, scale, shift};
+  const dit_status rule = fp8_rules(D, es, vs * es, out, ins, 6);
+  if (rule != DIT_OK) return rule;
+  if (((uintptr_t)quant_scale & 3) != 0) return DIT_ERR_MISALIGNED;
+  const int64_t bytes = n * es;
+  const int64_t vbytes = vector_span(B, D, vs, es);
+  const Span sr = span(residual_out, bytes);
+  const Span sq = span(out, n);
+  const Span inputs[6] = {span(hidden, bytes),
+                          span(update, bytes),
+                          span(gate, gate_layout == DIT_FULL ? bytes : vbytes),
+                          span(scale, mod_layout == DIT_FULL ? bytes : vbytes),
+                          span(shift, mod_layout == DIT_FULL ? bytes : vbytes),
+                          span(quant_scale, 4)};
+  if (overlaps(sr, sq)) return DIT_ERR_ALIAS;
+  for (int i = 0; i < 6; ++i) {
+    if (overlaps(sq, inputs[i])) return DIT_ERR_ALIAS;
+    if (i == 0 && residual_out == hidden) continue;
+    if (overlaps(sr, inputs[i])) return DIT_ERR_ALIAS;
+  }
+
+  DeviceInfo dev;
+  if (dit::current_device(&dev) != cudaSuccess) return DIT_ERR_NO_DEVICE;
+  RowArgs a = {};
+  a.out = residual_out;
+  a.out2 = out;
+  a.x = hidden;
+  a.u = update;
+  a.g = gate;
+  a.sc = scale;
+  a.sh = shift;
+  a.L = L;
+  a.D = D;
+  a.rows = B * L;
+  a.vstride = vs * es;
+  a.eps = eps;
+  a.d_f = (float)D;
+  a.inv_d = 1.0f / (float)D;
+  a.qscale = quant_scale;
+  const cudaError_t e = dit::launch_fused_fp8(dev, dtype, gate_layout == DIT_FULL,
+                                              mod_layout == DIT_FULL, a, B, (cudaStream_t)stream);
+  return e == cudaErrorNotSupported ? DIT_ERR_BAD_SHAPE : launch_status(e);
+}
+
+}  // extern "C"

@@ -54,6 +54,7 @@ struct RowArgs {
   int64_t ngroups;    // B * gpb
   int64_t step_b;     // G / gpb
   int64_t step_g;     // G % gpb
+  const float* qscale;  // E4M3 output: the per-tensor quantisation scale (device)
 };
 
 struct DeviceInfo {
@@ -94,6 +95,13 @@ cudaError_t launch_gelu(const DeviceInfo& dev, int dtype, void* out, const void*
 cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb,
                          bool gate_full, bool mod_full, const RowArgs& a,
                          int64_t B, cudaStream_t stream);
+// The modulation / fused op with an E4M3 modulated output (a.qscale set):
+// staged rows only (16-byte aligned, at most 8192 16-bit or 4096 fp32
+// elements); cudaErrorNotSupported otherwise.
+cudaError_t launch_modulate_fp8(const DeviceInfo& dev, int dtype, bool mod_full,
+                                const RowArgs& a, int64_t B, cudaStream_t stream);
+cudaError_t launch_fused_fp8(const DeviceInfo& dev, int dtype, bool gate_full, bool mod_full,
+                             const RowArgs& a, int64_t B, cudaStream_t stream);
 
 // Grouped launches of the staged row kernel: `count` problems of one
 // operation, dtype and layout, each with 16-byte aligned rows.  Return

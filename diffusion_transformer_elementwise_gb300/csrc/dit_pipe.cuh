@@ -107,9 +107,31 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[RC]) {
 #else
 #define DIT_PIPE_BOUNDS __launch_bounds__(512)
 #endif
+// Two fp32 values to two OCP E4M3 codes, each rounded to nearest-even and
+// saturated to +-448 (NaN stays NaN): the first value in the low byte, so
+// the pair is stored in element order.
+__device__ __forceinline__ uint32_t e4m3x2(F2 v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(f2_hi(v)), "f"(f2_lo(v)));
+  return r;
+}
+// a granule's P pairs, each scaled by qinv (one fp32 rounding), as E4M3:
+// 8 bytes for 16-bit dtypes, 4 for fp32
+template <int P>
+__device__ __forceinline__ Raw<2 * P> quantise_e4m3(const F2 (&y)[P], F2 qinv) {
+  Raw<2 * P> r;
+#pragma unroll
+  for (int i = 0; i < P / 2; ++i)
+    r.w[i] = e4m3x2(f2_mul(y[2 * i], qinv)) | (e4m3x2(f2_mul(y[2 * i + 1], qinv)) << 16);
+  return r;
+}
+
 // The body of one CTA: CTA `cta` of the problem's grid-stride schedule, on
-// column slice `slice` of the row.
-template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS>
+// column slice `slice` of the row.  Q8: the modulated output is OCP E4M3
+// (one byte per element, a.out2 for the fused op, a.out otherwise), the
+// fp32 value scaled by fl(1 / *a.qscale) first.
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS,
+          bool Q8 = false>
 __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, const int64_t slice) {
   using G = Granule<T>;
   constexpr int P = G::P;  // fp32 pairs per 16-byte granule
@@ -167,7 +189,14 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
     }
   }
   char* const out1 = (char*)a.out + g0 * 16;
-  char* const out2 = (char*)(OP == OP_FUSED ? a.out2 : a.out) + g0 * 16;
+  // the modulated output: 16 bytes per granule, or 16 / sizeof(T) in E4M3
+  constexpr int QB = 16 / (int)sizeof(T);
+  char* const out2 = (char*)(OP == OP_FUSED ? a.out2 : a.out) + g0 * (Q8 ? QB : 16);
+  const int64_t qpitch = a.D;                   // E4M3 row pitch, bytes
+  const int64_t qkstride = (int64_t)nthr * QB;  // bytes between a thread's E4M3 granules
+  float qinv_s = 1.0f;
+  if constexpr (Q8) qinv_s = __frcp_rn(__ldg(a.qscale));
+  const F2 qinv = f2(qinv_s, qinv_s);
 
   // shared addresses: slot (stage, j, op, k) = stage + j*JS + op*OS + k*KS
   const uint32_t KS = (uint32_t)nthr * 16;
@@ -287,7 +316,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
       for (int j = 0; j < RC; ++j) {
         const float r = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
         if (CHECK && row0 + j >= rend) continue;
-        const int64_t rowoff = (row0 + j) * pitch;
+        [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch;
         const F2 r2 = f2(r, r);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -306,7 +335,10 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
 #pragma unroll
             for (int i = 0; i < P; ++i) y[i] = modulate2(f2_mul(x[i], r2), onev[k][i], shv[k][i]);
           }
-          st_stream<16>(out2 + rowoff + k * kstride, G::narrow(y));
+          if constexpr (Q8)
+            st_stream<2 * P>(out2 + (row0 + j) * qpitch + k * qkstride, quantise_e4m3<P>(y, qinv));
+          else
+            st_stream<16>(out2 + rowoff + k * kstride, G::narrow(y));
         }
       }
     }
@@ -333,9 +365,10 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   cp_async_wait<0>();  // no copy may outlive the CTA's shared memory
 }
 
-template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS>
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS,
+          bool Q8 = false>
 __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
-  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS>(a, blockIdx.x, blockIdx.y);
+  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>(a, blockIdx.x, blockIdx.y);
 }
 
 // Several problems of one operation in one launch: problem p owns the CTAs
@@ -432,11 +465,11 @@ __host__ __device__ constexpr int pipe_rows() {
 
 // Launch the staged kernel with S stages; returns cudaErrorNotSupported when
 // the row is too long for it (the caller then uses the two-pass kernel).
-template <int OP, class T, int S, bool GFULL, bool MFULL, bool ALLCOLS>
+template <int OP, class T, int S, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false>
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
   constexpr int RC = pipe_rows<OP>();
-  auto kern = pipe_kernel<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS>;
+  auto kern = pipe_kernel<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8>;
   // allow the ring's dynamic shared memory: raised per device as needed
   static size_t configured[64];
   const bool cached = dev.device >= 0 && dev.device < 64;
@@ -462,7 +495,7 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
   return cudaGetLastError();
 }
 
-template <int OP, bool GFULL, bool MFULL>
+template <int OP, bool GFULL, bool MFULL, bool Q8 = false>
 cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
                         cudaStream_t stream) {
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
@@ -495,7 +528,7 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
     constexpr int SD = pipe_stages<OP>();
     auto go = [&](auto stages, auto cols) -> cudaError_t {
       constexpr int SS_ = decltype(stages)::value;
-      return launch_pipe_s<OP, T, SS_, GFULL, MFULL, decltype(cols)::value>(
+      return launch_pipe_s<OP, T, SS_, GFULL, MFULL, decltype(cols)::value, Q8>(
           dev, a, B, block, slices, SS_ * per_stage, stream);
     };
     auto by_cols = [&](auto stages) -> cudaError_t {

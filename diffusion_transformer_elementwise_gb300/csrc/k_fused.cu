@@ -20,6 +20,15 @@ cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb, bool gate_ful
                   : launch_row_op<OP_FUSED, false, false>(dev, dtype, vb, a, B, stream);
 }
 
+cudaError_t launch_fused_fp8(const DeviceInfo& dev, int dtype, bool gate_full, bool mod_full,
+                             const RowArgs& a, int64_t B, cudaStream_t stream) {
+  if (gate_full)
+    return mod_full ? launch_pipe<OP_FUSED, true, true, true>(dev, dtype, a, B, stream)
+                    : launch_pipe<OP_FUSED, true, false, true>(dev, dtype, a, B, stream);
+  return mod_full ? launch_pipe<OP_FUSED, false, true, true>(dev, dtype, a, B, stream)
+                  : launch_pipe<OP_FUSED, false, false, true>(dev, dtype, a, B, stream);
+}
+
 cudaError_t launch_fused_grouped(const DeviceInfo& dev, int dtype, bool gate_full,
                                  bool mod_full, const RowArgs* a, const int64_t* B, int count,
                                  cudaStream_t stream) {

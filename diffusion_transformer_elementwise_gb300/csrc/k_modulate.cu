@@ -18,6 +18,12 @@ cudaError_t launch_modulate(const DeviceInfo& dev, int dtype, int vb, bool mod_f
                   : launch_row_op<OP_MOD, false, false>(dev, dtype, vb, a, B, stream);
 }
 
+cudaError_t launch_modulate_fp8(const DeviceInfo& dev, int dtype, bool mod_full,
+                                const RowArgs& a, int64_t B, cudaStream_t stream) {
+  return mod_full ? launch_pipe<OP_MOD, false, true, true>(dev, dtype, a, B, stream)
+                  : launch_pipe<OP_MOD, false, false, true>(dev, dtype, a, B, stream);
+}
+
 cudaError_t launch_modulate_grouped(const DeviceInfo& dev, int dtype, bool mod_full,
                                     const RowArgs* a, const int64_t* B, int count,
                                     cudaStream_t stream) {

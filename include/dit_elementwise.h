@@ -9,6 +9,8 @@
  *   dit_rmsnorm_modulate           out = rms_norm(x, eps) * (1 + scale) + shift
  *   dit_gate_add_rmsnorm_modulate  both in one pass: writes the new residual
  *                                  and the modulated input of the next site
+ *   dit_*_fp8                      the modulation / fused op with an FP8
+ *                                  (E4M3) modulated output
  *   dit_gelu_tanh                  the feed-forward's tanh-GELU, elementwise
  *   dit_grouped                    one of the first three over several
  *                                  problems (e.g. video and audio streams)
@@ -211,6 +213,51 @@ dit_status dit_gate_add_rmsnorm_modulate_strided(
  */
 dit_status dit_gelu_tanh(void* out, const void* x, int64_t n, dit_dtype dtype,
                          dit_stream_t stream);
+
+/*
+ * Modulated output quantised to FP8 (OCP E4M3: 4 exponent bits, bias 7, 3
+ * fraction bits, no infinities, largest finite 448), with a static
+ * per-tensor scale:
+ *   y   = the fp32 modulation value of dit_rmsnorm_modulate (before any
+ *         rounding to the activation dtype)
+ *   out = e4m3(fl32(y * fl32(1 / *quant_scale)))
+ * rounded to nearest-even, saturating to +-448 (infinities included); NaN
+ * stays NaN.  One byte per element, [B, L, D] row-major.
+ *
+ * Source: the prhub summary of sglang PR #34172 lists, among its related
+ * PRs, the RMSNorm + FP8 quantisation fusion of the same fused-norm family;
+ * the pages give neither the format nor the scaling, so the plainest
+ * readings are taken: E4M3 (the activation FP8 format of such fusions), a
+ * per-tensor scale that divides (applied as a multiplication by its
+ * correctly rounded reciprocal), saturation instead of overflow.
+ *
+ * quant_scale: DEVICE pointer to one fp32 value, finite and > 0 (read by the
+ * kernel, so it may change between graph replays; not checked on the host:
+ * other values give defined but meaningless codes).  vec_stride: as in the
+ * _strided calls.
+ *
+ * These calls take the staged row kernel only: every input pointer (and
+ * residual_out) 16-byte aligned, D * element_size a multiple of 16 bytes (a
+ * multiple of 16 elements is what FP8 GEMM inputs need anyway), the vector
+ * stride in bytes a multiple of 16, and `out` aligned to 8 bytes (bf16/fp16)
+ * or 4 (fp32) -- otherwise DIT_ERR_MISALIGNED; rows of at most 16 KB (D <=
+ * 8192 for 16-bit, 4096 for fp32) -- otherwise DIT_ERR_BAD_SHAPE.  `out`
+ * may not overlap any other tensor or *quant_scale.
+ */
+dit_status dit_rmsnorm_modulate_fp8(void* out, const void* x, const void* scale,
+                                    const void* shift, int64_t B, int64_t L,
+                                    int64_t D, float eps, dit_dtype dtype,
+                                    dit_layout mod_layout, int64_t vec_stride,
+                                    const float* quant_scale, dit_stream_t stream);
+
+/* The fused op with its modulated output in E4M3 (residual_out keeps the
+ * dtype, bitwise that of dit_residual_gate_add). */
+dit_status dit_gate_add_rmsnorm_modulate_fp8(
+    void* residual_out, void* out, const void* hidden, const void* update,
+    const void* gate, const void* scale, const void* shift, int64_t B,
+    int64_t L, int64_t D, float eps, dit_dtype dtype, dit_layout gate_layout,
+    dit_layout mod_layout, int64_t vec_stride, const float* quant_scale,
+    dit_stream_t stream);
 
 /*
  * Grouped launches: one operation over up to DIT_MAX_GROUP independent

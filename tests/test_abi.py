@@ -233,3 +233,41 @@ def test_selfcheck_validation(lib):
     import torch
     if not torch.cuda.is_available():
         assert f(FUSED, BF16, BCAST, BCAST, 64, W, n, CNT, None) == NODEV
+
+
+def test_fp8_validation(lib):
+    """E4M3-output calls: the staged kernel's rules (16-byte aligned inputs and
+    rows, output aligned to its per-granule store, rows of at most 16 KB),
+    the quantisation scale as a device pointer, and one byte per output
+    element in the aliasing checks."""
+    f, g = lib.dit_rmsnorm_modulate_fp8, lib.dit_gate_add_rmsnorm_modulate_fp8
+    Q = A * 9
+    B, L, D = 1, 4, 64
+
+    def mod8(out=O, x=H, s=S, sh=SH, D=D, dt=BF16, lay=BCAST, vs=None, q=Q, eps=1e-6):
+        return f(out, x, s, sh, B, L, D, eps, dt, lay, D if vs is None else vs, q, None)
+
+    def fused8(r=O2, out=O, h=H, u=U, gt=G, s=S, sh=SH, D=D, dt=BF16, q=Q):
+        return g(r, out, h, u, gt, s, sh, B, L, D, 1e-6, dt, BCAST, BCAST, D, q, None)
+
+    ok = (NODEV, LAUNCH, OK)
+    assert mod8() in ok and fused8() in ok
+    assert mod8(q=None) == NULLP and fused8(q=None) == NULLP
+    assert mod8(q=Q + 2) == MISALIGNED
+    assert mod8(x=H + 2) == MISALIGNED           # element-aligned, not 16-byte aligned
+    assert fused8(r=O2 + 8) == MISALIGNED
+    assert mod8(D=60) == MISALIGNED              # rows of 120 bytes
+    assert mod8(D=60, dt=FP32) in ok             # 240 bytes = 15 * 16
+    assert mod8(D=62, dt=FP32) == MISALIGNED     # 248 bytes
+    assert mod8(out=O + 8) in ok                 # 8-byte aligned E4M3 output for 16-bit input
+    assert mod8(out=O + 4) == MISALIGNED
+    assert mod8(out=O + 4, dt=FP32) in ok        # 4-byte stores for fp32 input
+    assert mod8(D=8192) in ok and mod8(D=8200) == SHAPE
+    assert mod8(D=4096, dt=FP32) in ok and mod8(D=4104, dt=FP32) == SHAPE
+    assert mod8(eps=-1.0) == EPS
+    assert mod8(out=H + B * L * D * 2 - 16) == ALIAS   # inside x
+    assert mod8(out=Q - 32) == ALIAS                    # covers the scale word
+    assert mod8(out=H - B * L * D) in ok                # ends right where x begins
+    assert fused8(out=O2 + 64) == ALIAS                 # inside the residual
+    assert fused8(r=H) in ok                            # residual in place
+    assert f(None, None, None, None, 0, L, D, 1e-6, BF16, BCAST, D, None, None) == OK
