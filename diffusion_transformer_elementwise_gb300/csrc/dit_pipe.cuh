@@ -473,10 +473,9 @@ __host__ __device__ constexpr int pipe_rows() {
 
 // Launch the staged kernel with S stages; returns cudaErrorNotSupported when
 // the row is too long for it (the caller then uses the two-pass kernel).
-template <int OP, class T, int S, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false>
+template <int OP, class T, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false>
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
-  constexpr int RC = pipe_rows<OP, Q8>();
   auto kern = pipe_kernel<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8>;
   // allow the ring's dynamic shared memory: raised per device as needed
   static size_t configured[64];
@@ -503,6 +502,14 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
   return cudaGetLastError();
 }
 
+// Depth by shape (same-box sweeps, graph-replayed and L2-flushed, bf16 rows
+// of 3072-4608 elements): the residual gate's four rows per stage fill a
+// CTA's 128 KB ring, one CTA per SM, which pays off only with many rows per
+// SM ([1,32640,4096]); with fewer ([1,8160,4096], [1,4096,4608]) two rows
+// per stage and more CTAs are faster (31.5 -> 29.8 and 24.0 -> 19.7 us
+// graph-replayed, 31.4 -> 29.3 and 25.2 -> 23.2 us flushed).
+constexpr int64_t kRgaDeepRowsPerSm = 128;  // below: 2 rows per stage
+
 template <int OP, bool GFULL, bool MFULL, bool Q8 = false>
 cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
                         cudaStream_t stream) {
@@ -512,6 +519,10 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   a.nvec = row_bytes / 16;
   constexpr int VPT = pipe_vpt<OP>();
   const int64_t threads_needed = (a.nvec + VPT - 1) / VPT;
+  const int64_t rows_per_sm = B * a.L / (dev.sm_count > 0 ? dev.sm_count : 1);
+  constexpr bool kTwoRowsToo = OP == OP_RGA && RC > 2;  // an RC = 2 variant exists
+  const bool two_rows = kTwoRowsToo && rows_per_sm < kRgaDeepRowsPerSm;
+  const int rc = two_rows ? 2 : RC;
   int block;
   unsigned slices = 1;
   if (OP == OP_RGA) {
@@ -523,32 +534,38 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
     if (threads_needed > kPipeBlockMax) return cudaErrorNotSupported;
     block = (int)((threads_needed + 31) / 32 * 32);
   }
-  const size_t per_stage = (size_t)RC * NS * VPT * block * 16;
+  const size_t per_stage = (size_t)rc * NS * VPT * block * 16;
   const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
-  int S = pipe_stages<OP>();
+  constexpr int SD = pipe_stages<OP>();
+  int S = SD;
   while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;  // smaller rings
   if (per_stage * S > limit) return cudaErrorNotSupported;
-  // instantiated stage counts: the operation's default, 3 and 2 (when the
-  // default ring does not fit in shared memory)
   const bool allcols = (int64_t)block * VPT * slices == a.nvec;
   return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
     using T = typename decltype(tt)::type;
-    constexpr int SD = pipe_stages<OP>();
-    auto go = [&](auto stages, auto cols) -> cudaError_t {
+    auto go = [&](auto stages, auto rows, auto cols) -> cudaError_t {
       constexpr int SS_ = decltype(stages)::value;
-      return launch_pipe_s<OP, T, SS_, GFULL, MFULL, decltype(cols)::value, Q8>(
+      constexpr int RR_ = decltype(rows)::value;
+      return launch_pipe_s<OP, T, SS_, RR_, GFULL, MFULL, decltype(cols)::value, Q8>(
           dev, a, B, block, slices, SS_ * per_stage, stream);
     };
-    auto by_cols = [&](auto stages) -> cudaError_t {
-      return allcols ? go(stages, std::true_type{}) : go(stages, std::false_type{});
+    auto by_cols = [&](auto stages, auto rows) -> cudaError_t {
+      return allcols ? go(stages, rows, std::true_type{}) : go(stages, rows, std::false_type{});
     };
+    auto by_rows = [&](auto stages) -> cudaError_t {
+      if constexpr (kTwoRowsToo)
+        if (two_rows) return by_cols(stages, std::integral_constant<int, 2>{});
+      return by_cols(stages, std::integral_constant<int, RC>{});
+    };
+    // instantiated stage counts: the default, 3 and 2 (when the default ring
+    // does not fit in shared memory)
     if constexpr (SD == 2) {
-      return by_cols(std::integral_constant<int, 2>{});
+      return by_rows(std::integral_constant<int, 2>{});
     } else {
-      if (S == SD) return by_cols(std::integral_constant<int, SD>{});
+      if (S == SD) return by_rows(std::integral_constant<int, SD>{});
       if constexpr (SD > 3)
-        if (S == 3) return by_cols(std::integral_constant<int, 3>{});
-      return by_cols(std::integral_constant<int, 2>{});
+        if (S == 3) return by_rows(std::integral_constant<int, 3>{});
+      return by_rows(std::integral_constant<int, 2>{});
     }
   });
 }
