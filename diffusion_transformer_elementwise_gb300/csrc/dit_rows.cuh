@@ -43,14 +43,21 @@ constexpr int kRowBlockMax = 512;  // threads; rows up to 16 KB stay in register
 
 // Register budget of the row kernel: by default the launch bound alone (up to
 // 128 registers at 512 threads); DIT_ROW_MAXNREG caps it for tuning builds.
+// With 2-byte accesses the default holds it to 64 registers (two CTAs of up
+// to 512 threads per SM): the bf16 modulation of 2-byte aligned rows took 86
+// registers unbounded, one 416-thread CTA per SM, and ran at two thirds of
+// the fp16 kernel's speed (bounded: [1,4097,3077] 53.9 -> 39.6 us).  Wider
+// accesses were slower with the bound and keep the plain one.
+template <int VB>
+constexpr int row_min_blocks() { return VB == 2 ? 2 : 1; }
 #ifdef DIT_ROW_MAXNREG
-#define DIT_ROW_BOUNDS __maxnreg__(DIT_ROW_MAXNREG)
+#define DIT_ROW_BOUNDS(VB) __maxnreg__(DIT_ROW_MAXNREG)
 #else
-#define DIT_ROW_BOUNDS __launch_bounds__(kRowBlockMax)
+#define DIT_ROW_BOUNDS(VB) __launch_bounds__(kRowBlockMax, row_min_blocks<VB>())
 #endif
 
 template <int OP, class T, int VB, int R, bool GFULL, bool MFULL>
-__global__ void DIT_ROW_BOUNDS row_kernel(RowArgs a) {
+__global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
   using V = Vec<T, VB>;
   constexpr int N = V::N;
   constexpr int VPT = thread_bytes<VB>() / VB;
