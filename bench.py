@@ -509,6 +509,15 @@ def cpu_baseline(ops, budget_s=12.0, rows=512):
 # arms
 # ---------------------------------------------------------------------------
 
+def hotpath_config():
+    """The config of the headline workload (both arms print it)."""
+    return {"workload": "ltx2_bcast_s32640_c4096 hot path: rga_bcast, rga_bcast_inplace, "
+                        "rga_full, mod_bcast, fused_bcast",
+            "B": 1, "L": 32640, "D": 4096, "eps": EPS,
+            "l2": "no flush: every op reads its own inputs, each 267 MB or more, "
+                  "above the 129 MB L2"}
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle on the host cores, each step a
     bounded sample of the hot-path workload."""
@@ -556,8 +565,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / max(args.steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "ltx2_bcast_s32640_c4096 hot path (sampled rows)",
-                       "B": 1, "L": 32640, "D": 4096, "rows_per_step": rows},
+            "config": hotpath_config(),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -615,16 +623,15 @@ def run_ours(args):
                     "B": B, "L": L, "D": D, "blocks": 8}
     else:
         ops = hotpath_ops(device, only=args.op)
-        workload = {"workload": "ltx2_bcast_s32640_c4096 hot path: rga_bcast, "
-                                "rga_bcast_inplace, rga_full, mod_bcast, fused_bcast",
-                    "B": 1, "L": 32640, "D": 4096}
+        workload = hotpath_config()
         if args.op:
             workload["workload"] = f"ltx2_bcast_s32640_c4096 {args.op} only (profiling)"
     big = args.workload not in ("chain", "chain_av") or B * L * D * 2 > (129 << 20)
-    workload["l2"] = ("no flush: every op reads its own inputs, each 267 MB or more, "
-                      "above the 129 MB L2" if big else
-                      "no flush: the chain's buffers fit in the L2 (launch-bound case)")
-    workload["eps"] = EPS
+    if args.workload != "hotpath" or args.op:
+        workload["l2"] = ("no flush: every op reads its own inputs, each 267 MB or more, "
+                          "above the 129 MB L2" if big else
+                          "no flush: the chain's buffers fit in the L2 (launch-bound case)")
+        workload["eps"] = EPS
 
     with ClockSampler(local) as clk:
         total_ms, per_op = time_steps(ops, args.steps, args.warmup, dist)
