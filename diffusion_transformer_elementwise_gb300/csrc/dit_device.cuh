@@ -358,18 +358,15 @@ struct Granule {
   }
 };
 
-// hidden + update * gate on a pair.  For 16-bit storage the fp32 product of
-// two stored values is exact (8+8 or 11+11 significant bits), so one fused
-// multiply-add gives exactly fl(h + fl(u * g)); for fp32 storage the product
-// rounds, and the two operations are kept apart with the non-contractible
-// intrinsics.
+// hidden + update * gate on a pair, multiply then add, each rounded to
+// nearest (the non-contractible intrinsics: ptxas fuses a packed multiply and
+// a packed add into one FMA).  A fused multiply-add would differ for 16-bit
+// storage too: a negative product below fp32's range added to hidden = +0
+// gives +0 here and -0 from the FMA (found by the test of every bf16
+// update/gate pair).
 template <class T>
 __device__ __forceinline__ F2 residual_gate2(F2 h, F2 u, F2 g) {
-  if constexpr (sizeof(T) == 2) {
-    return f2_fma(u, g, h);
-  } else {
-    return f2(residual_gate(f2_lo(h), f2_lo(u), f2_lo(g)), residual_gate(f2_hi(h), f2_hi(u), f2_hi(g)));
-  }
+  return f2(residual_gate(f2_lo(h), f2_lo(u), f2_lo(g)), residual_gate(f2_hi(h), f2_hi(u), f2_hi(g)));
 }
 
 // fl(fl(n * one) + shift) per lane, n = x * r already formed: the product is

@@ -90,6 +90,7 @@ PINS = [
     lambda o: pr.test_bcast_equals_expanded_full_gate(o, "bf16"),
     lambda o: pr.test_bcast_batch_permutation(o),
     lambda o: pr.test_worked_examples_golden(o),
+    lambda o: pr.test_signed_zero_of_an_underflowing_product(o),
     lambda o: pr.test_exact_rational_bruteforce(o, "bf16", "bcast", (2, 3, 7)),
     lambda o: pr.test_exact_rational_bruteforce(o, "fp32", "full", (2, 3, 7)),
     lambda o: pm.test_zero_modulation_gives_unit_mean_square(o, "bcast"),

@@ -170,3 +170,20 @@ def test_bad_arguments_rejected(orc):
         orc.residual_gate_add(out, None, u, g, 1, 2, 3, "bf16", "full")
     # empty problems are fine and write nothing
     orc.residual_gate_add(None, None, None, None, 0, 5, 7, "bf16", "full")
+
+
+def test_signed_zero_of_an_underflowing_product(orc):
+    """Multiply, then add (reading R1): a product of bf16 subnormals below
+    fp32's range rounds to a signed zero first, and +0 + (-0) = +0 in
+    round-to-nearest; a fused multiply-add would keep the sign of the exact
+    product and give -0.  With hidden = -0 the sum of two negative zeros is
+    -0 either way."""
+    tiny = 2.0 ** -133  # the smallest bf16 subnormal
+    cases = [(0.0, tiny, -tiny, 0x0000), (-0.0, tiny, -tiny, 0x8000),
+             (0.0, -tiny, -tiny, 0x0000), (-0.0, tiny, tiny, 0x0000),
+             (0.0, 0.0, -1.0, 0x0000)]
+    for hv, uv, gv, want in cases:
+        h, u, g = (torch.tensor([[[v]]], dtype=torch.float32).to(torch.bfloat16)
+                   for v in (hv, uv, gv))
+        out = oracle_rga(orc, h, u, g, "bf16", "full")
+        assert int(out.view(torch.int16).item()) & 0xFFFF == want, (hv, uv, gv)
