@@ -24,6 +24,7 @@
 // writes it back over its own hidden slot, and pass two reads it from there.
 #pragma once
 
+#include <atomic>
 #include <type_traits>
 
 #include "dit_device.cuh"
@@ -454,6 +455,27 @@ __host__ __device__ constexpr int pipe_vpt() {
 constexpr int kPipeBlockMax = 512;    // threads: rows up to 16 KB
 constexpr int kStaticSmemReserve = 1024;  // bytes kept for the static arrays
 
+// Let kernel `fn` take more than the default 48 KB of shared memory: once per
+// (kernel, device), its dynamic shared memory cap is raised to the most any
+// launch here asks for (the opt-in limit less the static reserve), so the cap
+// never shrinks under a launch from another host thread.  `opted`: that
+// kernel's per-device flags.
+constexpr int kOptinDevices = 64;
+inline cudaError_t allow_dynamic_smem(const void* fn, const DeviceInfo& dev, size_t smem,
+                                      std::atomic<int>* opted) {
+  if (smem + kStaticSmemReserve <= 48 * 1024) return cudaSuccess;
+  const bool cached = dev.device >= 0 && dev.device < kOptinDevices;
+  if (cached && opted[dev.device].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             dev.smem_optin - kStaticSmemReserve);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // do not leave it for the next call to report
+    return e;
+  }
+  if (cached) opted[dev.device].store(1, std::memory_order_release);
+  return cudaSuccess;
+}
+
 template <int OP>
 __host__ __device__ constexpr int pipe_stages() {
   return OP == OP_RGA ? DIT_PIPE_S_RGA : OP == OP_MOD ? DIT_PIPE_S_MOD : DIT_PIPE_S_FUSED;
@@ -477,18 +499,9 @@ template <int OP, class T, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, 
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
   auto kern = pipe_kernel<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8>;
-  // allow the ring's dynamic shared memory: raised per device as needed
-  static size_t configured[64];
-  const bool cached = dev.device >= 0 && dev.device < 64;
-  // (the default limit, 48 KB, covers static and dynamic shared memory together)
-  if (smem + kStaticSmemReserve > 48 * 1024 && (!cached || configured[dev.device] < smem)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();  // do not leave it for the next call to report
-      return e;
-    }
-    if (cached) configured[dev.device] = smem;
-  }
+  static std::atomic<int> opted[kOptinDevices];
+  const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
+  if (e != cudaSuccess) return e;
   // one wave of resident CTAs, each striding over the groups
   a.gpb = (a.L + RC - 1) / RC;
   a.ngroups = B * a.gpb;
@@ -631,17 +644,9 @@ cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs*
       constexpr int SS_ = decltype(stages)::value;
       auto kern = pipe_group_kernel<OP, T, VPT, SS_, RC, GFULL, MFULL, decltype(cols)::value>;
       const size_t smem = SS_ * per_stage;
-      static size_t configured[64];
-      const bool cached = dev.device >= 0 && dev.device < 64;
-      if (smem + kStaticSmemReserve > 48 * 1024 && (!cached || configured[dev.device] < smem)) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) {
-          (void)cudaGetLastError();
-          return e;
-        }
-        if (cached) configured[dev.device] = smem;
-      }
+      static std::atomic<int> opted[kOptinDevices];
+      const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
+      if (e != cudaSuccess) return e;
       const int64_t wave = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
       // Work units: (row group, column slice) pairs.  A CTA streams its
       // groups one after another, about one per memory round trip, so every
