@@ -536,20 +536,26 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   constexpr bool kTwoRowsToo = OP == OP_RGA && RC > 2;  // an RC = 2 variant exists
   const bool two_rows = kTwoRowsToo && rows_per_sm < kRgaDeepRowsPerSm;
   const int rc = two_rows ? 2 : RC;
+  const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
+  constexpr int SD = pipe_stages<OP>();
   int block;
   unsigned slices = 1;
   if (OP == OP_RGA) {
-    block = (int)((threads_needed < 256 ? threads_needed : 256) + 31) / 32 * 32;
-    const int64_t s = (a.nvec + (int64_t)block * VPT - 1) / ((int64_t)block * VPT);
+    // the widest block whose ring fits (at most kPipeBlockMax threads), then
+    // equal column slices: a row of 576 granules runs as one 288-thread slice,
+    // not as 256 + 32 busy threads of two 256-thread slices
+    int64_t bmax = (int64_t)(limit / ((size_t)rc * NS * VPT * 16 * SD)) / 32 * 32;
+    if (bmax > kPipeBlockMax) bmax = kPipeBlockMax;
+    if (bmax < 32) bmax = 32;
+    const int64_t s = (threads_needed + bmax - 1) / bmax;
     if (s > 65535) return cudaErrorInvalidConfiguration;
     slices = (unsigned)s;
+    block = (int)(((threads_needed + s - 1) / s + 31) / 32 * 32);
   } else {
     if (threads_needed > kPipeBlockMax) return cudaErrorNotSupported;
     block = (int)((threads_needed + 31) / 32 * 32);
   }
   const size_t per_stage = (size_t)rc * NS * VPT * block * 16;
-  const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
-  constexpr int SD = pipe_stages<OP>();
   int S = SD;
   while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;  // smaller rings
   if (per_stage * S > limit) return cudaErrorNotSupported;

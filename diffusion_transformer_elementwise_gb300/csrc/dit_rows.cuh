@@ -355,12 +355,11 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
     int block;
     unsigned slices = 1;
     if (OP == OP_RGA) {
-      block = (int)(threads_needed < 256 ? threads_needed : 256);
-      block = (block + 31) / 32 * 32;
-      const int64_t per_cta = (int64_t)block * (TB / VB);
-      const int64_t s = (a.nvec + per_cta - 1) / per_cta;
+      // equal column slices of at most kRowBlockMax threads
+      const int64_t s = (threads_needed + kRowBlockMax - 1) / kRowBlockMax;
       if (s > 65535) return cudaErrorInvalidConfiguration;
       slices = (unsigned)s;
+      block = (int)(((threads_needed + s - 1) / s + 31) / 32 * 32);
     } else {
       if (threads_needed > kRowBlockMax) {
         too_long = true;
