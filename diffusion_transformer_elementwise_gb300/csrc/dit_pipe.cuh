@@ -520,7 +520,11 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
 // CTA's 128 KB ring, one CTA per SM, which pays off only with many rows per
 // SM ([1,32640,4096]); with fewer ([1,8160,4096], [1,4096,4608]) two rows
 // per stage and more CTAs are faster (31.5 -> 29.8 and 24.0 -> 19.7 us
-// graph-replayed, 31.4 -> 29.3 and 25.2 -> 23.2 us flushed).
+// graph-replayed, 31.4 -> 29.3 and 25.2 -> 23.2 us flushed).  The modulation
+// goes the other way, from one row per stage to two, below the same bound
+// (L2-flushed calls: [1,4096,4608] 23.3 -> 20.8 us, [1,8160,4096] 32.9 ->
+// 30.6 us); with many rows per SM one row stays faster inside a stream of
+// other kernels (the hot-path step: 6346 vs 6070 GB/s on [1,32640,4096]).
 constexpr int64_t kRgaDeepRowsPerSm = 128;  // below: 2 rows per stage
 
 template <int OP, bool GFULL, bool MFULL, bool Q8 = false>
@@ -533,7 +537,9 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   constexpr int VPT = pipe_vpt<OP>();
   const int64_t threads_needed = (a.nvec + VPT - 1) / VPT;
   const int64_t rows_per_sm = B * a.L / (dev.sm_count > 0 ? dev.sm_count : 1);
-  constexpr bool kTwoRowsToo = OP == OP_RGA && RC > 2;  // an RC = 2 variant exists
+  // an RC = 2 variant exists: the residual gate (default 4) and the
+  // 16-bit-output modulation (default 1)
+  constexpr bool kTwoRowsToo = (OP == OP_RGA && RC > 2) || (OP == OP_MOD && RC == 1);
   const bool two_rows = kTwoRowsToo && rows_per_sm < kRgaDeepRowsPerSm;
   const int rc = two_rows ? 2 : RC;
   const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
