@@ -372,6 +372,34 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
   pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>(a, blockIdx.x, blockIdx.y);
 }
 
+// The fused op's own entry, held to 80 registers: at its natural 94 two
+// 256-thread CTAs fit per SM, at 80 three (same-box, [1,32640,4096] bf16:
+// +2% in the hot-path step, the E4M3 variant 0.89 -> 0.98 of copy; 3-6% on
+// L2-flushed calls of every shape; no spills).  A register cap on the other
+// operations' kernels raised their allocation instead (ptxas uses the cap),
+// so they keep the plain launch bound.
+#ifndef DIT_PIPE_FUSED_MAXNREG
+#define DIT_PIPE_FUSED_MAXNREG 80
+#endif
+#ifdef DIT_PIPE_MAXNREG
+#define DIT_PIPE_FUSED_BOUNDS DIT_PIPE_BOUNDS
+#else
+#define DIT_PIPE_FUSED_BOUNDS __maxnreg__(DIT_PIPE_FUSED_MAXNREG)  // 80 x 512 threads fit
+#endif
+template <class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false>
+__global__ void DIT_PIPE_FUSED_BOUNDS pipe_fused_kernel(RowArgs a) {
+  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>(a, blockIdx.x, blockIdx.y);
+}
+
+// The kernel of one instantiation of the staged row path.
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8>
+constexpr auto pipe_kernel_for() {
+  if constexpr (OP == OP_FUSED)
+    return pipe_fused_kernel<T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>;
+  else
+    return pipe_kernel<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>;
+}
+
 // Several problems of one operation in one launch: problem p owns the CTAs
 // [begin[p], begin[p+1]), slices[p] per schedule position (column slices of
 // the residual gate's long rows; 1 otherwise).  Every problem runs the same
@@ -498,7 +526,7 @@ __host__ __device__ constexpr int pipe_rows() {
 template <int OP, class T, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false>
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
-  auto kern = pipe_kernel<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8>;
+  auto kern = pipe_kernel_for<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8>();
   static std::atomic<int> opted[kOptinDevices];
   const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
   if (e != cudaSuccess) return e;
