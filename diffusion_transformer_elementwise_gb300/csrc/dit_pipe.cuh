@@ -243,6 +243,11 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
 
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) issue();
+  // the first batch's vectors load while the first groups' copies are in
+  // flight (cta < ngroups, so that batch exists)
+  int64_t cb = cta / a.gpb, cg = cta - cb * a.gpb;
+  int64_t vec_b = cb;  // batch whose vectors are in registers
+  load_vectors(cb);
 
   __shared__ __align__(16) float part[2][RC][16];  // per-warp row partials (<= 16 warps)
   // entries of warps this CTA does not have stay zero (read by the tree sum)
@@ -345,8 +350,6 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
     }
   };
 
-  int64_t cb = cta / a.gpb, cg = cta - cb * a.gpb;
-  int64_t vec_b = -1;  // batch whose vectors are in registers
   while (cb < nbatch) {
     cp_async_wait<S - 2>();  // this thread's copies of this group have landed
     issue();                 // refill the stage consumed by the previous group
