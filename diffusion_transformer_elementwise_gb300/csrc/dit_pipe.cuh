@@ -1,4 +1,5 @@
-// dit_pipe.cuh -- shared-memory-staged row kernels (16-byte aligned rows).
+// dit_pipe.cuh -- shared-memory-staged row kernels (16-byte aligned rows, and
+// by phase rows of any pitch in 16-byte aligned tensors).
 //
 // Each thread streams the 16-byte granules it owns -- granules t + k * T of
 // every row, k < VPT, for T threads -- from HBM into its own slots of an
@@ -38,6 +39,12 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// the first `bytes` bytes of a 16-byte granule, the rest of the slot zeroed
+// (the last granule of a phased tensor: nothing past its end is read)
+__device__ __forceinline__ void cp_async16_part(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -127,12 +134,51 @@ __device__ __forceinline__ Raw<2 * P> quantise_e4m3(const F2 (&y)[P], F2 qinv) {
   return r;
 }
 
+// Phased rows: element i of a 16-byte granule (16 / sizeof(T) elements, pair
+// i / 2 of the widened granule) belongs to the row when lo <= i < hi.  The
+// row's elements of a granule it shares with a neighbouring row are stored
+// one by one, so that the neighbour's elements are never written here.
+template <class T>
+__device__ __forceinline__ void store_part(char* dst, const Raw<16>& r, int lo, int hi) {
+  constexpr int ES = (int)sizeof(T);
+#pragma unroll
+  for (int i = 0; i < 16 / ES; ++i) {
+    if (i < lo || i >= hi) continue;
+    if constexpr (ES == 4) {
+      Raw<4> v;
+      v.w[0] = r.w[i];
+      st_stream<4>(dst + i * 4, v);
+    } else {
+      Raw<2> v;
+      v.h = (uint16_t)(r.w[i >> 1] >> ((i & 1) * 16));
+      st_stream<2>(dst + i * 2, v);
+    }
+  }
+}
+// the granule's elements outside [lo, hi) set to zero (they add nothing to
+// the row's sum of squares)
+template <class T>
+__device__ __forceinline__ void mask_part(F2 (&x)[Granule<T>::P], int lo, int hi) {
+#pragma unroll
+  for (int i = 0; i < Granule<T>::P; ++i) {
+    const int e = 2 * i;
+    x[i] = f2(e >= lo && e < hi ? f2_lo(x[i]) : 0.0f, e + 1 >= lo && e + 1 < hi ? f2_hi(x[i]) : 0.0f);
+  }
+}
+
 // The body of one CTA: CTA `cta` of the problem's grid-stride schedule, on
 // column slice `slice` of the row.  Q8: the modulated output is OCP E4M3
 // (one byte per element, a.out2 for the fused op, a.out otherwise), the
-// fp32 value scaled by fl(1 / *a.qscale) first.
+// fp32 value scaled by fl(1 / *a.qscale) first.  PH (phased rows): the row
+// pitch is not a multiple of 16 bytes but every streamed tensor starts on a
+// 16-byte boundary; one row per group, and the grid is a multiple of the
+// period of the rows' offsets modulo 16, so all the rows a CTA takes start
+// the same `off` bytes past a 16-byte boundary.  The CTA copies the 16-byte
+// granules from that boundary on (a row's first and last granule hold
+// elements of its neighbours, masked out of the sum and never stored) and
+// holds its [B, 1, D] operands shifted by the same offset.
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS,
-          bool Q8 = false>
+          bool Q8 = false, bool PH = false>
 __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, const int64_t slice) {
   using G = Granule<T>;
   constexpr int P = G::P;  // fp32 pairs per 16-byte granule
@@ -150,29 +196,82 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   const int warp = tid >> 5;
   const int nwarps = nthr >> 5;
 
+  static_assert(!PH || (RC == 1 && !Q8 && !ALLCOLS), "phased rows: one row per group");
   if (cta >= a.ngroups) return;  // uniform over the CTA
-  const int64_t pitch = a.D * (int64_t)sizeof(T);
+  constexpr int ES = (int)sizeof(T);
+  constexpr int EPG = 16 / ES;  // elements per granule
+  const int64_t pitch = a.D * (int64_t)ES;
+  // phased rows: the byte offset of this CTA's rows past a 16-byte boundary
+  // (its first row is row `cta`), and the granules a row spans
+  int off = 0;
+  if constexpr (PH) off = (int)(((uint64_t)cta * (uint64_t)(pitch & 15)) & 15u);
+  const int64_t ngran = PH ? (off + pitch + 15) >> 4 : a.nvec;
 
   // this thread's granules: t + k * T (+ the column slice of the residual gate)
   const int64_t g0 = slice * nthr * VPT + tid;
   bool cval[VPT];
+  // phased rows: granule k's slots [lo, hi) belong to the row, packed as
+  // byte k = lo | hi << 4 (one register for every k)
+  [[maybe_unused]] uint32_t bounds = 0;
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) cval[k] = ALLCOLS || g0 + (int64_t)k * nthr < a.nvec;
+  for (int k = 0; k < VPT; ++k) {
+    const int64_t gk = g0 + (int64_t)k * nthr;
+    cval[k] = ALLCOLS || gk < ngran;
+    if constexpr (PH) {
+      const int64_t e = (gk * 16 - off) / ES;  // the row element at slot 0
+      const uint32_t lo = e < 0 ? (uint32_t)-e : 0u;
+      const uint32_t hi = a.D - e < EPG ? (uint32_t)(a.D - e) : (uint32_t)EPG;
+      bounds |= (lo | hi << 4) << (8 * k);
+    }
+  }
+  [[maybe_unused]] auto plo = [&](int k) { return (int)((bounds >> (8 * k)) & 15u); };
+  [[maybe_unused]] auto phi = [&](int k) { return (int)((bounds >> (8 * k + 4)) & 15u); };
+  // a phased granule shared with a neighbouring row
+  auto partial = [&](int k) {
+    if constexpr (PH)
+      return ((bounds >> (8 * k)) & 255u) != (uint32_t)EPG << 4;
+    else
+      return false;
+  };
   const int64_t kstride = (int64_t)nthr * 16;  // bytes between a thread's granules
 
   // [B, 1, D] operands of batch bb in fp32: gate; 1 + scale (one rounding); shift
   F2 gv[VPT][P], onev[VPT][P], shv[VPT][P];
   auto load_vectors = [&](int64_t bb) {
+    if constexpr (PH) {
+      // element by element, at the rows' offset (slots outside the row: 0)
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      if (!cval[k]) continue;
-      const int64_t off = bb * a.vstride + g0 * 16 + k * kstride;
-      if constexpr (kGate && !GFULL) G::widen(ld_bcast<16>((const char*)a.g + off), gv[k]);
-      if constexpr (kReduce && !MFULL) {
-        G::widen(ld_bcast<16>((const char*)a.sc + off), onev[k]);
+      for (int k = 0; k < VPT; ++k) {
+        if (!cval[k]) continue;
+        const int lo = plo(k), hi = phi(k);
+        const int64_t e0 = ((g0 + (int64_t)k * nthr) * 16 - off) / ES;  // the row element at slot 0
+        const int64_t vb = bb * a.vstride + e0 * ES;
+        auto elem = [&](const void* v, int i) {
+          float f[1] = {0.0f};
+          if (i >= lo && i < hi) Vec<T, ES>::widen(ld_bcast<ES>((const char*)v + vb + i * ES), f);
+          return f[0];
+        };
 #pragma unroll
-        for (int i = 0; i < P; ++i) onev[k][i] = f2_add(f2(1.0f, 1.0f), onev[k][i]);
-        G::widen(ld_bcast<16>((const char*)a.sh + off), shv[k]);
+        for (int i = 0; i < P; ++i) {
+          if constexpr (kGate && !GFULL) gv[k][i] = f2(elem(a.g, 2 * i), elem(a.g, 2 * i + 1));
+          if constexpr (kReduce && !MFULL) {
+            onev[k][i] = f2_add(f2(1.0f, 1.0f), f2(elem(a.sc, 2 * i), elem(a.sc, 2 * i + 1)));
+            shv[k][i] = f2(elem(a.sh, 2 * i), elem(a.sh, 2 * i + 1));
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!cval[k]) continue;
+        const int64_t vo = bb * a.vstride + g0 * 16 + k * kstride;
+        if constexpr (kGate && !GFULL) G::widen(ld_bcast<16>((const char*)a.g + vo), gv[k]);
+        if constexpr (kReduce && !MFULL) {
+          G::widen(ld_bcast<16>((const char*)a.sc + vo), onev[k]);
+#pragma unroll
+          for (int i = 0; i < P; ++i) onev[k][i] = f2_add(f2(1.0f, 1.0f), onev[k][i]);
+          G::widen(ld_bcast<16>((const char*)a.sh + vo), shv[k]);
+        }
       }
     }
   };
@@ -225,13 +324,26 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
       for (int j = 0; j < RC; ++j) {
         const int64_t row = row0 + j;
         if (row < rend) {
-          const int64_t rowoff = row * pitch;
+          const int64_t rowoff = row * pitch - off;
+          // phased rows: the last row's last granule may run past the
+          // tensors' end (uniform test)
+          const bool tail = PH && row == a.rows - 1;
 #pragma unroll
           for (int op = 0; op < NS; ++op) {
             const char* src = gp[op] + rowoff;
 #pragma unroll
-            for (int k = 0; k < VPT; ++k)
-              if (cval[k]) cp_async16(issue_stage + j * JS + op * OS + k * KS, src + k * kstride);
+            for (int k = 0; k < VPT; ++k) {
+              if (!cval[k]) continue;
+              const uint32_t dst = issue_stage + j * JS + op * OS + k * KS;
+              if (tail) {
+                const int64_t left = a.rows * pitch - (rowoff + (g0 + (int64_t)k * nthr) * 16);
+                if (left < 16) {
+                  cp_async16_part(dst, src + k * kstride, (uint32_t)left);
+                  continue;
+                }
+              }
+              cp_async16(dst, src + k * kstride);
+            }
           }
         }
       }
@@ -264,7 +376,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
     for (int j = 0; j < RC; ++j) {
       ss[j] = 0.0f;
       if (CHECK && row0 + j >= rend) continue;
-      [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch;
+      [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
       F2 acc[P];  // independent accumulators: no serial FMA chain
 #pragma unroll
       for (int i = 0; i < P; ++i) acc[i] = f2(0.0f, 0.0f);
@@ -281,7 +393,10 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
 #pragma unroll
           for (int i = 0; i < P; ++i) x[i] = residual_gate2<T>(h[i], u[i], GFULL ? gf[i] : gv[k][i]);
           const Raw<16> r = G::narrow(x);
-          st_stream<16>(out1 + rowoff + k * kstride, r);
+          if (partial(k))
+            store_part<T>(out1 + rowoff + k * kstride, r, plo(k), phi(k));
+          else
+            st_stream<16>(out1 + rowoff + k * kstride, r);
           if constexpr (kReduce) {
             sts16(sl + kX * OS, r);  // the stored residual, read again in pass two
             G::widen(r, x);
@@ -290,6 +405,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
           G::widen(lds16(sl + kX * OS), x);
         }
         if constexpr (kReduce) {
+          if (partial(k)) mask_part<T>(x, plo(k), phi(k));
 #pragma unroll
           for (int i = 0; i < P; ++i) acc[i] = f2_fma(x[i], x[i], acc[i]);
         }
@@ -322,7 +438,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
       for (int j = 0; j < RC; ++j) {
         const float r = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
         if (CHECK && row0 + j >= rend) continue;
-        [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch;
+        [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
         const F2 r2 = f2(r, r);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -343,6 +459,8 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
           }
           if constexpr (Q8)
             st_stream<2 * P>(out2 + (row0 + j) * qpitch + k * qkstride, quantise_e4m3<P>(y, qinv));
+          else if (partial(k))
+            store_part<T>(out2 + rowoff + k * kstride, G::narrow(y), plo(k), phi(k));
           else
             st_stream<16>(out2 + rowoff + k * kstride, G::narrow(y));
         }
@@ -370,9 +488,9 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
 }
 
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS,
-          bool Q8 = false>
+          bool Q8 = false, bool PH = false>
 __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
-  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>(a, blockIdx.x, blockIdx.y);
+  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>(a, blockIdx.x, blockIdx.y);
 }
 
 // The fused op's own entry, held to 80 registers: at its natural 94 two
@@ -389,18 +507,20 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
 #else
 #define DIT_PIPE_FUSED_BOUNDS __maxnreg__(DIT_PIPE_FUSED_MAXNREG)  // 80 x 512 threads fit
 #endif
-template <class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false>
+template <class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false,
+          bool PH = false>
 __global__ void DIT_PIPE_FUSED_BOUNDS pipe_fused_kernel(RowArgs a) {
-  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>(a, blockIdx.x, blockIdx.y);
+  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>(a, blockIdx.x, blockIdx.y);
 }
 
 // The kernel of one instantiation of the staged row path.
-template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8>
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8,
+          bool PH>
 constexpr auto pipe_kernel_for() {
   if constexpr (OP == OP_FUSED)
-    return pipe_fused_kernel<T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>;
+    return pipe_fused_kernel<T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>;
   else
-    return pipe_kernel<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8>;
+    return pipe_kernel<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>;
 }
 
 // Several problems of one operation in one launch: problem p owns the CTAs
@@ -507,6 +627,10 @@ inline cudaError_t allow_dynamic_smem(const void* fn, const DeviceInfo& dev, siz
   return cudaSuccess;
 }
 
+// stages of the phased kernel (one row per stage)
+#ifndef DIT_PIPE_S_PHASED
+#define DIT_PIPE_S_PHASED 2
+#endif
 template <int OP>
 __host__ __device__ constexpr int pipe_stages() {
   return OP == OP_RGA ? DIT_PIPE_S_RGA : OP == OP_MOD ? DIT_PIPE_S_MOD : DIT_PIPE_S_FUSED;
@@ -526,10 +650,11 @@ __host__ __device__ constexpr int pipe_rows() {
 
 // Launch the staged kernel with S stages; returns cudaErrorNotSupported when
 // the row is too long for it (the caller then uses the two-pass kernel).
-template <int OP, class T, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false>
+template <int OP, class T, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false,
+          bool PH = false>
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
-  auto kern = pipe_kernel_for<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8>();
+  auto kern = pipe_kernel_for<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>();
   static std::atomic<int> opted[kOptinDevices];
   const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
   if (e != cudaSuccess) return e;
@@ -538,6 +663,13 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
   a.ngroups = B * a.gpb;
   int64_t G = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
   if (G > a.ngroups) G = a.ngroups;
+  if constexpr (PH) {
+    // rows r and r + G start at the same offset modulo 16 bytes when G is a
+    // multiple of 16 / gcd(pitch, 16) (a power of two, at most 8)
+    const int64_t m = (a.D * (int64_t)sizeof(T)) & 15;
+    const int64_t period = m ? 16 / (m & -m) : 1;
+    if (G < a.ngroups) G -= G % period;
+  }
   if (G < 1) G = 1;
   if (G > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   a.step_b = G / a.gpb;
@@ -558,13 +690,17 @@ cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block
 // other kernels (the hot-path step: 6346 vs 6070 GB/s on [1,32640,4096]).
 constexpr int64_t kRgaDeepRowsPerSm = 128;  // below: 2 rows per stage
 
+// phased: rows whose pitch is not a multiple of 16 bytes, every streamed
+// tensor 16-byte aligned (one row per group; see pipe_body).
 template <int OP, bool GFULL, bool MFULL, bool Q8 = false>
 cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool phased = false) {
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
   constexpr int RC = pipe_rows<OP, Q8>();
+  if (Q8 && phased) return cudaErrorNotSupported;
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
-  a.nvec = row_bytes / 16;
+  // granules per row (phased: at most, over the rows' offsets)
+  a.nvec = phased ? (row_bytes + 30) / 16 : row_bytes / 16;
   constexpr int VPT = pipe_vpt<OP>();
   const int64_t threads_needed = (a.nvec + VPT - 1) / VPT;
   const int64_t rows_per_sm = B * a.L / (dev.sm_count > 0 ? dev.sm_count : 1);
@@ -572,7 +708,7 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   // 16-bit-output modulation (default 1)
   constexpr bool kTwoRowsToo = (OP == OP_RGA && RC > 2) || (OP == OP_MOD && RC == 1);
   const bool two_rows = kTwoRowsToo && rows_per_sm < kRgaDeepRowsPerSm;
-  const int rc = two_rows ? 2 : RC;
+  const int rc = phased ? 1 : two_rows ? 2 : RC;
   const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
   constexpr int SD = pipe_stages<OP>();
   int block;
@@ -596,19 +732,31 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   int S = SD;
   while (S > 2 && per_stage * S > limit) S = S > 3 ? 3 : 2;  // smaller rings
   if (per_stage * S > limit) return cudaErrorNotSupported;
-  const bool allcols = (int64_t)block * VPT * slices == a.nvec;
+  const bool allcols = !phased && (int64_t)block * VPT * slices == a.nvec;
   return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
     using T = typename decltype(tt)::type;
-    auto go = [&](auto stages, auto rows, auto cols) -> cudaError_t {
+    auto go = [&](auto stages, auto rows, auto cols, auto ph) -> cudaError_t {
       constexpr int SS_ = decltype(stages)::value;
       constexpr int RR_ = decltype(rows)::value;
-      return launch_pipe_s<OP, T, SS_, RR_, GFULL, MFULL, decltype(cols)::value, Q8>(
-          dev, a, B, block, slices, SS_ * per_stage, stream);
+      return launch_pipe_s<OP, T, SS_, RR_, GFULL, MFULL, decltype(cols)::value, Q8,
+                           decltype(ph)::value>(dev, a, B, block, slices, SS_ * per_stage,
+                                                stream);
     };
     auto by_cols = [&](auto stages, auto rows) -> cudaError_t {
-      return allcols ? go(stages, rows, std::true_type{}) : go(stages, rows, std::false_type{});
+      return allcols ? go(stages, rows, std::true_type{}, std::false_type{})
+                     : go(stages, rows, std::false_type{}, std::false_type{});
     };
     auto by_rows = [&](auto stages) -> cudaError_t {
+      if constexpr (!Q8) {
+        if (phased) {
+          constexpr int SP = DIT_PIPE_S_PHASED;
+          if (SP > 2 && per_stage * SP <= limit)
+            return go(std::integral_constant<int, SP>{}, std::integral_constant<int, 1>{},
+                      std::false_type{}, std::true_type{});
+          return go(std::integral_constant<int, 2>{}, std::integral_constant<int, 1>{},
+                    std::false_type{}, std::true_type{});
+        }
+      }
       if constexpr (kTwoRowsToo)
         if (two_rows) return by_cols(stages, std::integral_constant<int, 2>{});
       return by_cols(stages, std::integral_constant<int, RC>{});

@@ -316,13 +316,36 @@ cudaError_t launch_long_rows(const DeviceInfo& dev, int dtype, int vb, RowArgs a
   });
 }
 
+// Whether every tensor the staged kernel streams or stores starts on a
+// 16-byte boundary (the [B, 1, D] operands, read element by element in the
+// phased kernel, may start anywhere).
+template <int OP, bool GFULL, bool MFULL>
+bool streamed_bases_aligned(const RowArgs& a) {
+  uintptr_t bits = (uintptr_t)a.out | (uintptr_t)a.x;
+  if (OP != OP_MOD) bits |= (uintptr_t)a.u;
+  if (OP != OP_MOD && GFULL) bits |= (uintptr_t)a.g;
+  if (OP != OP_RGA && MFULL) bits |= (uintptr_t)a.sc | (uintptr_t)a.sh;
+  if (OP == OP_FUSED) bits |= (uintptr_t)a.out2;
+  return (bits & 15u) == 0;
+}
+
 // Rows aligned to 16 bytes take the shared-memory-staged kernel (dit_pipe.cuh);
-// narrower alignments the register-resident row kernel; rows too long for
-// one CTA the two-pass kernel.
+// rows of other pitches whose tensors start on 16-byte boundaries take it by
+// phase -- except the reducing operations on 8-byte aligned rows, where the
+// register kernel's 8-byte accesses were as fast or faster (L2-flushed,
+// [1,4097,3076] bf16: modulation 22.4 vs 22.7 us, fused 33.2 vs 36.8 us; the
+// residual gate 20.1 vs 20.5 us phased); other narrow alignments the
+// register-resident row kernel; rows too long for one CTA the two-pass kernel.
 template <int OP, bool GFULL, bool MFULL>
 cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, int64_t B,
                           cudaStream_t stream) {
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
+#ifndef DIT_ROWS_IN_REGISTERS
+  if (vb < 16 && (OP == OP_RGA || vb < 8) && streamed_bases_aligned<OP, GFULL, MFULL>(a)) {
+    const cudaError_t e = launch_pipe<OP, GFULL, MFULL>(dev, dtype, a, B, stream, true);
+    if (e != cudaErrorNotSupported) return e;
+  }
+#endif
 #ifdef DIT_ROWS_IN_REGISTERS  // tuning builds: the register kernel for every width
   if (false) {
 #else
