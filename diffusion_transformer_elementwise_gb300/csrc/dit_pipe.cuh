@@ -233,6 +233,19 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
     else
       return false;
   };
+  // phased rows of the residual gate: the warps that own a row's first or
+  // last granule take the masked code path, the others the aligned one (a
+  // warp-uniform branch; [1,4097,3077] bf16 L2-flushed 21.1 -> 19.6 us).  The
+  // reducing operations test every granule instead: the two copies of their
+  // larger passes cost them 9-16% on the same shapes.
+  constexpr bool kSplit = PH && !kReduce;
+  bool edge_warp = false;
+  if constexpr (kSplit) {
+    bool mine = false;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) mine = mine || (cval[k] && partial(k));
+    edge_warp = __any_sync(0xFFFFFFFFu, mine);
+  }
   const int64_t kstride = (int64_t)nthr * 16;  // bytes between a thread's granules
 
   // [B, 1, D] operands of batch bb in fp32: gate; 1 + scale (one rounding); shift
@@ -372,49 +385,63 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   auto group = [&](int64_t row0, int64_t rend, auto check_tag) {
     constexpr bool CHECK = decltype(check_tag)::value;
     float ss[RC];
+    // pass one: the residual (stored), the row sums of squares
+    auto pass1 = [&](auto edge_tag) {
+      [[maybe_unused]] constexpr bool EDGE = decltype(edge_tag)::value;
 #pragma unroll
-    for (int j = 0; j < RC; ++j) {
-      ss[j] = 0.0f;
-      if (CHECK && row0 + j >= rend) continue;
-      [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
-      F2 acc[P];  // independent accumulators: no serial FMA chain
+      for (int j = 0; j < RC; ++j) {
+        ss[j] = 0.0f;
+        if (CHECK && row0 + j >= rend) continue;
+        [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
+        F2 acc[P];  // independent accumulators: no serial FMA chain
 #pragma unroll
-      for (int i = 0; i < P; ++i) acc[i] = f2(0.0f, 0.0f);
+        for (int i = 0; i < P; ++i) acc[i] = f2(0.0f, 0.0f);
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        if (!cval[k]) continue;
-        const uint32_t sl = stage + j * JS + k * KS;
-        F2 x[P];
-        if constexpr (kGate) {
-          F2 h[P], u[P], gf[P];
-          G::widen(lds16(sl + kX * OS), h);
-          G::widen(lds16(sl + kU * OS), u);
-          if constexpr (GFULL) G::widen(lds16(sl + kG * OS), gf);
+        for (int k = 0; k < VPT; ++k) {
+          if (!cval[k]) continue;
+          const uint32_t sl = stage + j * JS + k * KS;
+          F2 x[P];
+          if constexpr (kGate) {
+            F2 h[P], u[P], gf[P];
+            G::widen(lds16(sl + kX * OS), h);
+            G::widen(lds16(sl + kU * OS), u);
+            if constexpr (GFULL) G::widen(lds16(sl + kG * OS), gf);
 #pragma unroll
-          for (int i = 0; i < P; ++i) x[i] = residual_gate2<T>(h[i], u[i], GFULL ? gf[i] : gv[k][i]);
-          const Raw<16> r = G::narrow(x);
-          if (partial(k))
-            store_part<T>(out1 + rowoff + k * kstride, r, plo(k), phi(k));
-          else
-            st_stream<16>(out1 + rowoff + k * kstride, r);
-          if constexpr (kReduce) {
-            sts16(sl + kX * OS, r);  // the stored residual, read again in pass two
-            G::widen(r, x);
+            for (int i = 0; i < P; ++i) x[i] = residual_gate2<T>(h[i], u[i], GFULL ? gf[i] : gv[k][i]);
+            const Raw<16> r = G::narrow(x);
+            if (EDGE && partial(k))
+              store_part<T>(out1 + rowoff + k * kstride, r, plo(k), phi(k));
+            else
+              st_stream<16>(out1 + rowoff + k * kstride, r);
+            if constexpr (kReduce) {
+              sts16(sl + kX * OS, r);  // the stored residual, read again in pass two
+              G::widen(r, x);
+            }
+          } else {
+            G::widen(lds16(sl + kX * OS), x);
           }
-        } else {
-          G::widen(lds16(sl + kX * OS), x);
+          if constexpr (kReduce) {
+            if (EDGE && partial(k)) mask_part<T>(x, plo(k), phi(k));
+#pragma unroll
+            for (int i = 0; i < P; ++i) acc[i] = f2_fma(x[i], x[i], acc[i]);
+          }
         }
         if constexpr (kReduce) {
-          if (partial(k)) mask_part<T>(x, plo(k), phi(k));
 #pragma unroll
-          for (int i = 0; i < P; ++i) acc[i] = f2_fma(x[i], x[i], acc[i]);
+          for (int i = 1; i < P; ++i) acc[0] = f2_add(acc[0], acc[i]);
+          ss[j] = f2_lo(acc[0]) + f2_hi(acc[0]);
         }
       }
-      if constexpr (kReduce) {
-#pragma unroll
-        for (int i = 1; i < P; ++i) acc[0] = f2_add(acc[0], acc[i]);
-        ss[j] = f2_lo(acc[0]) + f2_hi(acc[0]);
-      }
+    };
+    if constexpr (!PH) {
+      pass1(std::false_type{});
+    } else if constexpr (kSplit) {
+      if (edge_warp)
+        pass1(std::true_type{});
+      else
+        pass1(std::false_type{});
+    } else {
+      pass1(std::true_type{});
     }
 
     if constexpr (kReduce) {
@@ -434,37 +461,42 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
       }
       const float rl = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
       buf ^= 1;
+      // pass two: normalise, modulate, store
+      auto pass2 = [&](auto edge_tag) {
+        [[maybe_unused]] constexpr bool EDGE = decltype(edge_tag)::value;
 #pragma unroll
-      for (int j = 0; j < RC; ++j) {
-        const float r = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
-        if (CHECK && row0 + j >= rend) continue;
-        [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
-        const F2 r2 = f2(r, r);
+        for (int j = 0; j < RC; ++j) {
+          const float r = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
+          if (CHECK && row0 + j >= rend) continue;
+          [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
+          const F2 r2 = f2(r, r);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          if (!cval[k]) continue;
-          const uint32_t sl = stage + j * JS + k * KS;
-          F2 x[P], y[P];
-          G::widen(lds16(sl + kX * OS), x);
-          if constexpr (MFULL) {
-            F2 sc[P], sh[P];
-            G::widen(lds16(sl + kSc * OS), sc);
-            G::widen(lds16(sl + kSh * OS), sh);
+          for (int k = 0; k < VPT; ++k) {
+            if (!cval[k]) continue;
+            const uint32_t sl = stage + j * JS + k * KS;
+            F2 x[P], y[P];
+            G::widen(lds16(sl + kX * OS), x);
+            if constexpr (MFULL) {
+              F2 sc[P], sh[P];
+              G::widen(lds16(sl + kSc * OS), sc);
+              G::widen(lds16(sl + kSh * OS), sh);
 #pragma unroll
-            for (int i = 0; i < P; ++i)
-              y[i] = modulate2(f2_mul(x[i], r2), f2_add(f2(1.0f, 1.0f), sc[i]), sh[i]);
-          } else {
+              for (int i = 0; i < P; ++i)
+                y[i] = modulate2(f2_mul(x[i], r2), f2_add(f2(1.0f, 1.0f), sc[i]), sh[i]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < P; ++i) y[i] = modulate2(f2_mul(x[i], r2), onev[k][i], shv[k][i]);
+              for (int i = 0; i < P; ++i) y[i] = modulate2(f2_mul(x[i], r2), onev[k][i], shv[k][i]);
+            }
+            if constexpr (Q8)
+              st_stream<2 * P>(out2 + (row0 + j) * qpitch + k * qkstride, quantise_e4m3<P>(y, qinv));
+            else if (EDGE && partial(k))
+              store_part<T>(out2 + rowoff + k * kstride, G::narrow(y), plo(k), phi(k));
+            else
+              st_stream<16>(out2 + rowoff + k * kstride, G::narrow(y));
           }
-          if constexpr (Q8)
-            st_stream<2 * P>(out2 + (row0 + j) * qpitch + k * qkstride, quantise_e4m3<P>(y, qinv));
-          else if (partial(k))
-            store_part<T>(out2 + rowoff + k * kstride, G::narrow(y), plo(k), phi(k));
-          else
-            st_stream<16>(out2 + rowoff + k * kstride, G::narrow(y));
         }
-      }
+      };
+      pass2(std::integral_constant<bool, PH>{});
     }
   };
 

@@ -3,8 +3,9 @@ multiple of 16 (odd D, D = 2 mod 4 ...) in tensors that start on 16-byte
 boundaries.  Every offset period (2, 4 and 8 rows), fewer rows than the
 period, more rows than the grid (each CTA takes rows of one offset), batches
 changing inside a CTA's run, rows shorter than a granule, the last row's
-granule that runs past the tensors' end, in-place residuals, strided adaLN
-tables, and canaries around every output (a row's first and last granule are
+granule that runs past the tensors' end, rows too long for one CTA (column
+slices of the residual gate; the two-pass kernel for the reducing ops),
+in-place residuals, strided adaLN tables, and canaries around every output (a row's first and last granule are
 shared with its neighbours and must be stored element by element).
 """
 import pytest
@@ -31,6 +32,10 @@ CASES = [
     (2, 9, 3, "fp32"),         # rows inside one granule
     (1, 40000, 13, "bf16"),    # 26-byte rows, many rows per CTA
     (2, 3001, 6, "fp16"),      # 12-byte rows, period 4, odd row count
+    (1, 50, 8193, "bf16"),     # residual gate in two column slices; the
+    (1, 30, 8191, "fp16"),     # reducing ops then take the two-pass kernel
+    (1, 12, 20001, "bf16"),    # (a row beyond one CTA's 1024 granules)
+    (1, 40, 8191, "fp32"),
 ]
 IDS = [f"{b}x{l}x{d}-{t}" for b, l, d, t in CASES]
 
