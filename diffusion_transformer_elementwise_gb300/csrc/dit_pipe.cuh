@@ -545,12 +545,31 @@ __global__ void DIT_PIPE_FUSED_BOUNDS pipe_fused_kernel(RowArgs a) {
   pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>(a, blockIdx.x, blockIdx.y);
 }
 
+// The fused op on phased rows: its own entry and register cap.  At 80 it
+// spilled; under 104 ptxas takes 94 (no spill; three 224-thread CTAs still
+// fit an SM), the fastest of the caps 80/88/96/104 on [1,4097,3077] 16-bit
+// (L2-flushed 38.9 -> 35.7 us; fp32 unchanged).
+#ifndef DIT_PIPE_FUSED_PH_MAXNREG
+#define DIT_PIPE_FUSED_PH_MAXNREG 104
+#endif
+#ifdef DIT_PIPE_MAXNREG
+#define DIT_PIPE_FUSED_PH_BOUNDS DIT_PIPE_BOUNDS
+#else
+#define DIT_PIPE_FUSED_PH_BOUNDS __maxnreg__(DIT_PIPE_FUSED_PH_MAXNREG)
+#endif
+template <class T, int VPT, int S, int RC, bool GFULL, bool MFULL>
+__global__ void DIT_PIPE_FUSED_PH_BOUNDS pipe_fused_phased_kernel(RowArgs a) {
+  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, false, false, true>(a, blockIdx.x, blockIdx.y);
+}
+
 // The kernel of one instantiation of the staged row path.
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8,
           bool PH>
 constexpr auto pipe_kernel_for() {
-  if constexpr (OP == OP_FUSED)
-    return pipe_fused_kernel<T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>;
+  if constexpr (OP == OP_FUSED && PH)
+    return pipe_fused_phased_kernel<T, VPT, S, RC, GFULL, MFULL>;
+  else if constexpr (OP == OP_FUSED)
+    return pipe_fused_kernel<T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, false>;
   else
     return pipe_kernel<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>;
 }
