@@ -36,6 +36,8 @@ CASES = [
     (1, 30, 8191, "fp16"),     # reducing ops then take the two-pass kernel
     (1, 12, 20001, "bf16"),    # (a row beyond one CTA's 1024 granules)
     (1, 40, 8191, "fp32"),
+    (2, 512, 3077, "bf16"),    # batches whose length is a multiple of the
+    (4, 64, 1001, "fp16"),     # period: every batch starts at offset 0
 ]
 IDS = [f"{b}x{l}x{d}-{t}" for b, l, d, t in CASES]
 
