@@ -40,7 +40,12 @@
  * Alignment.  Pointers must be aligned to the element size (2 bytes for
  *   bf16/fp16, 4 for fp32); otherwise DIT_ERR_MISALIGNED.  Any such pointer
  *   is accepted: the widest vector access that every pointer and the row
- *   pitch D * element_size allow is chosen per call (up to 32 bytes).
+ *   pitch D * element_size allow is chosen per call (up to 32 bytes).  Rows
+ *   whose pitch is not a multiple of 16 bytes, in tensors that start on
+ *   16-byte boundaries, are still moved in 16-byte granules (the row-wise
+ *   operations group the rows by their offset modulo 16 bytes); only
+ *   sub-views that start off a 16-byte boundary fall back to narrower
+ *   accesses.
  * Errors.  Argument errors are returned before any launch and leave outputs
  *   untouched.  B, L, D >= 0; a call with B * L * D == 0 returns DIT_OK and
  *   launches nothing.  A launch failure reported by the CUDA runtime returns
