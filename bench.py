@@ -131,14 +131,40 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _code_only(text):
+    """C/C++/CUDA source without its comments, trailing blanks and blank
+    lines (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash():
-    """Hash of the CUDA sources (ties a stored ncu traffic figure to them)."""
+    """Hash of the CUDA sources' code (ties a stored ncu traffic figure to
+    them; an edit of comments only keeps it)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "diffusion_transformer_elementwise_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -730,6 +756,12 @@ def run_shapes(args):
                for D in (3080, 3076, 3077) for dt in ("bf16", "fp16", "fp32")]
     shapes += [(f"flux2_bcast_s4608_c3072_{dt}", 1, 4608, 3072, "bcast", dt)
                for dt in ("fp16", "fp32")]
+    if args.shape:
+        wanted = set(args.shape.split(","))
+        unknown = wanted - {s[0] for s in shapes}
+        if unknown:
+            raise SystemExit(f"unknown --shape {sorted(unknown)}; known: {[s[0] for s in shapes]}")
+        shapes = [s for s in shapes if s[0] in wanted]
     for name, B, L, D, lay, dt in shapes:
         es = 4 if dt == "fp32" else 2
         N, vbytes = B * L * D, B * D * es
@@ -815,6 +847,8 @@ def main():
     p.add_argument("--separate", action="store_true",
                    help="--workload chain_av: one launch per stream and site instead of "
                         "one grouped launch per site")
+    p.add_argument("--shape", default=None,
+                   help="--workload shapes: only these shapes (comma-separated names)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--op", default=None,

@@ -235,7 +235,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   };
   // phased rows of the residual gate: the warps that own a row's first or
   // last granule take the masked code path, the others the aligned one (a
-  // warp-uniform branch; [1,4097,3077] bf16 L2-flushed 21.1 -> 19.6 us).  The
+  // warp-uniform branch; [1,4097,3077] bf16 L2-flushed 21.1 -> 19.2 us).  The
   // reducing operations test every granule instead: the two copies of their
   // larger passes cost them 9-16% on the same shapes.
   constexpr bool kSplit = PH && !kReduce;
@@ -546,9 +546,9 @@ __global__ void DIT_PIPE_FUSED_BOUNDS pipe_fused_kernel(RowArgs a) {
 }
 
 // The fused op on phased rows: its own entry and register cap.  At 80 it
-// spilled; under 104 ptxas takes 94 (no spill; three 224-thread CTAs still
-// fit an SM), the fastest of the caps 80/88/96/104 on [1,4097,3077] 16-bit
-// (L2-flushed 38.9 -> 35.7 us; fp32 unchanged).
+// spilled; under 104 ptxas takes 94 (no spill; two 224-thread CTAs per SM,
+// as ncu shows, against three at 80), the fastest of the caps 80/88/96/104 on
+// [1,4097,3077] 16-bit (L2-flushed 38.9 -> 35.7 us; fp32 unchanged).
 #ifndef DIT_PIPE_FUSED_PH_MAXNREG
 #define DIT_PIPE_FUSED_PH_MAXNREG 104
 #endif
