@@ -31,3 +31,24 @@ def test_reference_arm_line():
     import bench
     assert d["config"] == bench.hotpath_config()
     assert d["metric"] == bench.METRIC
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The stored ncu traffic is tied to the kernels' code: comments and blank
+    lines do not change the hash; code, including string literals, does."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = ('int a = 1; // the count\n'
+           '/* a block\n   comment */\n'
+           'asm("mov.b32 %0, %1; // not a comment");\n'
+           "char c = '/';\n")
+    same = ('int a = 1;\n\n'
+            'asm("mov.b32 %0, %1; // not a comment");   \n'
+            "char c = '/'; /* trailing */\n")
+    assert bench._code_only(src) == bench._code_only(same)
+    assert "// not a comment" in bench._code_only(src)
+    changed = src.replace("int a = 1", "int a = 2")
+    assert bench._code_only(changed) != bench._code_only(src)
+    changed_literal = src.replace("not a comment", "not a remark")
+    assert bench._code_only(changed_literal) != bench._code_only(src)
+    assert len(bench.kernel_source_hash()) == 16
