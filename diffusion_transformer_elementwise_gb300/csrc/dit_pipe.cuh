@@ -211,7 +211,10 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   const int64_t g0 = slice * nthr * VPT + tid;
   bool cval[VPT];
   // phased rows: granule k's slots [lo, hi) belong to the row, packed as
-  // byte k = lo | hi << 4 (one register for every k)
+  // byte k = lo | hi << 4 (one register for every k).  A granule past the row
+  // (cval false: never read) gets a meaningless byte; such granules are
+  // always the higher k, so what spills out of their byte lands above every
+  // valid one.
   [[maybe_unused]] uint32_t bounds = 0;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
