@@ -732,7 +732,10 @@ def run_shapes(args):
     """One line per (shape, op): device-timed us per call with an L2 flush
     before every call, outside the timed region.  The flush *reads* a buffer
     of 4x the L2 size: a write-flush would leave the L2 full of dirty lines
-    whose write-back then falls inside the next timed call."""
+    whose write-back then falls inside the next timed call.  Beside the
+    single-call median (whose resolution is the event timer's ~2 us step):
+    cold_us, 30 x (flush + call) minus 30 x flush; back-to-back and
+    CUDA-graph means of 20 calls."""
     import torch
 
     import diffusion_transformer_elementwise_gb300 as dit
@@ -818,6 +821,23 @@ def run_shapes(args):
             torch.cuda.synchronize()
             graph_us = s.elapsed_time(e) / 20 * 1e3
             del graph
+            # the cold call without the event timer's ~2 us step: 30 x (flush
+            # + call) minus 30 x flush, back to back (the call's write-back,
+            # which lands in the next flush, counts against the call)
+            def run_n(call, n=30):
+                s.record()
+                for _ in range(n):
+                    call()
+                e.record()
+                torch.cuda.synchronize()
+                return s.elapsed_time(e) / n
+            def flush_only():
+                torch.amax(flush, dim=0, out=sink)
+            def flush_then_call():
+                torch.amax(flush, dim=0, out=sink)
+                fn()
+            pairs = [(run_n(flush_only), run_n(flush_then_call)) for _ in range(3)]
+            cold_us = statistics.median(b - a for a, b in pairs) * 1e3
             med = statistics.median(times)
             gbs = nbytes / (med * 1e-3) / 1e9
             print(json.dumps({"shape": name, "op": op, "dtype": dt, "B": B, "L": L, "D": D,
@@ -825,7 +845,7 @@ def run_shapes(args):
                               "min_us": min(times) * 1e3, "GB_s": gbs,
                               "frac_of_peak": gbs / peak,
                               "back_to_back_us": b2b * 1e3,
-                              "graph_us": graph_us}), flush=True)
+                              "graph_us": graph_us, "cold_us": cold_us}), flush=True)
         del h, u, g, o, o2
     return 0
 
