@@ -736,18 +736,6 @@ def run_shapes(args):
     single-call median (whose resolution is the event timer's ~2 us step):
     cold_us, 30 x (flush + call) minus 30 x flush; back-to-back and
     CUDA-graph means of 20 calls."""
-    import torch
-
-    import diffusion_transformer_elementwise_gb300 as dit
-    from diffusion_transformer_elementwise_gb300.build import build
-    from diffusion_transformer_elementwise_gb300.synth import draw, seed_for
-    build()
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty((), dtype=torch.float32, device=dev)
-    peak, _ = hbm_peak()
     shapes = [("ltx2_full_s126_c2048", 1, 126, 2048, "full", "bf16"),
               ("flux2_bcast_s4608_c3072", 1, 4608, 3072, "bcast", "bf16"),
               ("ideogram4_bcast_s4096_c4608", 1, 4096, 4608, "bcast", "bf16"),
@@ -765,6 +753,18 @@ def run_shapes(args):
         if unknown:
             raise SystemExit(f"unknown --shape {sorted(unknown)}; known: {[s[0] for s in shapes]}")
         shapes = [s for s in shapes if s[0] in wanted]
+    import torch
+
+    import diffusion_transformer_elementwise_gb300 as dit
+    from diffusion_transformer_elementwise_gb300.build import build
+    from diffusion_transformer_elementwise_gb300.synth import draw, seed_for
+    build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    peak, _ = hbm_peak()
     for name, B, L, D, lay, dt in shapes:
         es = 4 if dt == "fp32" else 2
         N, vbytes = B * L * D, B * D * es

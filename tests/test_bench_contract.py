@@ -52,3 +52,12 @@ def test_kernel_source_hash_ignores_comments_only():
     changed_literal = src.replace("not a comment", "not a remark")
     assert bench._code_only(changed_literal) != bench._code_only(src)
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_shapes_filter_rejects_unknown_names_before_any_gpu_work():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "shapes",
+                        "--shape", "no_such_shape"], capture_output=True, text=True,
+                       timeout=300, cwd=ROOT)
+    assert r.returncode != 0
+    assert "unknown --shape ['no_such_shape']" in r.stderr
+    assert "tail_s4097_c3077_bf16" in r.stderr
