@@ -96,6 +96,10 @@ def _bind(path):
     lib.orc_store_double.restype = None
     lib.orc_row_rms_inverse.argtypes = [vp, i64, fp, ci]
     lib.orc_row_rms_inverse.restype = fp
+    lib.orc_row_mean_square.argtypes = [vp, i64, ci]
+    lib.orc_row_mean_square.restype = fp
+    lib.orc_inverse_root_array.argtypes = [vp, vp, i64]
+    lib.orc_inverse_root_array.restype = None
     lib.orc_residual_gate_add_mt.argtypes = [ci, vp, vp, vp, vp, i64, i64,
                                              i64, ci, ci, vp, i64]
     lib.orc_residual_gate_add_mt.restype = ci
@@ -283,6 +287,21 @@ def row_rms_inverse(x_row, D, eps=1e-6, dtype="bf16") -> float:
     return _load().orc_row_rms_inverse(_ptr(x_row), D, float(eps), DTYPES[dtype])
 
 
+def row_mean_square(x_row, D, dtype="bf16") -> float:
+    """ms = RN32(mean(x^2)) of one row: the exact mean rounded once to fp32."""
+    return _load().orc_row_mean_square(_ptr(x_row), D, DTYPES[dtype])
+
+
+def inverse_root(v):
+    """RN32(1 / sqrt(v)) of fp32 values (numpy float32 result), the
+    statistic's inverse-root step."""
+    import numpy as np
+    src = np.ascontiguousarray(np.asarray(v, dtype=np.float32)).ravel()
+    dst = np.empty_like(src)
+    _load().orc_inverse_root_array(_ptr(src), _ptr(dst), src.size)
+    return dst
+
+
 def variant(lib_path: str):
     """A namespace with this module's functions bound to another build of the
     oracle source (used by the tests that plant mistakes in a copy of it)."""
@@ -292,7 +311,8 @@ def variant(lib_path: str):
     src = sys.modules[__name__]
     lib = _bind(lib_path)
     for name in ("decode", "encode", "residual_gate_add", "rmsnorm_modulate",
-                 "gate_add_rmsnorm_modulate", "row_rms_inverse", "gelu_tanh", "round_double",
+                 "gate_add_rmsnorm_modulate", "row_rms_inverse", "row_mean_square",
+                 "inverse_root", "gelu_tanh", "round_double",
                  "e4m3_decode", "e4m3_encode", "rmsnorm_modulate_fp8",
                  "gate_add_rmsnorm_modulate_fp8"):
         fn = getattr(src, name)

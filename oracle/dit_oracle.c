@@ -11,11 +11,14 @@
  * justification in the repository's design notes):
  *   R1  residual gate: p = fl(update * gate), s = fl(hidden + p), then one
  *       rounding of s to the storage dtype.  No FMA.
- *   R2  RMS statistic: sum of x^2 accumulated in double in index order,
- *       ms = (float)(sum / D), v = fl(ms + eps), r = (float)(1 / sqrt(v))
- *       evaluated in double -- i.e. the correctly rounded fp32 value of the
- *       inverse root of the fp32 v.  eps sits inside the root, added to the
- *       mean square (the standard weightless RMSNorm).
+ *   R2  RMS statistic ("fp32 statistics", and the pages' bound of one
+ *       bf16 ulp per output element): ms = RN32(sum x^2 / D), the exact mean
+ *       of the squares rounded once to fp32 (the sum taken exactly, as a
+ *       big integer); v = fl(ms + eps); r = RN32(1 / sqrt(v)), the correctly
+ *       rounded fp32 inverse root of the fp32 v.  Both are single roundings
+ *       of exact values, so they do not depend on a summation order.  eps
+ *       sits inside the root, added to the mean square (the standard
+ *       weightless RMSNorm).
  *   R3  modulation order, left to right as the expression is written:
  *       n = fl(x * r); one = fl(1 + scale); t = fl(n * one); y = fl(t + shift);
  *       then one rounding of y to the storage dtype.  1 + scale is formed in
@@ -222,16 +225,125 @@ static void residual_gate_row(void* out, const void* hidden, const void* update,
   }
 }
 
+/* ------------------------------------------------------------------------ */
+/* the row statistic (reading R2)                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Every fp32 value is M * 2^e with M an integer below 2^24 and e >= -149, so
+ * its square M^2 * 2^(2e) is an integer multiple of 2^-298 below 2^256.  A
+ * row's sum of squares times 2^298 is therefore an integer below 2^585 for
+ * rows of fewer than 2^31 elements: SQ_DIGITS base-2^32 digits hold it
+ * exactly. */
+#define SQ_SCALE 298
+#define SQ_DIGITS 19
+
+/* The exact sum of squares of a row (times 2^SQ_SCALE) as base-2^32 digits,
+ * least significant first.  Each square is added as 32-bit parts into 64-bit
+ * per-digit accumulators; the carries are propagated once at the end. */
+static void exact_sum_of_squares(const void* x_row, int64_t D, int dtype,
+                                 uint32_t digit[SQ_DIGITS]) {
+  uint64_t acc[SQ_DIGITS];
+  memset(acc, 0, sizeof acc);
+  for (int64_t d = 0; d < D; ++d) {
+    const float v = fabsf(orc_load(x_row, d, dtype));
+    if (v == 0.0f) continue;
+    int e2;
+    (void)frexpf(v, &e2);            /* v in [2^(e2-1), 2^e2) */
+    int e = e2 - 24;                 /* v = M * 2^e with M < 2^24 ... */
+    if (e < -149) e = -149;          /* ... or, below 2^-126, M * 2^-149 */
+    const uint64_t M = (uint64_t)ldexpf(v, -e); /* exact: an integer */
+    const uint64_t sq = M * M;       /* < 2^48 */
+    const int pos = 2 * e + SQ_SCALE; /* bit of the scaled sum where sq starts */
+    const int k = pos / 32, s = pos % 32;
+    const uint64_t t0 = (sq & 0xFFFFFFFFu) << s; /* < 2^63 */
+    const uint64_t t1 = (sq >> 32) << s;          /* < 2^47, weight 2^32 more */
+    acc[k] += t0 & 0xFFFFFFFFu;
+    acc[k + 1] += (t0 >> 32) + (t1 & 0xFFFFFFFFu);
+    acc[k + 2] += t1 >> 32;
+  }
+  uint64_t carry = 0;
+  for (int i = 0; i < SQ_DIGITS; ++i) {
+    const uint64_t t = acc[i] + carry;
+    digit[i] = (uint32_t)t;
+    carry = t >> 32;
+  }
+}
+
+/* bit b of a little-endian base-2^32 number of n digits (0 outside it) */
+static int bit_at(const uint32_t* q, int n, int b) {
+  if (b < 0 || b >= 32 * n) return 0;
+  return (int)((q[b / 32] >> (b % 32)) & 1u);
+}
+
+/* The fp32 value nearest (ties to even) to (digits * 2^-SQ_SCALE) / D.  The
+ * digits, with 64 zero bits appended below them, are divided by D by long
+ * division; the quotient then has at least 33 bits for any nonzero sum, and
+ * the remainder says whether anything lies below it.  The result keeps 24
+ * bits from the quotient's leading one, or the bits down to 2^-149 when it is
+ * below 2^-126 (subnormal); the bit after the kept ones and the "sticky" OR
+ * of everything below decide the rounding. */
+static float rn32_mean(const uint32_t digit[SQ_DIGITS], uint32_t D) {
+  enum { N = SQ_DIGITS + 2 };
+  uint32_t num[N], q[N];
+  num[0] = num[1] = 0;
+  for (int i = 0; i < SQ_DIGITS; ++i) num[i + 2] = digit[i];
+  uint64_t rem = 0;
+  for (int i = N - 1; i >= 0; --i) {
+    const uint64_t cur = (rem << 32) | num[i];
+    q[i] = (uint32_t)(cur / D);
+    rem = cur % D;
+  }
+  const int w0 = SQ_SCALE + 64; /* bit b of q weighs 2^(b - w0) */
+  int top = -1;
+  for (int b = 32 * N - 1; b >= 0; --b)
+    if (bit_at(q, N, b)) {
+      top = b;
+      break;
+    }
+  if (top < 0) return 0.0f; /* every element was zero */
+  int lsb = top - 23;
+  if (lsb - w0 < -149) lsb = w0 - 149;
+  uint64_t mant = 0;
+  for (int b = top; b >= lsb; --b) mant = 2 * mant + (uint64_t)bit_at(q, N, b);
+  const int guard = bit_at(q, N, lsb - 1);
+  int sticky = rem != 0;
+  for (int b = lsb - 2; b >= 0 && !sticky; --b) sticky = bit_at(q, N, b);
+  if (guard && (sticky || (mant & 1u))) mant += 1;
+  return (float)ldexp((double)mant, lsb - w0); /* exact, or +inf past FLT_MAX */
+}
+
+/* ms = RN32(mean(x^2)) of one row (reading R2): NaN if the row holds a NaN,
+ * +inf if it holds an infinity, else the exact mean of the squares rounded
+ * once to fp32 (+inf when that passes FLT_MAX). */
+float orc_row_mean_square(const void* x_row, int64_t D, int dtype) {
+  if (D <= 0 || D > 0x7FFFFFFF) return NAN;
+  int inf = 0;
+  for (int64_t d = 0; d < D; ++d) {
+    const float v = orc_load(x_row, d, dtype);
+    if (isnan(v)) return NAN;
+    if (isinf(v)) inf = 1;
+  }
+  if (inf) return INFINITY;
+  uint32_t digit[SQ_DIGITS];
+  exact_sum_of_squares(x_row, D, dtype, digit);
+  return rn32_mean(digit, (uint32_t)D);
+}
+
+/* RN32(1 / sqrt(v)): the root and the quotient in double, then one rounding
+ * to fp32.  That is the correctly rounded fp32 value for every fp32 v (an
+ * exhaustive check over one binade pair, [1, 4), covers all others, since
+ * v * 4^k only scales the result by 2^-k). */
+static float inverse_root(float v) { return (float)(1.0 / sqrt((double)v)); }
+
+void orc_inverse_root_array(const float* v, float* r, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) r[i] = inverse_root(v[i]);
+}
+
 /* r = 1 / sqrt(mean(x^2) + eps) for one row (reading R2). */
 float orc_row_rms_inverse(const void* x_row, int64_t D, float eps, int dtype) {
-  double sum = 0.0;
-  for (int64_t d = 0; d < D; ++d) {
-    double v = (double)orc_load(x_row, d, dtype);
-    sum += v * v;
-  }
-  float ms = (float)(sum / (double)D);
+  float ms = orc_row_mean_square(x_row, D, dtype);
   float v = ms + eps;
-  return (float)(1.0 / sqrt((double)v));
+  return inverse_root(v);
 }
 
 /* Row r of  out = rms_norm(x, eps) * (1 + scale) + shift  (reading R3). */
@@ -415,6 +527,7 @@ static int modulate_impl(int nthreads, void* out, float* t_out, const void* x,
                          int mod_layout, const int64_t* rows, int64_t nrows,
                          int fp8, float qinv) {
   if (bad_common(B, L, D, dtype, rows, nrows) || bad_layout(mod_layout)) return -1;
+  if (D > 0x7FFFFFFF) return -1; /* the statistic's divisor is 32-bit */
   if (B * L * D > 0 && (!out || !x || !scale || !shift)) return -1;
   orc_job j = {0};
   j.op = 1;
@@ -459,7 +572,7 @@ static int fused_impl(int nthreads, void* residual_out, void* modulated_out,
                       int gate_layout, int mod_layout, const int64_t* rows,
                       int64_t nrows, int fp8, float qinv) {
   if (bad_common(B, L, D, dtype, rows, nrows) || bad_layout(gate_layout) ||
-      bad_layout(mod_layout))
+      bad_layout(mod_layout) || D > 0x7FFFFFFF)
     return -1;
   if (B * L * D > 0 && (!residual_out || !modulated_out || !hidden || !update ||
                         !gate || !scale || !shift))

@@ -117,9 +117,14 @@ int orc_gate_add_rmsnorm_modulate_fp8(void* residual_out, uint8_t* out,
                                       float quant_scale, const int64_t* rows,
                                       int64_t nrows);
 
-/* The per-row statistic, exposed for the tests: r = 1/sqrt(mean(x^2) + eps)
- * for one row of D elements. */
+/* The per-row statistic, exposed for the tests: ms = RN32(mean(x^2)), the
+ * exact mean of the squares of one row of D elements (0 < D < 2^31) rounded
+ * once to fp32 (NaN if the row holds a NaN, +inf if it holds an infinity);
+ * r = RN32(1/sqrt(fl(ms + eps))); and the inverse-root step alone, r[i] =
+ * RN32(1/sqrt(v[i])) for n fp32 values. */
+float orc_row_mean_square(const void* x_row, int64_t D, int dtype);
 float orc_row_rms_inverse(const void* x_row, int64_t D, float eps, int dtype);
+void  orc_inverse_root_array(const float* v, float* r, int64_t n);
 
 /* Multi-threaded drivers for the CPU baseline: the same functions, with the
  * selected rows split into `nthreads` contiguous parts, one POSIX thread each.

@@ -5,7 +5,9 @@ least one pin from the oracle test files fails on it.
 Mistakes planted: a wrong sign, a dropped term, a transposed or wrong
 operand, a wrong row index for a broadcast operand, eps outside the root or
 dropped, a wrong divisor in the mean, a fused multiply-add, wrong rounding of
-the storage dtype, the fused op reading the unrounded residual, and in the
+the storage dtype, the fused op reading the unrounded residual; in the row
+statistic a double-precision sum, truncation, ties away from zero, squares
+cut to fp32 precision and a doubly rounded inverse root; and in the
 GELU a wrong coefficient, power, sign or scale, and double rounding; in the
 FP8 output the scale applied the wrong way, no saturation, ties away from
 zero and a wrong subnormal spacing.
@@ -23,6 +25,7 @@ import test_oracle_fused as pf
 import test_oracle_gelu as pg
 import test_oracle_modulate as pm
 import test_oracle_residual_gate as pr
+import test_oracle_statistic as ps
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "dit_oracle.c")
 
@@ -40,10 +43,26 @@ MUTANTS = {
                              "float sc = orc_load(shift, mrow * D + d, dtype);\n"
                              "    float sh = orc_load(scale, mrow * D + d, dtype);"),
     "mod_drop_eps": ("float v = ms + eps;", "float v = ms; (void)eps;"),
-    "mod_eps_outside": ("return (float)(1.0 / sqrt((double)v));",
-                        "return (float)(1.0 / (sqrt((double)ms) + (double)eps)); (void)v;"),
-    "mod_mean_divisor": ("float ms = (float)(sum / (double)D);",
-                         "float ms = (float)(sum / (double)(D + 1));"),
+    "mod_eps_outside": ("  float v = ms + eps;\n  return inverse_root(v);",
+                        "  return (float)(1.0 / (sqrt((double)ms) + (double)eps));"),
+    "mod_mean_divisor": ("return rn32_mean(digit, (uint32_t)D);",
+                         "return rn32_mean(digit, (uint32_t)D + 1);"),
+    # the statistic: a double-precision sum (the earlier reading), no
+    # rounding, ties away from zero, squares cut to fp32 precision, and the
+    # inverse root rounded twice (fp32 root, then fp32 quotient)
+    "stat_double_sum": ("  exact_sum_of_squares(x_row, D, dtype, digit);\n"
+                        "  return rn32_mean(digit, (uint32_t)D);",
+                        "  double s = 0.0; (void)digit;\n"
+                        "  for (int64_t d = 0; d < D; ++d) { double v = orc_load(x_row, d, dtype); s += v * v; }\n"
+                        "  return (float)(s / (double)D);"),
+    "stat_truncate": ("if (guard && (sticky || (mant & 1u))) mant += 1;",
+                      "(void)guard; (void)sticky;"),
+    "stat_ties_away": ("if (guard && (sticky || (mant & 1u))) mant += 1;",
+                       "if (guard) mant += 1; (void)sticky;"),
+    "stat_fp32_squares": ("const uint64_t sq = M * M;",
+                          "const uint64_t sq = (M * M) >> 24 << 24;"),
+    "stat_root_in_fp32": ("static float inverse_root(float v) { return (float)(1.0 / sqrt((double)v)); }",
+                          "static float inverse_root(float v) { return 1.0f / sqrtf(v); }"),
     "mod_bcast_row": ("int64_t mrow = (mod_layout == ORC_FULL) ? r : r / L;",
                       "int64_t mrow = (mod_layout == ORC_FULL) ? r : 0;"),
     "bf16_round_half_up": ("x += 0x7FFFu + lsb;", "x += 0x8000u; (void)lsb;"),
@@ -106,6 +125,10 @@ PINS = [
     lambda o: p8.test_ties_golden(o),
     lambda o: p8.test_encode_against_torch(o),
     lambda o: p8.test_modulate_fp8_is_quantised_fp32_modulation(o, "bf16", 0.005),
+    lambda o: [ps.test_mean_square_golden(o, c) for c in ps.parse_golden()],
+    lambda o: ps.test_mean_square_matches_exact_rationals(o, "bf16", 7),
+    lambda o: ps.test_mean_square_matches_exact_rationals(o, "fp32", 3),
+    lambda o: ps.test_inverse_root_across_the_range(o),
 ]
 
 
