@@ -142,6 +142,10 @@ bool valid_vector_stride(int64_t B, int64_t D, int64_t vs, int es) {
   return !__builtin_mul_overflow(B - 1, vs, &t) && !__builtin_mul_overflow(t + D, (int64_t)es, &t);
 }
 
+// The longest row the modulating operations take: D is exact in fp32 and the
+// exact path's 64-bit digit totals cannot overflow.
+constexpr int64_t kMaxStatisticRow = int64_t(1) << 24;
+
 // A validated call of one operation: its kernel arguments, its access width
 // and the byte spans it writes and reads (for the aliasing checks of grouped
 // calls).
@@ -218,6 +222,7 @@ dit_status prepare_modulate(void* out, const void* x, const void* scale, const v
   if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
   const bool full = mod_layout == DIT_FULL;
   if (!full && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
+  if (D > kMaxStatisticRow) return DIT_ERR_BAD_SHAPE;
   if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
   *p = Prepared{};
   p->op = dit::OP_MOD;
@@ -247,7 +252,6 @@ dit_status prepare_modulate(void* out, const void* x, const void* scale, const v
   a.vstride = (B > 1 && !full ? vs : D) * es;
   a.eps = eps;
   a.d_f = (float)D;
-  a.inv_d = 1.0f / (float)D;
   const uint64_t bits = (uintptr_t)out | (uintptr_t)x | (uintptr_t)scale | (uintptr_t)shift |
                         (uint64_t)(D * es) | (uint64_t)a.vstride;
   p->vb = dit::widest_access(bits);
@@ -272,6 +276,7 @@ dit_status prepare_fused(void* residual_out, void* modulated_out, const void* hi
   if (!element_count(B, L, D, es, &n)) return DIT_ERR_BAD_SHAPE;
   const bool any_bcast = gate_layout == DIT_ROW_BCAST || mod_layout == DIT_ROW_BCAST;
   if (any_bcast && !valid_vector_stride(B, D, vs, es)) return DIT_ERR_BAD_SHAPE;
+  if (D > kMaxStatisticRow) return DIT_ERR_BAD_SHAPE;
   if (!(eps >= 0.0f) || isinf(eps)) return DIT_ERR_BAD_EPS;
   *p = Prepared{};
   p->op = dit::OP_FUSED;
@@ -316,7 +321,6 @@ dit_status prepare_fused(void* residual_out, void* modulated_out, const void* hi
   a.vstride = (B > 1 && any_bcast ? vs : D) * es;
   a.eps = eps;
   a.d_f = (float)D;
-  a.inv_d = 1.0f / (float)D;
   const uint64_t bits = (uintptr_t)residual_out | (uintptr_t)modulated_out | (uintptr_t)hidden |
                         (uintptr_t)update | (uintptr_t)gate | (uintptr_t)scale |
                         (uintptr_t)shift | (uint64_t)(D * es) | (uint64_t)a.vstride;
@@ -680,7 +684,6 @@ dit_status dit_rmsnorm_modulate_fp8(void* out, const void* x, const void* scale,
   a.vstride = vs * es;
   a.eps = eps;
   a.d_f = (float)D;
-  a.inv_d = 1.0f / (float)D;
   a.qscale = quant_scale;
   const cudaError_t e = dit::launch_modulate_fp8(dev, dtype, full, a, B, (cudaStream_t)stream);
   return e == cudaErrorNotSupported ? DIT_ERR_BAD_SHAPE : launch_status(e);
@@ -740,7 +743,6 @@ dit_status dit_gate_add_rmsnorm_modulate_fp8(
   a.vstride = vs * es;
   a.eps = eps;
   a.d_f = (float)D;
-  a.inv_d = 1.0f / (float)D;
   a.qscale = quant_scale;
   const cudaError_t e = dit::launch_fused_fp8(dev, dtype, gate_layout == DIT_FULL,
                                               mod_layout == DIT_FULL, a, B, (cudaStream_t)stream);

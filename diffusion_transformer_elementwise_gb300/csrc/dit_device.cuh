@@ -245,26 +245,6 @@ __device__ __forceinline__ float modulate(float x, float r, float s, float h) {
   return __fadd_rn(__fmul_rn(n, one), h);
 }
 
-// 1 / sqrt(mean + eps) from the row's fp32 sum of squares S over D elements,
-// in fp32 throughout:
-// * mean: q = S * fl(1/D), then one correction with the exact residual
-//   e = S - q*D (an FMA), q + e * fl(1/D) -- Markstein's division refinement,
-//   which yields the correctly rounded S/D except in rare near-halfway cases
-//   (and exactly S/D whenever D is a power of two);
-// * inverse root: the hardware estimate y0 = rsqrtf(v), then one
-//   Newton-Raphson step y1 = y0 + y0/2 * (1 - v*y0^2), accurate to about an
-//   ulp.
-// The oracle takes the correctly rounded values; the difference is a few fp32
-// ulps of r, the same order as the one the summation order already makes.
-__device__ __forceinline__ float rms_inverse(float sumsq, float D, float inv_d, float eps) {
-  const float q = sumsq * inv_d;
-  const float ms = fmaf(fmaf(-q, D, sumsq), inv_d, q);
-  const float v = __fadd_rn(ms, eps);
-  const float y0 = rsqrtf(v);
-  const float e = fmaf(-v * y0, y0, 1.0f);
-  return fmaf(0.5f * y0, e, y0);
-}
-
 // ---------------------------------------------------------------------------
 // packed fp32 pairs (sm_100+ f32x2 arithmetic: two IEEE fp32 operations, each
 // rounded to nearest-even, per instruction)
@@ -376,12 +356,6 @@ __device__ __forceinline__ F2 residual_gate2(F2 h, F2 u, F2 g) {
 __device__ __forceinline__ F2 modulate2(F2 n, F2 one, F2 shift) {
   const F2 t = f2_mul(n, one);
   return f2(__fadd_rn(f2_lo(t), f2_lo(shift)), __fadd_rn(f2_hi(t), f2_hi(shift)));
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
 }
 
 }  // namespace dit

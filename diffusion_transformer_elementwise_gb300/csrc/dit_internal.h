@@ -46,8 +46,7 @@ struct RowArgs {
   int64_t vstride;    // bytes between batches of a [B, 1, D] operand (D * s when contiguous)
   int64_t nvec;       // vectors of the kernel's width per row
   float eps;
-  float d_f;          // D as fp32
-  float inv_d;        // fl(1 / D)
+  float d_f;          // D as fp32 (exact: D <= 2^24)
   // grid-stride schedule of the row kernels: groups of rows, never
   // straddling a batch; CTA c takes groups c, c + G, c + 2G, ...
   int64_t gpb;        // groups per batch

@@ -30,6 +30,7 @@
 
 #include "dit_device.cuh"
 #include "dit_internal.h"
+#include "dit_stat.cuh"
 
 namespace dit {
 
@@ -74,36 +75,6 @@ __device__ __forceinline__ char* gp_out(void* p, int64_t g0) { return (char*)p +
 template <int OP, bool GFULL, bool MFULL>
 __host__ __device__ constexpr int streamed_operands() {
   return OP == OP_MOD ? (MFULL ? 3 : 1) : OP == OP_RGA ? 2 : (2 + (GFULL ? 1 : 0) + (MFULL ? 2 : 0));
-}
-
-// Sum each of RC per-lane values over the warp.  The rows are spread over
-// lane groups by exchanging halves (xor 16, then xor 8 for RC = 4) and each
-// group finishes with a butterfly, so RC rows cost about as many shuffles as
-// one.  Returns the sum of row (lane >> (5 - log2 RC)) in every lane.
-template <int RC>
-__device__ __forceinline__ float warp_sum_rows(const float (&v)[RC]) {
-  const int lane = threadIdx.x & 31;
-  float z;
-  if constexpr (RC == 1) {
-    z = v[0];
-  } else if constexpr (RC == 2) {
-    const bool hi = lane & 16;
-    const float send = hi ? v[0] : v[1];
-    const float keep = hi ? v[1] : v[0];
-    z = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
-  } else {
-    static_assert(RC == 4, "rows per group: 1, 2 or 4");
-    const bool b4 = lane & 16, b3 = lane & 8;
-    const float s0 = b4 ? v[0] : v[2], s1 = b4 ? v[1] : v[3];
-    const float k0 = b4 ? v[2] : v[0], k1 = b4 ? v[3] : v[1];
-    const float w0 = k0 + __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
-    const float w1 = k1 + __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
-    z = (b3 ? w1 : w0) + __shfl_xor_sync(0xFFFFFFFFu, b3 ? w0 : w1, 8);
-  }
-  constexpr int first = RC == 1 ? 16 : RC == 2 ? 8 : 4;
-#pragma unroll
-  for (int o = first; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-  return z;
 }
 
 // ALLCOLS: every thread owns VPT valid granules (T * VPT * slices == nvec),
@@ -377,28 +348,36 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   int64_t vec_b = cb;  // batch whose vectors are in registers
   load_vectors(cb);
 
-  __shared__ __align__(16) float part[2][RC][16];  // per-warp row partials (<= 16 warps)
-  // entries of warps this CTA does not have stay zero (read by the tree sum)
+  // per-warp row partials (<= 16 warps); the entries of warps this CTA does
+  // not have stay zero (merging a zero pair is exact)
+  __shared__ __align__(16) SumPair part[2][RC][16];
+  __shared__ uint64_t exact_scratch[16];  // the exact path's warp totals
   for (int i = tid; i < 2 * RC * 16; i += nthr)
-    if ((i & 15) >= nwarps) (&part[0][0][0])[i] = 0.0f;
+    if ((i & 15) >= nwarps) (&part[0][0][0])[i] = SumPair{0.0f, 0.0f};
+  // the statistic's accumulators: two packed slots per thread and row
+  constexpr int kNA = 2;
+  using Acc = SqAcc<T, kNA>;
+  // terms per scalar accumulator: 16-bit P / kNA per granule, fp32 one
+  constexpr int kTerms = (sizeof(T) == 2 ? P / kNA : 1) * VPT;
+  const float coef = Acc::coef(kTerms);
+  constexpr int kLevels = Log2<Acc::kScalar>::value + 5 + 4;  // thread, warp, 16 warps
   int buf = 0;
   uint32_t stage = base;
 
   // one group of RC rows starting at row0; CHECK: rows at or past rend are skipped
   auto group = [&](int64_t row0, int64_t rend, auto check_tag) {
     constexpr bool CHECK = decltype(check_tag)::value;
-    float ss[RC];
+    SumPair ss[RC];
     // pass one: the residual (stored), the row sums of squares
     auto pass1 = [&](auto edge_tag) {
       [[maybe_unused]] constexpr bool EDGE = decltype(edge_tag)::value;
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
-        ss[j] = 0.0f;
+        ss[j] = SumPair{0.0f, 0.0f};
         if (CHECK && row0 + j >= rend) continue;
         [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
-        F2 acc[P];  // independent accumulators: no serial FMA chain
-#pragma unroll
-        for (int i = 0; i < P; ++i) acc[i] = f2(0.0f, 0.0f);
+        Acc acc;
+        acc.zero();
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           if (!cval[k]) continue;
@@ -426,14 +405,10 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
           if constexpr (kReduce) {
             if (EDGE && partial(k)) mask_part<T>(x, plo(k), phi(k));
 #pragma unroll
-            for (int i = 0; i < P; ++i) acc[i] = f2_fma(x[i], x[i], acc[i]);
+            for (int i = 0; i < P; ++i) acc.add_pair(i % kNA, x[i]);
           }
         }
-        if constexpr (kReduce) {
-#pragma unroll
-          for (int i = 1; i < P; ++i) acc[0] = f2_add(acc[0], acc[i]);
-          ss[j] = f2_lo(acc[0]) + f2_hi(acc[0]);
-        }
+        if constexpr (kReduce) ss[j] = acc.total();
       }
     };
     if constexpr (!PH) {
@@ -448,28 +423,46 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
     }
 
     if constexpr (kReduce) {
-      // row sums: warp (rows spread over lane groups), then across warps
-      const float w = warp_sum_rows<RC>(ss);
-      constexpr int grp_lanes = 32 / RC;
-      if ((lane & (grp_lanes - 1)) == 0) part[buf][lane / grp_lanes][warp] = w;
-      __syncthreads();
-      // lane l finishes row l % RC (lane-parallel), then broadcasts
-      const int jr = lane % RC;
-      const float4* pp = reinterpret_cast<const float4*>(&part[buf][jr][0]);
-      const float4 p0 = pp[0], p1 = pp[1];
-      float tot = ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w));
-      if (nwarps > 8) {  // uniform
-        const float4 p2 = pp[2], p3 = pp[3];
-        tot += ((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w));
+      // row pairs: merged over the warp, then over the warps (lane l of
+      // every warp takes warp l % 16's pair, a 16-lane butterfly merges them)
+#pragma unroll
+      for (int j = 0; j < RC; ++j) {
+        const SumPair w = warp_merge(ss[j]);
+        if (lane == 0) part[buf][j][warp] = w;
       }
-      const float rl = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
+      __syncthreads();
+      float rr[RC];
+#pragma unroll
+      for (int j = 0; j < RC; ++j) {
+        const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
+        // the exact path reads the row back from this thread's ring slots
+        const uint32_t sl0 = stage + j * JS + kX * OS;
+        auto each = [=](auto&& f) {
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            if (!cval[k]) continue;
+            F2 x[P];
+            G::widen(lds16(sl0 + k * KS), x);
+            if constexpr (PH) {
+              const uint32_t bk = (bounds >> (8 * k)) & 255u;
+              if (bk != (uint32_t)EPG << 4) mask_part<T>(x, (int)(bk & 15u), (int)(bk >> 4));
+            }
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+              f(f2_lo(x[i]));
+              f(f2_hi(x[i]));
+            }
+          }
+        };
+        rr[j] = row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each, CtaRow{exact_scratch});
+      }
       buf ^= 1;
       // pass two: normalise, modulate, store
       auto pass2 = [&](auto edge_tag) {
         [[maybe_unused]] constexpr bool EDGE = decltype(edge_tag)::value;
 #pragma unroll
         for (int j = 0; j < RC; ++j) {
-          const float r = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
+          const float r = rr[j];
           if (CHECK && row0 + j >= rend) continue;
           [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
           const F2 r2 = f2(r, r);

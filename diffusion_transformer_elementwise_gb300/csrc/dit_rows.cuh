@@ -93,11 +93,19 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
     }
   };
 
-  __shared__ float part[2][R][32];
+  __shared__ SumPair part[2][R][16];       // per-warp row pairs (<= 16 warps)
+  __shared__ uint64_t exact_scratch[16];   // the exact path's warp totals
+  for (int i = tid; i < 2 * R * 16; i += nthr)
+    if ((i & 15) >= (nthr >> 5)) (&part[0][0][0])[i] = SumPair{0.0f, 0.0f};
+  // the statistic: four scalar (hi, lo) accumulators per thread and row,
+  // element e of the thread's row part into accumulator e % 4
+  using Acc = Sq32<4>;
+  constexpr int kTerms = (VPT * N + 3) / 4;
+  const float coef = Acc::coef(kTerms);
+  constexpr int kLevels = 2 + 5 + 4;  // thread, warp, 16 warps
   int buf = 0;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int nwarps = nthr >> 5;
 
   // grid-stride over groups of R rows (never straddling a batch): CTA c takes
   // groups c, c + G, c + 2G, ...
@@ -137,10 +145,11 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
       }
     }
 
-    float ss[R];
+    SumPair ss[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      ss[j] = 0.0f;
+      Acc acc;
+      acc.zero();
       const int64_t rowoff = (r0 + j) * pitch;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -159,24 +168,35 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
         if constexpr (kReduce) {
           V::widen(xv[j][k], f);
 #pragma unroll
-          for (int e = 0; e < N; ++e) ss[j] = fmaf(f[e], f[e], ss[j]);
+          for (int e = 0; e < N; ++e) acc.add((k * N + e) % 4, f[e]);
         }
       }
+      ss[j] = acc.total();
     }
     if constexpr (kReduce) {
-      // sum over the row
+      // row pairs over the warp, then over the warps
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        const float w = warp_sum(ss[j]);
+        const SumPair w = warp_merge(ss[j]);
         if (lane == 0) part[buf][j][warp] = w;
       }
       __syncthreads();
       float rinv[R];
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        float tot = 0.0f;
-        for (int w = 0; w < nwarps; ++w) tot += part[buf][j][w];
-        rinv[j] = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
+        const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
+        auto each = [=](auto&& f) {
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            if (!(rval[j] && cval[k])) continue;
+            float x[N];
+            V::widen(xv[j][k], x);
+#pragma unroll
+            for (int e = 0; e < N; ++e) f(x[e]);
+          }
+        };
+        rinv[j] = row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each,
+                                  CtaRow{exact_scratch});
       }
       buf ^= 1;
 
@@ -211,15 +231,25 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
   const int warp = tid >> 5;
   const int nwarps = nthr >> 5;
   const int64_t pitch = a.D * (int64_t)sizeof(T);
-  __shared__ float part[2][32];
+  __shared__ SumPair part[2][32];        // per-warp row pairs
+  __shared__ uint64_t exact_scratch[32];  // the exact path's warp totals
+  for (int i = tid; i < 64; i += nthr)
+    if ((i & 31) >= nwarps) (&part[0][0])[i] = SumPair{0.0f, 0.0f};
   int buf = 0;
+  // the statistic: each vector's squares go through four scalar (hi, lo)
+  // accumulators, then merge into the thread's running pair -- one merge
+  // level per vector the thread takes
+  using Acc = Sq32<4>;
+  const int64_t per_thread = (a.nvec + nthr - 1) / nthr;
+  const float coef = Acc::coef((N + 3) / 4);
+  const int levels = (int)per_thread + 2 + 5 + 5;  // D <= 2^24: per_thread < 2^24
 
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t b = row / a.L;
     const int64_t rowoff = row * pitch;
     const int64_t goff = GFULL ? rowoff : b * a.vstride;
     const int64_t moff = MFULL ? rowoff : b * a.vstride;
-    float ss = 0.0f;
+    SumPair ss{0.0f, 0.0f};
     for (int64_t v = tid; v < a.nvec; v += nthr) {
       const int64_t c = v * VB;
       float f[N];
@@ -236,20 +266,33 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
         st_stream<VB>((char*)a.out + rowoff + c, xr);
       }
       V::widen(xr, f);
+      Acc acc;
+      acc.zero();
 #pragma unroll
-      for (int e = 0; e < N; ++e) ss = fmaf(f[e], f[e], ss);
+      for (int e = 0; e < N; ++e) acc.add(e % 4, f[e]);
+      ss = merge(ss, acc.total());
     }
-    const float w = warp_sum(ss);
+    const SumPair w = warp_merge(ss);
     if (lane == 0) part[buf][warp] = w;
     __syncthreads();
-    float tot = 0.0f;
-    for (int i = 0; i < nwarps; ++i) tot += part[buf][i];
+    const SumPair p = warp_merge(part[buf][lane]);
     buf ^= 1;
-    const float rinv = rms_inverse(tot, a.d_f, a.inv_d, a.eps);
+    // each thread's vectors, read again by the exact path and the second
+    // pass (for the fused op, its own residual stores)
+    const void* src = OP == OP_FUSED ? (const void*)a.out : a.x;
+    const int64_t nvec = a.nvec;
+    auto each = [=](auto&& f) {
+      for (int64_t v = tid; v < nvec; v += nthr) {
+        float x[N];
+        V::widen(ld_stream<VB>((const char*)src + rowoff + v * VB), x);
+#pragma unroll
+        for (int e = 0; e < N; ++e) f(x[e]);
+      }
+    };
+    const float rinv = row_inverse_rms(p, coef, levels, a.D, a.d_f, a.eps, each,
+                                       CtaRow{exact_scratch});
 
     // second pass: each thread re-reads exactly the vectors it handled above
-    // (for the fused op, its own residual stores)
-    const void* src = OP == OP_FUSED ? (const void*)a.out : a.x;
     void* dst = OP == OP_FUSED ? a.out2 : a.out;
     for (int64_t v = tid; v < a.nvec; v += nthr) {
       const int64_t c = v * VB;

@@ -121,13 +121,18 @@ dit_status dit_residual_gate_add(void* out, const void* hidden,
 
 /*
  * adaLN modulation with a weightless RMSNorm over each row:
- *   r   = 1 / sqrt(mean_d(x[b,l,d]^2) + eps)     (fp32 statistic per row)
+ *   ms  = RN32(mean_d(x[b,l,d]^2))               (fp32 statistic per row)
+ *   r   = RN32(1 / sqrt(fl32(ms + eps)))
  *   out = rnd(fl32(fl32(fl32(x * r) * fl32(1 + S)) + H))
  * with S, H = scale, shift at [b,l,d] (mod_layout DIT_FULL) or [b,0,d]
- * (DIT_ROW_BCAST).  The statistic is fp32: the sum of squares in tree order,
- * the mean and the inverse root each within about one fp32 ulp of the
- * correctly rounded value (a refined quotient and a Newton-refined inverse
- * root).
+ * (DIT_ROW_BCAST).  The statistic is two single roundings of exact values:
+ * ms is the exact mean of the row's squares rounded once to fp32 (NaN if the
+ * row holds a NaN, +inf if it holds an infinity, +inf when the mean passes
+ * FLT_MAX), r the correctly rounded inverse root.  It does not depend on a
+ * summation order, so every launch configuration -- and the fused and
+ * grouped calls -- gives the same output bits.
+ *
+ * Rows of at most 2^24 elements (D larger: DIT_ERR_BAD_SHAPE).
  *
  * Source: prhub summary of sglang PR #34172 (LTX-2 quality=high fused
  * RMSNorm+modulate), section "key source snippet" (the eager expression
@@ -148,9 +153,8 @@ dit_status dit_rmsnorm_modulate(void* out, const void* x, const void* scale,
  *   residual_out = dit_residual_gate_add(hidden, update, gate)   (stored)
  *   modulated_out = dit_rmsnorm_modulate(residual_out, scale, shift, eps)
  * The statistic is taken over the residual as stored (rounded to the dtype),
- * with the same reduction order as dit_rmsnorm_modulate, so the two outputs
- * are bitwise those of the two separate calls.  The residual is never re-read
- * from memory.
+ * so the two outputs are bitwise those of the two separate calls.  The
+ * residual is never re-read from memory.  D at most 2^24.
  *
  * Source: the two operations above; the pages name the fused family member
  * (fused_gate_rmsnorm, prhub summary of sglang PR #34172, "implementation
@@ -275,10 +279,8 @@ dit_status dit_gate_add_rmsnorm_modulate_fp8(
  * so one grouped call covers both streams of a site.
  *
  * Each problem computes exactly what the single call of the same operation
- * computes: the residual is bitwise that of dit_residual_gate_add, and the
- * modulated output is within the same bound of the exact statistic (its
- * fp32 sum of squares may be reduced in another tree order than a single
- * call's, as the launch's block is that of the widest problem).
+ * computes, bit for bit (the row statistic is a single rounding of an exact
+ * value, whatever the launch's block).
  *
  * Launch: when every non-empty problem has 16-byte aligned pointers, pitch
  * and vec_stride and (for the modulating operations) rows of at most 8192

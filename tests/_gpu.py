@@ -3,13 +3,12 @@
 Criteria (each stated in the repository's design notes with its derivation):
 
 * residual gate and the fused op's residual: bit-exact;
-* modulation, bf16/fp16: every element bit-exact or 1 ulp away; where the
-  final add cancels (|t| >> |y|), an element may instead be within one ulp of
-  the dtype at max(|t|, |y|) -- the bound of a rounded sum -- and such elements
-  are counted;
-* modulation, fp32: |gpu - oracle| <= 2^-18 * max(|t|, |y|) (the fp32
-  tree-order sum of squares vs the oracle's double sum, propagated through
-  the inverse root, the products and the sum).
+* modulation (every dtype): bit-exact.  The row statistic is defined as two
+  single roundings of exact values (ms = RN32(mean x^2), r = RN32(1/sqrt(v))),
+  which the GPU computes exactly, and the rest of the modulation is the same
+  IEEE operations in the same order on both sides.  NaN outputs must be NaN
+  at the same positions (their payload bits are not compared).  The helper
+  still reports the ulp statistics (all zero when the criterion holds).
 """
 from __future__ import annotations
 
@@ -63,30 +62,24 @@ def assert_bit_exact(gpu: torch.Tensor, ref: torch.Tensor, what=""):
 
 def modulation_stats(gpu: torch.Tensor, ref: torch.Tensor, t: np.ndarray, dtype: str,
                      what="") -> dict:
-    """Check the modulation criterion; return the reported statistics."""
+    """Check the modulation criterion (bit-exact, NaN positions equal); return
+    the reported statistics.  `t` (the oracle's pre-shift values) is kept in
+    the signature for the error report."""
     gv, rv = values(gpu), values(ref)
     nan_g, nan_r = np.isnan(gv), np.isnan(rv)
     assert np.array_equal(nan_g, nan_r), f"{what}: NaN positions differ"
     ok = ~nan_r
     gv, rv, tt = gv[ok], rv[ok], np.abs(t.reshape(-1)[ok].astype(np.float64))
-    scale = np.maximum(tt, np.abs(rv))
     diff = np.abs(gv - rv)
     d = ulp_distance(gpu, ref)[ok]
-    if dtype == "fp32":
-        bad = diff > 2.0 ** -18 * scale + 1e-38
-        fallback = np.zeros_like(bad)
-    else:
-        within = d <= 1
-        fallback = ~within & (diff <= spacing(scale, dtype))
-        bad = ~within & ~fallback
-    idx = np.nonzero(bad)[0]
-    assert idx.size == 0, (f"{what}: {idx.size} elements outside tolerance, first "
-                           f"{idx[:5]}: gpu {gv[idx[:5]]} oracle {rv[idx[:5]]} t {tt[idx[:5]]}")
+    idx = np.nonzero(d)[0]
+    assert idx.size == 0, (f"{what}: {idx.size} elements not bit-exact (max {int(d.max())} ulp), "
+                           f"first {idx[:5]}: gpu {gv[idx[:5]]} oracle {rv[idx[:5]]} "
+                           f"t {tt[idx[:5]]}")
     denom = np.sqrt(np.sum(rv * rv))
     return {
         "max_ulp": int(d.max()) if d.size else 0,
         "not_bit_exact": int(np.count_nonzero(d)),
-        "fallback": int(np.count_nonzero(fallback)),
         "max_abs": float(diff.max()) if diff.size else 0.0,
         "rel_l2": float(np.sqrt(np.sum(diff * diff)) / denom) if denom > 0 else 0.0,
         "n": int(d.size),

@@ -19,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+from _cases import BOUNDARY_VARIANTS, boundary_tensor
 from _exact import round_to_fp32
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "statistic_ties.txt")
@@ -194,3 +195,19 @@ def test_rms_inverse_composes_the_steps(orc):
         ms = np.float32(orc.row_mean_square(raw, D, "bf16"))
         v = ms + np.float32(1e-6)
         assert same(orc.row_rms_inverse(raw, D, 1e-6, "bf16"), orc.inverse_root([v])[0])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+def test_boundary_rows_have_the_intended_mean(orc, dtype):
+    """The rows the GPU tests build on the statistic's rounding boundaries:
+    the oracle's mean against the hand-derived one, and the exact rational
+    mean against the same."""
+    for D in (64, 3077, 4096):
+        for scale_exp in ((0, 6) if dtype == "fp16" else (0, 20, -30)):
+            x, names = boundary_tensor(1, 8, D, dtype, seed=D + scale_exp, scale_exp=scale_exp)
+            for i, name in enumerate(names):
+                want = np.float32(BOUNDARY_VARIANTS[name][2] * 4.0 ** scale_exp)
+                vals = x[0, i].double().numpy()
+                assert same(exact_ms(vals.tolist()), want), (dtype, D, name)
+                raw = storage(vals.tolist(), dtype)
+                assert same(orc.row_mean_square(raw, D, dtype), want), (dtype, D, name, scale_exp)
