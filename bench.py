@@ -721,7 +721,7 @@ def run_ours(args):
                 "data": "synthetic", "config": workload, "roofline": roof,
                 "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": sum(op.launches for op in ops) * args.steps, "clocks": clocks,
-                "per_op": table}
+                "statistic": args.statistic, "per_op": table}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -734,8 +734,10 @@ def run_shapes(args):
     of 4x the L2 size: a write-flush would leave the L2 full of dirty lines
     whose write-back then falls inside the next timed call.  Beside the
     single-call median (whose resolution is the event timer's ~2 us step):
-    cold_us, 30 x (flush + call) minus 30 x flush; back-to-back and
-    CUDA-graph means of 20 calls."""
+    cold_us, 30 x (flush + call) minus 30 x flush, from which GB_s and
+    frac_of_peak are computed; back-to-back and CUDA-graph means of 20 calls.
+    Shapes with a full [B, L, D] gate also time the per-token modulation
+    (modulate_full) and the fused op with full gate, scale and shift."""
     shapes = [("ltx2_full_s126_c2048", 1, 126, 2048, "full", "bf16"),
               ("flux2_bcast_s4608_c3072", 1, 4608, 3072, "bcast", "bf16"),
               ("ideogram4_bcast_s4096_c4608", 1, 4096, 4608, "bcast", "bf16"),
@@ -783,6 +785,15 @@ def run_shapes(args):
                   lambda: dit.gate_add_rmsnorm_modulate(h, u, g, sc, sh, EPS, residual_out=o,
                                                         modulated_out=o2),
                   4 * N * es + (3 * vbytes if lay == "bcast" else N * es + 2 * vbytes))]
+        if lay == "full":  # per-token modulation: [B, L, D] scale and shift
+            scf = draw("mod", (B, L, D), seed_for(name, "scf"), dt, dev)
+            shf = draw("mod", (B, L, D), seed_for(name, "shf"), dt, dev)
+            cases += [("modulate_full", lambda: dit.rmsnorm_modulate(h, scf, shf, EPS, out=o),
+                       4 * N * es),
+                      ("fused_full_full",
+                       lambda: dit.gate_add_rmsnorm_modulate(h, u, g, scf, shf, EPS,
+                                                             residual_out=o, modulated_out=o2),
+                       7 * N * es)]
         if lay == "bcast" and dt == "bf16" and name.startswith(("ltx2", "flux2_bcast_s4608")):
             xf = draw("act", (B, L, 4 * D), seed_for(name, "ffn"), dt, dev)
             of = torch.empty_like(xf)
@@ -839,14 +850,21 @@ def run_shapes(args):
             pairs = [(run_n(flush_only), run_n(flush_then_call)) for _ in range(3)]
             cold_us = statistics.median(b - a for a, b in pairs) * 1e3
             med = statistics.median(times)
-            gbs = nbytes / (med * 1e-3) / 1e9
+            # bandwidth from cold_us (the event timer's step would inflate
+            # the single-call median of a few-us call); the median's beside it
+            gbs = nbytes / (cold_us * 1e-6) / 1e9 if cold_us > 0 else float("nan")
+            gbs_med = nbytes / (med * 1e-3) / 1e9
             print(json.dumps({"shape": name, "op": op, "dtype": dt, "B": B, "L": L, "D": D,
-                              "bytes": nbytes, "median_us": med * 1e3,
-                              "min_us": min(times) * 1e3, "GB_s": gbs,
-                              "frac_of_peak": gbs / peak,
+                              "statistic": dit.get_statistic(),
+                              "bytes": nbytes, "cold_us": cold_us, "GB_s": gbs,
+                              "frac_of_peak": gbs / peak, "median_us": med * 1e3,
+                              "min_us": min(times) * 1e3, "GB_s_median": gbs_med,
+                              "frac_of_peak_median": gbs_med / peak,
                               "back_to_back_us": b2b * 1e3,
-                              "graph_us": graph_us, "cold_us": cold_us}), flush=True)
+                              "graph_us": graph_us}), flush=True)
         del h, u, g, o, o2
+        if lay == "full":
+            del scf, shf
     return 0
 
 
@@ -869,6 +887,8 @@ def main():
                         "one grouped launch per site")
     p.add_argument("--shape", default=None,
                    help="--workload shapes: only these shapes (comma-separated names)")
+    p.add_argument("--statistic", choices=["fast", "exact"], default="fast",
+                   help="row statistic of the modulating operations (dit_set_statistic)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--op", default=None,
@@ -880,6 +900,11 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.statistic != "fast":
+        from diffusion_transformer_elementwise_gb300.build import build
+        build()
+        import diffusion_transformer_elementwise_gb300 as dit
+        dit.set_statistic(args.statistic)
     if args.workload == "shapes":
         return run_shapes(args)
     return run_ours(args)

@@ -11,6 +11,8 @@ LTX-2-style video diffusion transformers.
   audio streams of a block) in one launch
 * :func:`selfcheck` / :func:`ensure_checked` -- bit-for-bit check of one
   runtime key (op, dtype, layouts, D) on the GPU
+* :func:`set_statistic` / :func:`statistic` -- the modulation's row
+  statistic: "fast" (default) or "exact" (correctly rounded, bit-exact)
 
 Each call is one kernel of ``libdit_elementwise.so`` (C ABI in
 ``include/dit_elementwise.h``), launched on the current torch stream.  Build
@@ -29,7 +31,10 @@ from ._binding import (  # noqa: F401
     rmsnorm_modulate,
     rmsnorm_modulate_fp8,
     rmsnorm_modulate_grouped,
+    get_statistic,
     selfcheck,
     set_first_use_check,
+    set_statistic,
+    statistic,
 )
 from .build import build  # noqa: F401

@@ -94,6 +94,10 @@ def library() -> ctypes.CDLL:
             lib.dit_selfcheck_workspace_bytes.restype = i64
             lib.dit_selfcheck.argtypes = [ci, ci, ci, ci, i64, vp, i64, vp, vp]
             lib.dit_selfcheck.restype = ci
+            lib.dit_set_statistic.argtypes = [ci]
+            lib.dit_set_statistic.restype = ci
+            lib.dit_get_statistic.argtypes = []
+            lib.dit_get_statistic.restype = ci
             _lib = lib
     return _lib
 
@@ -102,6 +106,40 @@ def check(status: int, what: str) -> None:
     if status != 0:
         msg = library().dit_status_string(status).decode()
         raise DitError(status, f"{what}: {msg}")
+
+
+STATISTICS = {"fast": 0, "exact": 1}
+
+
+def set_statistic(kind: str) -> None:
+    """The row statistic of the modulating operations for the whole process
+    (dit_set_statistic): "fast" (default) or "exact"."""
+    if kind not in STATISTICS:
+        raise ValueError(f"statistic must be one of {sorted(STATISTICS)}")
+    check(library().dit_set_statistic(STATISTICS[kind]), "set_statistic")
+
+
+def get_statistic() -> str:
+    code = library().dit_get_statistic()
+    return {v: k for k, v in STATISTICS.items()}[code]
+
+
+class statistic:
+    """Context manager: the given row statistic inside the block, the
+    previous one restored after it (calls are read when made)."""
+
+    def __init__(self, kind: str):
+        self.kind = kind
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = get_statistic()
+        set_statistic(self.kind)
+        return self
+
+    def __exit__(self, *exc):
+        set_statistic(self.prev)
+        return False
 
 
 def _shape3(t: torch.Tensor, name: str):

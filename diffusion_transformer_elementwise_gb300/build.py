@@ -11,6 +11,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import glob
 import os
+import re
 import shutil
 import subprocess
 
@@ -40,6 +41,22 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+def _units():
+    """(source, extra nvcc flags, object name) of every compilation: each .cu
+    once, and k_instances.cu once per DIT_INSTANCE group it holds (the
+    longest compilations, started first)."""
+    units = []
+    for src in _sources():
+        base = os.path.basename(src)
+        if base == "k_instances.cu":
+            groups = sorted({int(k) for k in re.findall(r"DIT_INSTANCE == (\d+)", open(src).read())})
+            units += [(src, [f"-DDIT_INSTANCE={k}"], f"{base}.{k}.o") for k in groups]
+        else:
+            units.append((src, [], base + ".o"))
+    inst = [u for u in units if u[1]]
+    return inst + [u for u in units if not u[1]]
+
+
 def _inputs():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
         sorted(glob.glob(os.path.join(CSRC, "*.h"))) + \
@@ -62,16 +79,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(LIB_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(unit):
+        src, defs, name = unit
+        obj = os.path.join(BUILD_DIR, name)
+        cmd = [nvcc, *ARCH, *FLAGS, *defs, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {src} {defs}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        results = list(ex.map(compile_one, _sources()))
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        results = list(ex.map(compile_one, _units()))
     if verbose or ptxas_info:
         for _, log in results:
             if log:

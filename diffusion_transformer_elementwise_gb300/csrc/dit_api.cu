@@ -4,6 +4,7 @@
 // kernel on the caller's stream and returns; nothing is allocated.
 #include <math.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -100,11 +101,30 @@ bool misaligned(const void* p, int es) { return ((uintptr_t)p & (uintptr_t)(es -
 
 dit_status launch_status(cudaError_t e) { return e == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH; }
 
+// The process's row statistic (dit_set_statistic), read when a call is made.
+std::atomic<int> g_statistic{DIT_STATISTIC_FAST};
+
+void set_statistic(RowArgs& a, int64_t D) {
+  a.inv_d = 1.0f / (float)D;
+  a.exact = g_statistic.load(std::memory_order_relaxed) == DIT_STATISTIC_EXACT;
+}
+
 }  // namespace
 
 extern "C" {
 
 int dit_abi_version(void) { return DIT_ABI_VERSION; }
+
+dit_status dit_set_statistic(dit_statistic statistic) {
+  if (statistic != DIT_STATISTIC_FAST && statistic != DIT_STATISTIC_EXACT)
+    return DIT_ERR_BAD_STATISTIC;
+  g_statistic.store((int)statistic, std::memory_order_relaxed);
+  return DIT_OK;
+}
+
+dit_statistic dit_get_statistic(void) {
+  return (dit_statistic)g_statistic.load(std::memory_order_relaxed);
+}
 
 const char* dit_status_string(dit_status s) {
   switch (s) {
@@ -122,6 +142,8 @@ const char* dit_status_string(dit_status s) {
       return "DIT_ERR_BAD_OP: op is not a dit_op value, or count is outside [0, DIT_MAX_GROUP]";
     case DIT_ERR_WORKSPACE:
       return "DIT_ERR_WORKSPACE: workspace NULL, too small or not 256-byte aligned";
+    case DIT_ERR_BAD_STATISTIC:
+      return "DIT_ERR_BAD_STATISTIC: not a dit_statistic value";
   }
   return "unknown dit_status";
 }
@@ -252,6 +274,7 @@ dit_status prepare_modulate(void* out, const void* x, const void* scale, const v
   a.vstride = (B > 1 && !full ? vs : D) * es;
   a.eps = eps;
   a.d_f = (float)D;
+  set_statistic(a, D);
   const uint64_t bits = (uintptr_t)out | (uintptr_t)x | (uintptr_t)scale | (uintptr_t)shift |
                         (uint64_t)(D * es) | (uint64_t)a.vstride;
   p->vb = dit::widest_access(bits);
@@ -321,6 +344,7 @@ dit_status prepare_fused(void* residual_out, void* modulated_out, const void* hi
   a.vstride = (B > 1 && any_bcast ? vs : D) * es;
   a.eps = eps;
   a.d_f = (float)D;
+  set_statistic(a, D);
   const uint64_t bits = (uintptr_t)residual_out | (uintptr_t)modulated_out | (uintptr_t)hidden |
                         (uintptr_t)update | (uintptr_t)gate | (uintptr_t)scale |
                         (uintptr_t)shift | (uint64_t)(D * es) | (uint64_t)a.vstride;
@@ -684,6 +708,7 @@ dit_status dit_rmsnorm_modulate_fp8(void* out, const void* x, const void* scale,
   a.vstride = vs * es;
   a.eps = eps;
   a.d_f = (float)D;
+  set_statistic(a, D);
   a.qscale = quant_scale;
   const cudaError_t e = dit::launch_modulate_fp8(dev, dtype, full, a, B, (cudaStream_t)stream);
   return e == cudaErrorNotSupported ? DIT_ERR_BAD_SHAPE : launch_status(e);
@@ -743,6 +768,7 @@ dit_status dit_gate_add_rmsnorm_modulate_fp8(
   a.vstride = vs * es;
   a.eps = eps;
   a.d_f = (float)D;
+  set_statistic(a, D);
   a.qscale = quant_scale;
   const cudaError_t e = dit::launch_fused_fp8(dev, dtype, gate_layout == DIT_FULL,
                                               mod_layout == DIT_FULL, a, B, (cudaStream_t)stream);

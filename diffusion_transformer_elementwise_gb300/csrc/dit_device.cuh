@@ -246,42 +246,18 @@ __device__ __forceinline__ float modulate(float x, float r, float s, float h) {
 }
 
 // ---------------------------------------------------------------------------
-// packed fp32 pairs (sm_100+ f32x2 arithmetic: two IEEE fp32 operations, each
-// rounded to nearest-even, per instruction)
+// packed fp32 pairs: float2 with the sm_100 vector intrinsics -- two IEEE
+// fp32 operations per instruction, each rounded to nearest-even.  A packed
+// multiply whose result feeds a packed add may still be fused into one FMA,
+// so where that would change the result the add is a scalar intrinsic.
 // ---------------------------------------------------------------------------
-struct F2 {
-  uint64_t v;
-};
-__device__ __forceinline__ F2 f2(float lo, float hi) {
-  F2 r;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(r.v) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float f2_lo(F2 a) {
-  float lo;
-  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0,t}, %1;\n\t}" : "=f"(lo) : "l"(a.v));
-  return lo;
-}
-__device__ __forceinline__ float f2_hi(F2 a) {
-  float hi;
-  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t,%0}, %1;\n\t}" : "=f"(hi) : "l"(a.v));
-  return hi;
-}
-__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
-  F2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
-__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
-  F2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
-__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
-  F2 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
-  return r;
-}
+using F2 = float2;
+__device__ __forceinline__ F2 f2(float lo, float hi) { return make_float2(lo, hi); }
+__device__ __forceinline__ float f2_lo(F2 a) { return a.x; }
+__device__ __forceinline__ float f2_hi(F2 a) { return a.y; }
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) { return __ffma2_rn(a, b, c); }
 
 // One 32-bit word of storage <-> a pair of fp32 values (bf16x2, half2), or
 // one fp32 word <-> one value.
@@ -290,7 +266,7 @@ struct Pair;
 template <>
 struct Pair<__nv_bfloat16> {
   __device__ __forceinline__ static F2 widen(uint32_t w) {
-    return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
   }
   __device__ __forceinline__ static uint32_t narrow(F2 a) {
     __nv_bfloat162 p = __floats2bfloat162_rn(f2_lo(a), f2_hi(a));
@@ -339,23 +315,23 @@ struct Granule {
 };
 
 // hidden + update * gate on a pair, multiply then add, each rounded to
-// nearest (the non-contractible intrinsics: ptxas fuses a packed multiply and
-// a packed add into one FMA).  A fused multiply-add would differ for 16-bit
-// storage too: a negative product below fp32's range added to hidden = +0
-// gives +0 here and -0 from the FMA (found by the test of every bf16
-// update/gate pair).
+// nearest, with the scalar non-contractible intrinsics: ptxas fuses a packed
+// multiply and a packed add into one FMA (even written with the packed
+// intrinsics), and an FMA differs for 16-bit storage too -- a negative
+// product below fp32's range added to hidden = +0 gives +0 here and -0 from
+// the FMA (found by the test of every bf16 update/gate pair).
 template <class T>
 __device__ __forceinline__ F2 residual_gate2(F2 h, F2 u, F2 g) {
-  return f2(residual_gate(f2_lo(h), f2_lo(u), f2_lo(g)), residual_gate(f2_hi(h), f2_hi(u), f2_hi(g)));
+  return f2(residual_gate(h.x, u.x, g.x), residual_gate(h.y, u.y, g.y));
 }
 
-// fl(fl(n * one) + shift) per lane, n = x * r already formed: the product is
-// packed, the final add is the non-contractible scalar intrinsic.  (ptxas
-// contracts a packed multiply followed by a packed add -- or by an FMA with
-// multiplier 1 -- into one FMA; the bit-exact rounding-order test catches it.)
+// fl(fl(n * one) + shift) on a pair, n = x * r already formed: the product is
+// packed, the final add the non-contractible scalar intrinsic (ptxas
+// contracts a packed multiply followed by a packed add into one FMA; the
+// bit-exact tests catch it where the add cancels).
 __device__ __forceinline__ F2 modulate2(F2 n, F2 one, F2 shift) {
   const F2 t = f2_mul(n, one);
-  return f2(__fadd_rn(f2_lo(t), f2_lo(shift)), __fadd_rn(f2_hi(t), f2_hi(shift)));
+  return f2(__fadd_rn(t.x, shift.x), __fadd_rn(t.y, shift.y));
 }
 
 }  // namespace dit

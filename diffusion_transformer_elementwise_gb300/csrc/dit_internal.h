@@ -47,6 +47,8 @@ struct RowArgs {
   int64_t nvec;       // vectors of the kernel's width per row
   float eps;
   float d_f;          // D as fp32 (exact: D <= 2^24)
+  float inv_d;        // fl(1 / D): the fast statistic's quotient
+  int exact;          // the exact statistic (dit_set_statistic) when nonzero
   // grid-stride schedule of the row kernels: groups of rows, never
   // straddling a batch; CTA c takes groups c, c + G, c + 2G, ...
   int64_t gpb;        // groups per batch

@@ -405,7 +405,12 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
           if constexpr (kReduce) {
             if (EDGE && partial(k)) mask_part<T>(x, plo(k), phi(k));
 #pragma unroll
-            for (int i = 0; i < P; ++i) acc.add_pair(i % kNA, x[i]);
+            for (int i = 0; i < P; ++i) {
+              if (a.exact)
+                acc.add_pair(i % kNA, x[i]);
+              else
+                acc.add_pair_fast(i % kNA, x[i]);
+            }
           }
         }
         if constexpr (kReduce) ss[j] = acc.total();
@@ -454,7 +459,9 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
             }
           }
         };
-        rr[j] = row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each, CtaRow{exact_scratch});
+        rr[j] = a.exact ? row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each,
+                                          CtaRow{exact_scratch})
+                        : fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
       }
       buf ^= 1;
       // pass two: normalise, modulate, store
@@ -944,5 +951,33 @@ cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs*
     }
   });
 }
+
+// Instantiated once each, in k_instances.cu (the residual gate's in
+// k_residual_gate.cu, where it is used).
+#define DIT_PIPE_SIG(o, g, m, q)                                                             \
+  template cudaError_t launch_pipe<o, g, m, q>(const DeviceInfo&, int, RowArgs, int64_t, \
+                                               cudaStream_t, bool)
+#define DIT_GROUPED_SIG(o, g, m)                                                                 \
+  template cudaError_t launch_pipe_grouped<o, g, m>(const DeviceInfo&, int, const RowArgs*, \
+                                                    const int64_t*, int, cudaStream_t)
+extern DIT_PIPE_SIG(OP_MOD, false, false, false);
+extern DIT_PIPE_SIG(OP_MOD, false, true, false);
+extern DIT_PIPE_SIG(OP_MOD, false, false, true);
+extern DIT_PIPE_SIG(OP_MOD, false, true, true);
+extern DIT_PIPE_SIG(OP_FUSED, false, false, false);
+extern DIT_PIPE_SIG(OP_FUSED, false, true, false);
+extern DIT_PIPE_SIG(OP_FUSED, true, false, false);
+extern DIT_PIPE_SIG(OP_FUSED, true, true, false);
+extern DIT_PIPE_SIG(OP_FUSED, false, false, true);
+extern DIT_PIPE_SIG(OP_FUSED, false, true, true);
+extern DIT_PIPE_SIG(OP_FUSED, true, false, true);
+extern DIT_PIPE_SIG(OP_FUSED, true, true, true);
+extern DIT_GROUPED_SIG(OP_RGA, false, false);
+extern DIT_GROUPED_SIG(OP_MOD, false, false);
+extern DIT_GROUPED_SIG(OP_MOD, false, true);
+extern DIT_GROUPED_SIG(OP_FUSED, false, false);
+extern DIT_GROUPED_SIG(OP_FUSED, false, true);
+extern DIT_GROUPED_SIG(OP_FUSED, true, false);
+extern DIT_GROUPED_SIG(OP_FUSED, true, true);
 
 }  // namespace dit

@@ -28,6 +28,7 @@
 #include "dit_device.cuh"
 #include "dit_internal.h"
 #include "dit_pipe.cuh"
+#include "dit_wrow.cuh"
 
 namespace dit {
 
@@ -168,7 +169,12 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
         if constexpr (kReduce) {
           V::widen(xv[j][k], f);
 #pragma unroll
-          for (int e = 0; e < N; ++e) acc.add((k * N + e) % 4, f[e]);
+          for (int e = 0; e < N; ++e) {
+            if (a.exact)
+              acc.add((k * N + e) % 4, f[e]);
+            else
+              acc.add_fast((k * N + e) % 4, f[e]);
+          }
         }
       }
       ss[j] = acc.total();
@@ -195,8 +201,9 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
             for (int e = 0; e < N; ++e) f(x[e]);
           }
         };
-        rinv[j] = row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each,
-                                  CtaRow{exact_scratch});
+        rinv[j] = a.exact ? row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each,
+                                            CtaRow{exact_scratch})
+                          : fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
       }
       buf ^= 1;
 
@@ -269,7 +276,12 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
       Acc acc;
       acc.zero();
 #pragma unroll
-      for (int e = 0; e < N; ++e) acc.add(e % 4, f[e]);
+      for (int e = 0; e < N; ++e) {
+        if (a.exact)
+          acc.add(e % 4, f[e]);
+        else
+          acc.add_fast(e % 4, f[e]);
+      }
       ss = merge(ss, acc.total());
     }
     const SumPair w = warp_merge(ss);
@@ -289,8 +301,9 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
         for (int e = 0; e < N; ++e) f(x[e]);
       }
     };
-    const float rinv = row_inverse_rms(p, coef, levels, a.D, a.d_f, a.eps, each,
-                                       CtaRow{exact_scratch});
+    const float rinv = a.exact ? row_inverse_rms(p, coef, levels, a.D, a.d_f, a.eps, each,
+                                                 CtaRow{exact_scratch})
+                               : fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
 
     // second pass: each thread re-reads exactly the vectors it handled above
     void* dst = OP == OP_FUSED ? a.out2 : a.out;
@@ -394,6 +407,10 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
 #else
   if (vb >= 16) {
 #endif
+    if constexpr (OP != OP_RGA) {  // one warp per row when the row fits its registers
+      const cudaError_t w = launch_wrow<OP, GFULL, MFULL>(dev, dtype, a, B, stream);
+      if (w != cudaErrorNotSupported) return w;
+    }
     const cudaError_t e = launch_pipe<OP, GFULL, MFULL>(dev, dtype, a, B, stream);
     if (e != cudaErrorNotSupported) return e;
     if constexpr (OP == OP_RGA) {

@@ -1,5 +1,8 @@
 // dit_stat.cuh -- the row statistic of the RMSNorm-modulation (sm_103a).
 //
+// Two statistics, chosen per process (dit_set_statistic): the fast one
+// (default; fast_inverse_rms below) and the exact one described here.
+//
 // ms = RN32(sum x^2 / D), the exact mean of a row's squares rounded once to
 // fp32; v = fl(ms + eps); r = RN32(1 / sqrt(v)), the correctly rounded
 // inverse root.  Both are single roundings of exact values, so every kernel
@@ -27,6 +30,12 @@
 // path; the decision depends only on (H, L), which every thread of the row
 // holds bit for bit, so the branch is uniform.
 //
+// Window pass.  A normal row the pair cannot decide first sums its squares
+// exactly on the top 62 bits of the sum (64-bit integers, one pass) and
+// counts the squares with bits below; that settles every row but a tie or a
+// near-tie within a few units of 2^-60 of the sum, which the exact path
+// takes.
+//
 // Exact path.  The squares are summed as a big integer: x = M * 2^e with
 // M < 2^24, e >= -149, so x^2 = M^2 * 2^(2e) is an integer multiple of 2^-298
 // below 2^256.  One pass per base-2^32 digit of the scaled sum, from the
@@ -50,11 +59,8 @@
 
 namespace dit {
 
-__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
-  F2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
+// a - b on a pair, one rounding: b * (-1) + a is exact before the rounding
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) { return f2_fma(b, make_float2(-1.0f, -1.0f), a); }
 
 // s + e = a + b exactly (Knuth's TwoSum; every operation rounded to nearest)
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -113,8 +119,7 @@ struct Log2 {
 // ---------------------------------------------------------------------------
 
 // Squares of 16-bit values (exact in fp32) in NA packed (hi, lo) pairs (NA a
-// power of two).  If ptxas contracts the product into the additions that
-// follow it the results do not change: the product is exact.
+// power of two).
 template <int NA>
 struct Sq16 {
   static constexpr int kScalar = 2 * NA;
@@ -131,6 +136,20 @@ struct Sq16 {
     const F2 e = f2_add(f2_sub(hi[a], av), f2_sub(p, bv));
     hi[a] = s;
     lo[a] = f2_add(lo[a], e);
+  }
+  // the fast statistic: the square added with one FMA (lo stays zero), and
+  // the thread's plain fp32 sum of its accumulators
+  __device__ __forceinline__ void add_fast(int a, F2 x) { hi[a] = f2_fma(x, x, hi[a]); }
+  __device__ __forceinline__ float fast_total() const {
+    F2 h[NA];
+#pragma unroll
+    for (int a = 0; a < NA; ++a) h[a] = hi[a];
+#pragma unroll
+    for (int w = NA / 2; w >= 1; w /= 2) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) h[i] = f2_add(h[i], h[i + w]);
+    }
+    return __fadd_rn(h[0].x, h[0].y);
   }
   // the thread's pair: its 2 * NA accumulators renormalised and merged, two
   // at a time in the packed halves, then the two halves (log2(2 NA) levels)
@@ -187,6 +206,22 @@ struct Sq32 {
     add(a, f2_lo(x));
     add(a + 1, f2_hi(x));
   }
+  __device__ __forceinline__ void add_fast(int a, float x) { hi[a] = __fmaf_rn(x, x, hi[a]); }
+  __device__ __forceinline__ float fast_total() const {
+    float h[NS];
+#pragma unroll
+    for (int a = 0; a < NS; ++a) h[a] = hi[a];
+#pragma unroll
+    for (int w = NS / 2; w >= 1; w /= 2) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) h[i] = __fadd_rn(h[i], h[i + w]);
+    }
+    return h[0];
+  }
+  __device__ __forceinline__ void add_fast(int a, F2 x) {
+    add_fast(a, f2_lo(x));
+    add_fast(a + 1, f2_hi(x));
+  }
   __device__ __forceinline__ SumPair total() const {
     SumPair p[NS];
 #pragma unroll
@@ -201,15 +236,24 @@ struct Sq32 {
 template <class T, int NA>
 struct SqAcc : Sq16<NA> {
   __device__ __forceinline__ void add_pair(int a, F2 x) { Sq16<NA>::add(a, x); }
+  __device__ __forceinline__ void add_pair_fast(int a, F2 x) { Sq16<NA>::add_fast(a, x); }
 };
 template <int NA>
 struct SqAcc<float, NA> : Sq32<2 * NA> {
   __device__ __forceinline__ void add_pair(int a, F2 x) { Sq32<2 * NA>::add(2 * a, x); }
+  __device__ __forceinline__ void add_pair_fast(int a, F2 x) { Sq32<2 * NA>::add_fast(2 * a, x); }
 };
 
 // ---------------------------------------------------------------------------
 // warp-level merge
 // ---------------------------------------------------------------------------
+
+// A value summed over the warp (xor butterfly: every lane gets the same sum).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
 
 // The pair of every lane merged over the warp (5 levels); all lanes return
 // the same pair.
@@ -372,6 +416,95 @@ __device__ __forceinline__ uint32_t square_digit(float x, int j) {
   return sh > -48 ? (uint32_t)(Q >> -sh) : 0u;
 }
 
+// RN32((T + s) * 2^w / D) for a nonzero 64-bit T, where s is 0 or, when
+// `sticky`, a positive amount below one unit of T's last bit (1 <= D <= 2^24).
+// T is shifted up to bit 63; the quotient by D then keeps at least 40 bits,
+// and its bits below fp32's last place, the remainder and `sticky` decide the
+// rounding to nearest even (last place 2^-149 below 2^-126; +inf past
+// FLT_MAX).
+__device__ __forceinline__ float round_quotient(uint64_t T, int w, uint64_t D, bool sticky) {
+  const int lz = __clzll((long long)T);
+  T <<= lz;
+  w -= lz;
+  const uint64_t q = T / D;
+  sticky = sticky || (T - q * D) != 0u;
+  const int top = 63 - __clzll((long long)q);  // q >= 2^63 / 2^24
+  int lsb = top - 23;
+  if (lsb + w < -149) lsb = -149 - w;  // subnormal result: last place 2^-149
+  uint64_t mant = lsb < 64 ? q >> lsb : 0u;
+  const int g = lsb - 1;
+  const bool guard = g < 64 ? ((q >> g) & 1u) != 0u : false;
+  if (g < 64) {
+    sticky = sticky || (q & ((1ull << g) - 1u)) != 0u;
+  } else {
+    sticky = sticky || q != 0u;
+  }
+  if (guard && (sticky || (mant & 1u))) ++mant;
+  // mant * 2^(lsb + w), mant <= 2^24: build the fp32 bits
+  if (mant == 0u) return 0.0f;
+  int ex = lsb + w;  // exponent of mant's last bit
+  if (mant == (1ull << 24)) {
+    mant >>= 1;
+    ++ex;
+  }
+  if (mant < (1ull << 23)) return __uint_as_float((uint32_t)mant);  // subnormal (ex == -149)
+  const int field = ex + 23 + 127;
+  if (field >= 255) return __uint_as_float(0x7F800000u);
+  return __uint_as_float(((uint32_t)field << 23) | ((uint32_t)mant & 0x7FFFFFu));
+}
+
+// The fp32 value's 2M+1 midpoint above it, times D, in units of 2^lsbe: an
+// exact 64-bit integer when it fits (positive normal value given by bits).
+__device__ __forceinline__ uint64_t midpoint_times_d(uint32_t qb, uint64_t D, int lsbe) {
+  const uint64_t M = (qb & 0x7FFFFFu) | 0x800000u;
+  const int e = (int)(qb >> 23) - 150;  // q = M * 2^e; midpoint (2M+1) 2^(e-1)
+  return ((2 * M + 1) * D) << (e - 1 - lsbe);
+}
+
+// The second tier, for normal rows the pair could not decide: every square
+// summed exactly on a window of the sum's top bits.  With 2^eh <= H (H within
+// a hair of the sum S, so S < 2^(eh+2)), the window's last bit is
+// l = 2^(eh-60): A = sum of floor(x^2 / l) is exact in 64 bits (A <= S / l <
+// 2^62), and nb counts the squares with bits below l, so S / l lies in
+// [A, A + nb) -- exactly A when nb = 0, strictly inside otherwise.  The mean
+// is decided when no rounding boundary of RN32(S / D) lies in [A, A + nb]
+// (boundaries m * D / l are exact integers for D <= 2^24).  Returns false when
+// one does (a tie or a near-tie closer than nb units of 2^(eh-60)).
+template <class Each, class Row>
+__device__ __forceinline__ bool window_mean_square(Each each, Row row, float H, int64_t D, float& ms) {
+  const int eh = (int)(__float_as_uint(H) >> 23) - 127;
+  const int base = eh - 60 + 298;  // the window's last bit, as a bit of the 2^-298-scaled sum
+  uint64_t A = 0;
+  unsigned nb = 0;
+  each([&](float x) {  // no branches: zero gives M = 0
+    uint64_t M;
+    const int sh = square_position(__float_as_uint(x) & 0x7FFFFFFFu, M) - base;
+    const uint64_t Q = M * M;  // < 2^48; Q << sh < 2^62 since x^2 <= S
+    const int up = sh > 0 ? sh : 0, down = sh < 0 ? min(-sh, 63) : 0;
+    const uint64_t part = (Q >> down) << up;
+    A += part;
+    nb += ((part >> up) << down) != Q;  // bits below the window
+  });
+  A = row.sum(A);
+  nb = (unsigned)row.sum((uint64_t)nb);
+  if (A == 0u) return false;
+  const int lsbe = eh - 60;
+  const float q = round_quotient(A, lsbe, (uint64_t)D, nb != 0u);
+  if (nb == 0u) {  // S = A * 2^lsbe exactly
+    ms = q;
+    return true;
+  }
+  const uint32_t qb = __float_as_uint(q);
+  if (!(q >= 0x1p-100f) || qb >= 0x7F000000u) return false;
+  const uint64_t up = midpoint_times_d(qb, (uint64_t)D, lsbe);
+  const uint64_t dn = midpoint_times_d(qb - 1, (uint64_t)D, lsbe);
+  if (dn < A && A + nb < up) {
+    ms = q;
+    return true;
+  }
+  return false;
+}
+
 // Exact RN32(sum x^2 / D) over the row.  `each(f)` calls f(float x) for every
 // element of the row that this thread holds; `row` combines over the row's
 // threads (WarpRow or CtaRow).
@@ -425,34 +558,8 @@ __device__ __forceinline__ float exact_mean_square(Each each, Row row, int64_t D
   } else {
     sticky = sticky || w0 != 0u;
   }
-  // bit 0 of T weighs 2^w; quotient and remainder by D
-  const int w = 32 * (it + j0) - 32 - lz - 298;
-  const uint64_t Dq = (uint64_t)D;
-  const uint64_t q = T / Dq;
-  sticky = sticky || (T - q * Dq) != 0u;
-  const int top = 63 - __clzll((long long)q);  // q >= 2^63 / 2^24
-  int lsb = top - 23;
-  if (lsb + w < -149) lsb = -149 - w;  // subnormal result: last place 2^-149
-  uint64_t mant = lsb < 64 ? q >> lsb : 0u;
-  const int g = lsb - 1;
-  const bool guard = g < 64 ? ((q >> g) & 1u) != 0u : false;
-  if (g < 64) {
-    sticky = sticky || (q & ((1ull << g) - 1u)) != 0u;
-  } else {
-    sticky = sticky || q != 0u;
-  }
-  if (guard && (sticky || (mant & 1u))) ++mant;
-  // mant * 2^(lsb + w), mant <= 2^24: build the fp32 bits
-  if (mant == 0u) return 0.0f;
-  int ex = lsb + w;  // exponent of mant's last bit
-  if (mant == (1ull << 24)) {
-    mant >>= 1;
-    ++ex;
-  }
-  if (mant < (1ull << 23)) return __uint_as_float((uint32_t)mant);  // subnormal (ex == -149)
-  const int field = ex + 23 + 127;
-  if (field >= 255) return __uint_as_float(0x7F800000u);
-  return __uint_as_float(((uint32_t)field << 23) | ((uint32_t)mant & 0x7FFFFFu));
+  // bit 0 of T weighs 2^(32 (it + j0) - 32 - lz - 298)
+  return round_quotient(T, 32 * (it + j0) - 32 - lz - 298, (uint64_t)D, sticky);
 }
 
 // ---------------------------------------------------------------------------
@@ -503,14 +610,35 @@ __device__ __forceinline__ float rsqrt_rn(float v) {
 
 // r of one row from its merged pair: the fast decision, else the exact path.
 // Uniform over the row's threads (they hold the same pair).
+// The fast statistic (the library's default): from the row's fp32 sum of
+// squares S -- each thread's squares added with one FMA each, merged in tree
+// order -- ms = S * fl(1/D) with one correction by the exact residual
+// S - q D (an FMA; the correctly rounded S / D except in rare near-halfway
+// cases), v = fl(ms + eps), and r = rsqrtf(v) refined by one Newton-Raphson
+// step.  The sum carries up to about 15 fp32 ulps of rounding in tree order,
+// the quotient one, the root about one: r is within some ten fp32 ulps of the
+// exact statistic's.
+__device__ __forceinline__ float fast_inverse_rms(float S, float Df, float inv_d, float eps) {
+  const float q = __fmul_rn(S, inv_d);
+  const float ms = __fmaf_rn(__fmaf_rn(-q, Df, S), inv_d, q);
+  const float v = __fadd_rn(ms, eps);
+  const float y0 = rsqrtf(v);
+  const float e = __fmaf_rn(__fmul_rn(-v, y0), y0, 1.0f);
+  return __fmaf_rn(__fmul_rn(0.5f, y0), e, y0);
+}
+
 // `each` is taken by value (and should capture by value): only the exact
 // path, a separate function, needs the row's elements in memory.
 template <class Each, class Row>
 __device__ __forceinline__ float row_inverse_rms(SumPair p, float coef, int levels, int64_t D,
                                                  float Df, float eps, const Each& each, Row row) {
   float ms;
-  if (!mean_from_pair(p.h, p.l, sum_bound(p.h, coef, levels, Df), Df, ms))
-    ms = exact_mean_square(each, row, D);
+  if (!mean_from_pair(p.h, p.l, sum_bound(p.h, coef, levels, Df), Df, ms)) {
+    // normal rows: the window pass; ties, and rows the pair cannot stand
+    // for (not finite, too large or small), the exact path
+    const bool normal = p.h >= __fmul_rn(Df, 0x1p-100f) && p.h < 0x1p120f;
+    if (!(normal && window_mean_square(each, row, p.h, D, ms))) ms = exact_mean_square(each, row, D);
+  }
   return rsqrt_rn(__fadd_rn(ms, eps));
 }
 

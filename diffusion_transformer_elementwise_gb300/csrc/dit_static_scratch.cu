@@ -11,14 +11,14 @@
 // exits.  The caller still passes the output, the mismatch counter.
 //
 // The array's name in host code is only a stand-in for the device symbol, so
-// the host asks the runtime for its device address (cudaGetSymbolAddress),
-// once per device with that device current, and hands that address on.
+// the host asks the runtime for its device address (cudaGetSymbolAddress) on
+// every call, with the caller's device current, and hands that address on.
+// It is not cached: after cudaDeviceReset the module is loaded again in a new
+// context and the array may sit elsewhere.
 // Nothing in the array needs to start at zero: each check writes every
 // element it later reads.  Every call shares the array, so calls that
 // overlap on the GPU (other streams, other host threads) race on it.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "dit_elementwise.h"
 
@@ -26,23 +26,15 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_scratch[DIT_SELFCHECK_STATIC_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device
-std::mutex g_scratch_mu;
-
-// The device address of g_scratch on the current device (set up on the
-// first call per device); NULL if the runtime cannot provide it.
-void* scratch_address(int device) {
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[device]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) {
-      (void)cudaGetLastError();  // not the caller's next error
-      return nullptr;
-    }
-    g_scratch_addr[device] = p;
+// The device address of g_scratch in the current context; NULL if the
+// runtime cannot provide it.
+void* scratch_address() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) {
+    (void)cudaGetLastError();  // not the caller's next error
+    return nullptr;
   }
-  return g_scratch_addr[device];
+  return p;
 }
 
 }  // namespace
@@ -61,14 +53,30 @@ dit_status dit_selfcheck_static(dit_op op, dit_dtype dtype, dit_layout gate_layo
   const int64_t need = dit_selfcheck_workspace_bytes(op, dtype, D);
   if (need < 0 || need > (int64_t)DIT_SELFCHECK_STATIC_BYTES) return DIT_ERR_WORKSPACE;
   int device = -1;
-  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) {
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0) {
     (void)cudaGetLastError();
     return DIT_ERR_NO_DEVICE;
   }
-  void* ws = scratch_address(device);
+  void* ws = scratch_address();
   if (!ws) return DIT_ERR_NO_DEVICE;
   return dit_selfcheck(op, dtype, gate_layout, mod_layout, D, ws,
                        (int64_t)DIT_SELFCHECK_STATIC_BYTES, mismatches, stream);
+}
+
+dit_status dit_selfcheck_static_workspace(void** workspace, int64_t* bytes) {
+  if (!workspace || !bytes) return DIT_ERR_NULL_PTR;
+  *workspace = nullptr;
+  *bytes = 0;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0) {
+    (void)cudaGetLastError();
+    return DIT_ERR_NO_DEVICE;
+  }
+  void* ws = scratch_address();
+  if (!ws) return DIT_ERR_NO_DEVICE;
+  *workspace = ws;
+  *bytes = (int64_t)DIT_SELFCHECK_STATIC_BYTES;
+  return DIT_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,390 @@
+// dit_wrow.cuh -- the modulation and the fused op with two warps per row
+// (sm_103a; rows whose pitch and tensors are 16-byte aligned, up to 16 KB).
+//
+// A row belongs to a team of two warps; lane l of member m holds 16-byte
+// granules l + 32 m + 64 j, j < NG, in registers, so every warp-wide access is
+// 512 contiguous bytes.  The row statistic (dit_stat.cuh) is merged with warp
+// shuffles and one exchange between the two warps (a 64-thread named
+// barrier) -- no CTA barrier -- and its per-row work (pair merges, the
+// rounding of the mean, the inverse root) runs in the two warps of the row,
+// where a CTA spanning the row repeats it in each of its warps.  Two warps per
+// row halve the registers that hold the row (more warps resident per SM to
+// cover latency) and the time a warp spends on a row (a shorter tail).
+//
+// Prefetch.  Each warp owns a stage in shared memory holding its half of one
+// row of the streamed inputs (x; or hidden, update and a full gate).  Each
+// lane copies the granules it will read itself (cp.async), so
+// cp.async.wait_group -- a hardware wait, no spin -- is the only
+// synchronisation the stage needs.  The copy of the team's next row is issued
+// as soon as the current row has been read out of the stage (after pass one,
+// or after the fused op's residual), so it is in flight while the warp
+// finishes the row.  A full scale and shift (per-token modulation) are read
+// straight from global memory in pass two.
+//
+// The [B, 1, D] operands of the CTA's batch live in shared memory as fp32 --
+// gate, 1 + scale (formed once, one fp32 rounding, as the definition has it)
+// and shift -- in planes of four columns: plane q of granule g holds columns
+// g * EPG + 4q .. + 3, so a warp's 16-byte reads of one plane are 512
+// contiguous bytes (no bank conflicts).
+//
+// Schedule: the CTAs are split over the batches (CTAs per batch = grid /
+// min(B, grid)); CTA k of a batch's CTAs gives its team t rows
+// k * T + t, then + (CTAs per batch) * T, ... (T teams per CTA): the teams of
+// a batch sweep its rows in order, one moving window per batch.  With more
+// batches than CTAs a CTA takes batches c, c + grid, ..., reloading the
+// vectors (two barriers) between them.
+#pragma once
+
+#include <atomic>
+
+#include "dit_device.cuh"
+#include "dit_internal.h"
+#include "dit_pipe.cuh"
+#include "dit_stat.cuh"
+
+namespace dit {
+
+constexpr int kWrowWarps = 8;  // warps per CTA: four teams of two
+
+// [B, 1, D] vectors held in shared memory, and operands staged per row.
+template <int OP, bool GFULL, bool MFULL>
+__host__ __device__ constexpr int wrow_vectors() {
+  return (OP == OP_FUSED && !GFULL ? 1 : 0) + (MFULL ? 0 : 2);
+}
+template <int OP, bool GFULL>
+__host__ __device__ constexpr int wrow_staged() {
+  return OP == OP_MOD ? 1 : (GFULL ? 3 : 2);
+}
+
+// CTAs per SM the register bound is set for: the modulation three 8-warp
+// CTAs (at most 85 registers) and the fused op two (128), with up to 8
+// granules per lane; rows of 12 or 16 granules per lane one fewer.
+template <int OP, int NG>
+constexpr int wrow_min_blocks() {
+  return (OP == OP_FUSED ? 2 : 3) - (NG > 8 ? 1 : 0);
+}
+
+// The two warps of a row, for the exact paths of the statistic: a warp
+// reduction, then the two warps' values through shared memory between two
+// 64-thread named barriers (id 1 + team).
+struct TeamRow {
+  uint64_t* xch;  // two words of this team
+  int id, m;
+  __device__ __forceinline__ uint64_t both(uint64_t v, bool add, bool take_min) const {
+    if ((threadIdx.x & 31) == 0) xch[m] = v;
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+    const uint64_t a = xch[0], b = xch[1];
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+    return add ? a + b : take_min ? (a < b ? a : b) : (a > b ? a : b);
+  }
+  __device__ __forceinline__ uint64_t sum(uint64_t v) const { return both(WarpRow().sum(v), true, false); }
+  __device__ __forceinline__ int imin(int v) const {
+    return (int)both((uint64_t)(int64_t)(WarpRow().imin(v) + 1), false, true) - 1;
+  }
+  __device__ __forceinline__ int imax(int v) const {
+    return (int)both((uint64_t)(int64_t)(WarpRow().imax(v) + 1), false, false) - 1;
+  }
+  __device__ __forceinline__ bool any(bool b) const {
+    return both(WarpRow().any(b) ? 1u : 0u, false, false) != 0u;
+  }
+};
+
+template <int OP, class T, int NG, bool GFULL, bool MFULL, bool Q8>
+__global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wrow_kernel(RowArgs a) {
+  using G = Granule<T>;
+  constexpr int P = G::P;     // fp32 pairs per granule
+  constexpr int NPL = P / 2;  // planes of four columns per granule
+  constexpr int NV = wrow_vectors<OP, GFULL, MFULL>();
+  constexpr int NS = wrow_staged<OP, GFULL>();
+  constexpr bool kGateV = OP == OP_FUSED && !GFULL;
+  // the statistic: 4 packed slots, granule j's pair i in slot (j % R) * P + i
+  constexpr int kNA = 4;
+  constexpr int R = kNA / P;
+  using Acc = SqAcc<T, kNA>;
+  constexpr int kTerms = (NG + R - 1) / R;
+  constexpr int kLevels = Log2<Acc::kScalar>::value + 5 + 1;  // thread, warp, team
+  constexpr uint32_t kStage = NG * 512;  // bytes of one staged operand per warp
+
+  extern __shared__ float4 vsm[];  // [NV][NPL][ngr] vectors, then [W][NS][NG * 32] stages
+  __shared__ SumPair xch_pair[2][kWrowWarps / 2][2];  // the team's pair exchange, by row parity
+  __shared__ uint64_t xch_exact[kWrowWarps / 2][2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = warp >> 1, m = warp & 1;
+  const int nteams = blockDim.x >> 6;
+  const int64_t ngr = a.nvec;  // granules per row
+  const uint32_t pls = (uint32_t)ngr * 16;  // bytes per vector plane
+  // this lane's granules: l + 32 m + 64 j
+  const uint32_t lg = (uint32_t)(lane + 32 * m);
+  bool val[NG];
+#pragma unroll
+  for (int j = 0; j < NG; ++j) val[j] = lg + 64 * j < ngr;
+  const float coef = Acc::coef(kTerms);
+
+  // shared addresses of this lane's granule 0 (granule j: + j * 1024): one
+  // base per vector plane and per staged operand
+  const uint32_t vbase = smem_addr(vsm) + lg * 16;
+  uint32_t gvs[NPL], onev[NPL], shv[NPL], stage[3];
+#pragma unroll
+  for (int q = 0; q < NPL; ++q) {
+    gvs[q] = vbase + q * pls;
+    onev[q] = vbase + ((kGateV ? NPL : 0) + q) * pls;
+    shv[q] = vbase + ((kGateV ? NPL : 0) + NPL + q) * pls;
+  }
+  const uint32_t sbase = smem_addr(vsm) + NV * NPL * pls + (uint32_t)warp * NS * kStage + lane * 16;
+#pragma unroll
+  for (int op = 0; op < 3; ++op) stage[op] = sbase + op * kStage;
+  const char* const src[3] = {(const char*)a.x, (const char*)a.u, (const char*)a.g};
+  const TeamRow trow{&xch_exact[team][0], 1 + team, m};
+
+  // batches: a.gpb = CTAs per batch, a.ngroups = batches served at once
+  const int64_t cpb = a.gpb;
+  const int64_t slot = (int64_t)blockIdx.x / cpb, kc = (int64_t)blockIdx.x - slot * cpb;
+  const int64_t nbatch = a.rows / (a.L > 0 ? a.L : 1);
+  const int64_t pitch = ngr * 16;
+  const int64_t rstep = cpb * nteams;
+  float qinv_s = 1.0f;
+  if constexpr (Q8) qinv_s = __frcp_rn(__ldg(a.qscale));
+  const F2 qinv = f2(qinv_s, qinv_s);
+  constexpr int QB = 16 / (int)sizeof(T);  // E4M3 bytes per granule
+  int par = 0;
+
+  for (int64_t b = slot; b < nbatch; b += a.ngroups) {
+    if constexpr (NV > 0) {
+      __syncthreads();  // the previous batch's vectors are no longer read
+      for (int64_t g = threadIdx.x; g < ngr; g += blockDim.x) {
+        const int64_t vo = b * a.vstride + g * 16;
+        int v = 0;
+        auto put = [&](const void* vsrc, bool plus_one) {
+          F2 f[P];
+          G::widen(ld_bcast<16>((const char*)vsrc + vo), f);
+          if (plus_one) {
+#pragma unroll
+            for (int i = 0; i < P; ++i) f[i] = f2_add(f2(1.0f, 1.0f), f[i]);
+          }
+#pragma unroll
+          for (int q = 0; q < NPL; ++q)
+            vsm[((int64_t)v * NPL + q) * ngr + g] =
+                make_float4(f2_lo(f[2 * q]), f2_hi(f[2 * q]), f2_lo(f[2 * q + 1]), f2_hi(f[2 * q + 1]));
+          ++v;
+        };
+        if constexpr (kGateV) put(a.g, false);
+        if constexpr (!MFULL) {
+          put(a.sc, true);
+          put(a.sh, false);
+        }
+      }
+      __syncthreads();
+    }
+
+    // copy this warp's half of row l into the stage (an empty group past the end)
+    auto prefetch = [&](int64_t l) {
+      if (l < a.L) {
+        const int64_t rowoff = (b * a.L + l) * pitch + lg * 16;
+#pragma unroll
+        for (int op = 0; op < NS; ++op)
+#pragma unroll
+          for (int j = 0; j < NG; ++j)
+            if (val[j]) cp_async16(stage[op] + j * 512, src[op] + rowoff + j * 1024);
+      }
+      cp_async_commit();
+    };
+
+    int64_t l = kc * nteams + team;
+    prefetch(l);
+    for (; l < a.L; l += rstep) {
+      const int64_t row = b * a.L + l;
+      const int64_t rowoff = row * pitch + lg * 16;
+      cp_async_wait<0>();  // this lane's copies of row l have landed
+      Raw<16> xr[NG];
+      if constexpr (OP == OP_FUSED) {
+        // the residual: hidden + update * gate, rounded, stored, kept
+        char* const res = (char*)a.out + rowoff;
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+          if (!val[j]) continue;
+          F2 h[P], u[P], g[P], x[P];
+          G::widen(lds16(stage[0] + j * 512), h);
+          G::widen(lds16(stage[1] + j * 512), u);
+          if constexpr (GFULL) {
+            G::widen(lds16(stage[2] + j * 512), g);
+          } else {
+#pragma unroll
+            for (int q = 0; q < NPL; ++q) {
+              const Raw<16> v = lds16(gvs[q] + j * 1024);
+              g[2 * q] = f2(__uint_as_float(v.w[0]), __uint_as_float(v.w[1]));
+              g[2 * q + 1] = f2(__uint_as_float(v.w[2]), __uint_as_float(v.w[3]));
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < P; ++i) x[i] = residual_gate2<T>(h[i], u[i], g[i]);
+          xr[j] = G::narrow(x);
+          st_stream<16>(res + j * 1024, xr[j]);
+        }
+        prefetch(l + rstep);  // the stage has been read
+      } else {
+#pragma unroll
+        for (int j = 0; j < NG; ++j)
+          if (val[j]) xr[j] = lds16(stage[0] + j * 512);
+      }
+
+      // pass one and the statistic (the exact one or the fast one, as the
+      // call chose); the stage's next copy is issued once xr is read out
+      float r;
+      if (a.exact) {
+        Acc acc;
+        acc.zero();
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+          if (!val[j]) continue;
+          F2 x[P];
+          G::widen(xr[j], x);
+#pragma unroll
+          for (int i = 0; i < P; ++i) acc.add_pair((j % R) * P + i, x[i]);
+        }
+        if constexpr (OP != OP_FUSED) prefetch(l + rstep);
+        SumPair p = warp_merge(acc.total());
+        // the other warp of the row: exchange through shared memory (one
+        // slot pair per row parity, so a slot is rewritten only after the
+        // next barrier, which the other warp reaches after reading it)
+        if (lane == 0) xch_pair[par][team][m] = p;
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + team) : "memory");
+        p = merge(p, xch_pair[par][team][m ^ 1]);
+        // the exact paths read the lane's granules back from global memory
+        // (x, or the residual this lane stored): nothing of the hot path's
+        // registers is captured, and the loop is not unrolled
+        const char* const back = (OP == OP_FUSED ? (const char*)a.out : (const char*)a.x) + rowoff;
+        auto each = [=](auto&& f) {
+#pragma unroll 1
+          for (int j = 0; j < NG; ++j) {
+            if (lg + 64 * j >= ngr) continue;
+            F2 x[P];
+            G::widen(ld_stream<16>(back + j * 1024), x);
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+              f(f2_lo(x[i]));
+              f(f2_hi(x[i]));
+            }
+          }
+        };
+        r = row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each, trow);
+      } else {
+        Acc acc;
+        acc.zero();
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+          if (!val[j]) continue;
+          F2 x[P];
+          G::widen(xr[j], x);
+#pragma unroll
+          for (int i = 0; i < P; ++i) acc.add_pair_fast((j % R) * P + i, x[i]);
+        }
+        if constexpr (OP != OP_FUSED) prefetch(l + rstep);
+        const float ws = warp_sum(acc.fast_total());
+        if (lane == 0) xch_pair[par][team][m] = SumPair{ws, 0.0f};
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + team) : "memory");
+        // both warps add the two halves in the same order
+        const float S = __fadd_rn(xch_pair[par][team][0].h, xch_pair[par][team][1].h);
+        r = fast_inverse_rms(S, a.d_f, a.inv_d, a.eps);
+      }
+      par ^= 1;
+      const F2 r2 = f2(r, r);
+
+      // pass two: normalise, modulate, store
+      char* const mout = (char*)(OP == OP_FUSED ? a.out2 : a.out) + (Q8 ? row * a.D + lg * QB : rowoff);
+      const char* const scr = (const char*)a.sc + rowoff;
+      const char* const shr = (const char*)a.sh + rowoff;
+#pragma unroll
+      for (int j = 0; j < NG; ++j) {
+        if (!val[j]) continue;
+        F2 x[P], one[P], sh[P], y[P];
+        G::widen(xr[j], x);
+        if constexpr (MFULL) {
+          G::widen(ld_stream<16>(scr + j * 1024), one);
+#pragma unroll
+          for (int i = 0; i < P; ++i) one[i] = f2_add(f2(1.0f, 1.0f), one[i]);
+          G::widen(ld_stream<16>(shr + j * 1024), sh);
+        } else {
+#pragma unroll
+          for (int q = 0; q < NPL; ++q) {
+            const Raw<16> o = lds16(onev[q] + j * 1024), s = lds16(shv[q] + j * 1024);
+            one[2 * q] = f2(__uint_as_float(o.w[0]), __uint_as_float(o.w[1]));
+            one[2 * q + 1] = f2(__uint_as_float(o.w[2]), __uint_as_float(o.w[3]));
+            sh[2 * q] = f2(__uint_as_float(s.w[0]), __uint_as_float(s.w[1]));
+            sh[2 * q + 1] = f2(__uint_as_float(s.w[2]), __uint_as_float(s.w[3]));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < P; ++i) y[i] = modulate2(f2_mul(x[i], r2), one[i], sh[i]);
+        if constexpr (Q8)
+          st_stream<2 * P>(mout + j * 64 * QB, quantise_e4m3<P>(y, qinv));
+        else
+          st_stream<16>(mout + j * 1024, G::narrow(y));
+      }
+    }
+    cp_async_wait<0>();  // the last (empty) group: nothing outlives the batch
+  }
+}
+
+// Granules per lane of the instantiated kernels: 2, 4, 8, 12, 16 (a row of
+// n granules takes the smallest NG >= n / 64).
+constexpr int kWrowMaxNG = 16;
+
+// Launch the two-warps-per-row kernel; cudaErrorNotSupported when the row
+// does not fit it (more than 64 * kWrowMaxNG granules, or the stages and the
+// vectors do not fit shared memory) -- the caller then takes the CTA-per-row
+// kernel.
+template <int OP, bool GFULL, bool MFULL, bool Q8 = false>
+cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
+                        cudaStream_t stream) {
+  const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
+  a.nvec = row_bytes / 16;
+  const int64_t need = (a.nvec + 63) / 64;
+  if (need > kWrowMaxNG) return cudaErrorNotSupported;
+  constexpr int NV = wrow_vectors<OP, GFULL, MFULL>();
+  constexpr int NS = wrow_staged<OP, GFULL>();
+  const size_t vbytes = (size_t)NV * (size_t)a.nvec * 16 * (dtype == 2 ? 1 : 2);
+  const size_t limit = (size_t)(dev.smem_optin - kStaticSmemReserve);
+  return dispatch_dtype_width(dtype, 16, [&](auto tt, auto) -> cudaError_t {
+    using T = typename decltype(tt)::type;
+    auto go = [&](auto ng) -> cudaError_t {
+      constexpr int NG = decltype(ng)::value;
+      auto kern = wrow_kernel<OP, T, NG, GFULL, MFULL, Q8>;
+      const size_t smem = vbytes + (size_t)kWrowWarps * NS * NG * 512;
+      if (smem > limit) return cudaErrorNotSupported;
+      static std::atomic<int> opted[kOptinDevices];
+      const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
+      if (e != cudaSuccess) return e;
+      const int block = kWrowWarps * 32;
+      const int teams = kWrowWarps / 2;
+      int64_t G = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
+      const int64_t ctas_for_rows = B * ((a.L + teams - 1) / teams);  // no idle CTAs
+      if (G > ctas_for_rows) G = ctas_for_rows;
+      if (G < 1) G = 1;
+      const int64_t nb = B < G ? B : G;  // batches served at once
+      const int64_t cpb = G / nb;         // CTAs per batch
+      a.gpb = cpb;
+      a.ngroups = nb;
+      const int64_t grid = nb * cpb;
+      if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+      kern<<<(unsigned)grid, block, smem, stream>>>(a);
+      return cudaGetLastError();
+    };
+    if (need <= 2) return go(std::integral_constant<int, 2>{});
+    if (need <= 4) return go(std::integral_constant<int, 4>{});
+    if (need <= 8) return go(std::integral_constant<int, 8>{});
+    if (need <= 12) return go(std::integral_constant<int, 12>{});
+    return go(std::integral_constant<int, 16>{});
+  });
+}
+
+// Instantiated once, in k_instances.cu.
+#define DIT_WROW_SIG(o, g, m, q) \
+  template cudaError_t launch_wrow<o, g, m, q>(const DeviceInfo&, int, RowArgs, int64_t, cudaStream_t)
+extern DIT_WROW_SIG(OP_MOD, false, false, false);
+extern DIT_WROW_SIG(OP_MOD, false, true, false);
+extern DIT_WROW_SIG(OP_FUSED, false, false, false);
+extern DIT_WROW_SIG(OP_FUSED, false, true, false);
+extern DIT_WROW_SIG(OP_FUSED, true, false, false);
+extern DIT_WROW_SIG(OP_FUSED, true, true, false);
+
+}  // namespace dit

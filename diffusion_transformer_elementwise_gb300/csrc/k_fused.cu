@@ -3,9 +3,11 @@
 // residual_out = hidden + update * gate (sglang PR #29361, Motivation), then
 // modulated_out = rms_norm(residual_out, eps) * (1 + scale) + shift (prhub
 // summary of sglang PR #34172, "key source snippet"), the statistic taken
-// over the residual as stored.  The rounded residual stays in registers
-// between the store and the modulation, so the row is read from HBM once
-// (hidden, update, gate) and written twice (residual, modulated input).
+// over the residual as stored.  The rounded residual stays on chip between
+// its store and the modulation -- written back over the row's shared-memory
+// slot in the staged kernels, held in registers in the register kernel -- so
+// the row is read from HBM once (hidden, update, gate) and written twice
+// (residual, modulated output).
 // Kernels: dit_rows.cuh (OP_FUSED).
 #include "dit_rows.cuh"
 

@@ -87,17 +87,56 @@ typedef enum {
   DIT_ERR_NO_DEVICE = 9,    /* no current CUDA device could be queried        */
   DIT_ERR_BAD_OP = 10,      /* op is not a dit_op value, or (dit_grouped) count
                                is outside [0, DIT_MAX_GROUP]                  */
-  DIT_ERR_WORKSPACE = 11    /* dit_selfcheck: workspace NULL, smaller than
+  DIT_ERR_WORKSPACE = 11,   /* dit_selfcheck: workspace NULL, smaller than
                                dit_selfcheck_workspace_bytes or not 256-byte
                                aligned                                        */
+  DIT_ERR_BAD_STATISTIC = 12  /* dit_set_statistic: not a dit_statistic value */
 } dit_status;
 
 /* Version of this interface; bumped on any incompatible change. */
-#define DIT_ABI_VERSION 2
+#define DIT_ABI_VERSION 3
 int dit_abi_version(void);
 
 /* A static, human-readable name for a status code. */
 const char* dit_status_string(dit_status status);
+
+/*
+ * The row statistic r = 1 / sqrt(mean(x^2) + eps) of the modulating
+ * operations (dit_rmsnorm_modulate, dit_gate_add_rmsnorm_modulate, their
+ * _strided, grouped and _fp8 forms), chosen for the whole process:
+ *
+ *   DIT_STATISTIC_FAST (default): the row's fp32 sum of squares, one FMA per
+ *     element, merged in tree order; ms = S / D by a corrected quotient;
+ *     r = rsqrtf(fl(ms + eps)) refined by one Newton-Raphson step.  r is
+ *     within about ten fp32 ulps of the exact statistic's, so each output
+ *     element is within one bf16/fp16 ulp of the exact definition's except
+ *     where the final + shift cancels (|y| much smaller than
+ *     |x r (1 + scale)|), where the difference stays below one dtype ulp of
+ *     max(|t|, |y|), t = n (1 + scale).
+ *   DIT_STATISTIC_EXACT: ms = RN32(mean(x^2)), the exact mean of the row's
+ *     squares rounded once to fp32, and r = RN32(1 / sqrt(fl(ms + eps))),
+ *     correctly rounded: every output element equals the definition
+ *     evaluated in fp32 with those values, bit for bit (NaN payloads aside),
+ *     whatever kernel or launch shape computes it.  The squares are summed in
+ *     compensated (TwoSum) pairs with a proven error bound and the rounding
+ *     decided from it; rows the bound cannot decide (ties and near-ties) are
+ *     summed exactly.  It costs up to about a quarter of the modulation's
+ *     throughput (the compensated sum makes it compute-bound).
+ *
+ * Sources: the statistic is fp32 and the result is held to one bf16 ulp per
+ * element (prhub summary of sglang PR #34172, "implementation breakdown"
+ * item 2 and risks item 1).
+ *
+ * The mode is read when a call is made (host side); set it before launching,
+ * not concurrently with calls from other threads.  dit_set_statistic returns
+ * DIT_ERR_BAD_STATISTIC for other values and leaves the mode unchanged.
+ */
+typedef enum {
+  DIT_STATISTIC_FAST = 0,
+  DIT_STATISTIC_EXACT = 1
+} dit_statistic;
+dit_status dit_set_statistic(dit_statistic statistic);
+dit_statistic dit_get_statistic(void);
 
 /*
  * Gated residual update:  out[b,l,d] = hidden[b,l,d] + update[b,l,d] * G
@@ -121,16 +160,13 @@ dit_status dit_residual_gate_add(void* out, const void* hidden,
 
 /*
  * adaLN modulation with a weightless RMSNorm over each row:
- *   ms  = RN32(mean_d(x[b,l,d]^2))               (fp32 statistic per row)
- *   r   = RN32(1 / sqrt(fl32(ms + eps)))
+ *   r   = 1 / sqrt(mean_d(x[b,l,d]^2) + eps)     (fp32 statistic per row)
  *   out = rnd(fl32(fl32(fl32(x * r) * fl32(1 + S)) + H))
  * with S, H = scale, shift at [b,l,d] (mod_layout DIT_FULL) or [b,0,d]
- * (DIT_ROW_BCAST).  The statistic is two single roundings of exact values:
- * ms is the exact mean of the row's squares rounded once to fp32 (NaN if the
- * row holds a NaN, +inf if it holds an infinity, +inf when the mean passes
- * FLT_MAX), r the correctly rounded inverse root.  It does not depend on a
- * summation order, so every launch configuration -- and the fused and
- * grouped calls -- gives the same output bits.
+ * (DIT_ROW_BCAST).  The statistic is computed as dit_set_statistic chose
+ * (fast by default; exact: ms = RN32(mean(x^2)) and r = RN32(1/sqrt(fl(ms +
+ * eps))), the same output bits whatever the launch shape).  A row holding a
+ * NaN gives NaN; a row holding an infinity a zero statistic.
  *
  * Rows of at most 2^24 elements (D larger: DIT_ERR_BAD_SHAPE).
  *
@@ -278,9 +314,10 @@ dit_status dit_gate_add_rmsnorm_modulate_fp8(
  * feed-forward) and the test section (hidden 4096 = video, 2048 = audio) --
  * so one grouped call covers both streams of a site.
  *
- * Each problem computes exactly what the single call of the same operation
- * computes, bit for bit (the row statistic is a single rounding of an exact
- * value, whatever the launch's block).
+ * Each problem computes what the single call of the same operation
+ * computes: the residual bit for bit; the modulated output bit for bit with
+ * the exact statistic, and within the fast statistic's bound otherwise (its
+ * sum may be taken in another tree order than a single call's).
  *
  * Launch: when every non-empty problem has 16-byte aligned pointers, pitch
  * and vec_stride and (for the modulating operations) rows of at most 8192
@@ -375,12 +412,16 @@ dit_status dit_selfcheck(dit_op op, dit_dtype dtype, dit_layout gate_layout,
  * larger returns DIT_ERR_WORKSPACE.  The caller passes `mismatches` (device,
  * one unsigned int) as for dit_selfcheck; the call allocates nothing.
  *
- * The first call on each device looks up the array's device address (with
- * that device current), so make that first call before anything that must
- * not see such a runtime query.  All calls share the one array, and nothing
- * in it needs to start at zero; calls whose work overlaps on the GPU (other
- * streams, other host threads) race on its contents, so order them -- one
- * stream, or a synchronisation between them.
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress, a host-side runtime query that allocates nothing;
+ * the first one per context may load the library's device code).  All calls
+ * share the one array, and nothing in it needs to start at zero; calls whose
+ * work overlaps on the GPU (other streams, other host threads) race on its
+ * contents, so order them -- one stream, or a synchronisation between them.
+ * After the check the array holds dit_selfcheck's workspace layout: nine
+ * slots of round_up(2 * 7 * D * element size, 256) bytes -- inputs hidden/x,
+ * update, gate, scale, shift, outputs out (residual), modulated, and the
+ * plain kernels' expected out and modulated -- then the row statistics.
  */
 #define DIT_SELFCHECK_STATIC_BYTES (4u << 20)
 
@@ -388,6 +429,17 @@ dit_status dit_selfcheck_static(dit_op op, dit_dtype dtype,
                                 dit_layout gate_layout, dit_layout mod_layout,
                                 int64_t D, unsigned int* mismatches,
                                 dit_stream_t stream);
+
+/*
+ * dit_selfcheck_static_workspace: the device address (*workspace) and size
+ * (*bytes, DIT_SELFCHECK_STATIC_BYTES) of dit_selfcheck_static's array in
+ * the current context, for reading back what a check left there.  The array
+ * belongs to the library: the caller may read it (after the check's stream
+ * is synchronised) and must not free it.  DIT_ERR_NULL_PTR for a NULL
+ * argument; DIT_ERR_NO_DEVICE (with *workspace = NULL, *bytes = 0) when no
+ * device is current or the runtime cannot give the address.
+ */
+dit_status dit_selfcheck_static_workspace(void** workspace, int64_t* bytes);
 
 #ifdef __cplusplus
 }

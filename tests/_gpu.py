@@ -3,12 +3,15 @@
 Criteria (each stated in the repository's design notes with its derivation):
 
 * residual gate and the fused op's residual: bit-exact;
-* modulation (every dtype): bit-exact.  The row statistic is defined as two
-  single roundings of exact values (ms = RN32(mean x^2), r = RN32(1/sqrt(v))),
-  which the GPU computes exactly, and the rest of the modulation is the same
-  IEEE operations in the same order on both sides.  NaN outputs must be NaN
-  at the same positions (their payload bits are not compared).  The helper
-  still reports the ulp statistics (all zero when the criterion holds).
+* modulation with the exact row statistic (dit_set_statistic): bit-exact for
+  every dtype -- the statistic is two single roundings of exact values on
+  both sides and the rest is the same IEEE operations in the same order;
+* modulation with the fast statistic (the default): bf16/fp16 every element
+  bit-exact or 1 ulp away, except where the final add cancels (|t| >> |y|):
+  there within one dtype ulp of max(|t|, |y|) -- the bound of a rounded sum --
+  and such elements are counted; fp32 |gpu - oracle| <= 2^-18 max(|t|, |y|).
+NaN outputs must be NaN at the same positions (their payload bits are not
+compared).
 """
 from __future__ import annotations
 
@@ -61,25 +64,41 @@ def assert_bit_exact(gpu: torch.Tensor, ref: torch.Tensor, what=""):
 
 
 def modulation_stats(gpu: torch.Tensor, ref: torch.Tensor, t: np.ndarray, dtype: str,
-                     what="") -> dict:
-    """Check the modulation criterion (bit-exact, NaN positions equal); return
-    the reported statistics.  `t` (the oracle's pre-shift values) is kept in
-    the signature for the error report."""
+                     what="", exact=None) -> dict:
+    """Check the modulation criterion of the library's current row statistic
+    (or of `exact` when given); return the reported statistics."""
+    if exact is None:
+        import diffusion_transformer_elementwise_gb300 as dit
+        exact = dit.get_statistic() == "exact"
     gv, rv = values(gpu), values(ref)
     nan_g, nan_r = np.isnan(gv), np.isnan(rv)
     assert np.array_equal(nan_g, nan_r), f"{what}: NaN positions differ"
     ok = ~nan_r
     gv, rv, tt = gv[ok], rv[ok], np.abs(t.reshape(-1)[ok].astype(np.float64))
+    scale = np.maximum(tt, np.abs(rv))
     diff = np.abs(gv - rv)
     d = ulp_distance(gpu, ref)[ok]
-    idx = np.nonzero(d)[0]
-    assert idx.size == 0, (f"{what}: {idx.size} elements not bit-exact (max {int(d.max())} ulp), "
-                           f"first {idx[:5]}: gpu {gv[idx[:5]]} oracle {rv[idx[:5]]} "
-                           f"t {tt[idx[:5]]}")
+    if exact:
+        bad = d != 0
+        fallback = np.zeros_like(bad)
+    elif dtype == "fp32":
+        bad = diff > 2.0 ** -18 * scale + 1e-38
+        fallback = np.zeros_like(bad)
+    else:
+        within = d <= 1
+        fallback = ~within & (diff <= spacing(scale, dtype))
+        bad = ~within & ~fallback
+    idx = np.nonzero(bad)[0]
+    assert idx.size == 0, (f"{what}: {idx.size} elements outside the "
+                           f"{'exact' if exact else 'fast'}-statistic criterion "
+                           f"(max {int(d.max())} ulp), first {idx[:5]}: gpu {gv[idx[:5]]} "
+                           f"oracle {rv[idx[:5]]} t {tt[idx[:5]]}")
     denom = np.sqrt(np.sum(rv * rv))
     return {
+        "statistic": "exact" if exact else "fast",
         "max_ulp": int(d.max()) if d.size else 0,
         "not_bit_exact": int(np.count_nonzero(d)),
+        "fallback": int(np.count_nonzero(fallback)),
         "max_abs": float(diff.max()) if diff.size else 0.0,
         "rel_l2": float(np.sqrt(np.sum(diff * diff)) / denom) if denom > 0 else 0.0,
         "n": int(d.size),

@@ -22,3 +22,12 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(params=["fast", "exact"])
+def statistic(request):
+    """Runs the test under each row statistic of the modulating operations
+    (restoring the previous one after it)."""
+    import diffusion_transformer_elementwise_gb300 as dit
+    with dit.statistic(request.param):
+        yield request.param

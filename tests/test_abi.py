@@ -14,8 +14,8 @@ from diffusion_transformer_elementwise_gb300.build import build
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
                       "dit_elementwise.h")
 
-OK, NULLP, SHAPE, DTYPE, LAYOUT, ALIAS, EPS, LAUNCH, MISALIGNED, NODEV, BADOP, WORKSPACE = \
-    range(12)
+(OK, NULLP, SHAPE, DTYPE, LAYOUT, ALIAS, EPS, LAUNCH, MISALIGNED, NODEV, BADOP, WORKSPACE,
+ BADSTAT) = range(13)
 BF16, FP16, FP32 = 0, 1, 2
 FULL, BCAST = 0, 1
 
@@ -45,7 +45,7 @@ def test_version_and_status_strings(lib):
     m = re.search(r"#define DIT_ABI_VERSION (\d+)", open(HEADER).read())
     assert lib.dit_abi_version() == int(m.group(1))
     seen = set()
-    for code in range(12):
+    for code in range(13):
         s = lib.dit_status_string(code).decode()
         assert s.startswith("DIT_") and s not in seen
         seen.add(s)
@@ -271,3 +271,28 @@ def test_fp8_validation(lib):
     assert fused8(out=O2 + 64) == ALIAS                 # inside the residual
     assert fused8(r=H) in ok                            # residual in place
     assert f(None, None, None, None, 0, L, D, 1e-6, BF16, BCAST, D, None, None) == OK
+
+
+def test_statistic_mode(lib):
+    """dit_set_statistic / dit_get_statistic: fast (0) by default, exact (1)
+    on request, anything else rejected with the mode left as it was."""
+    import diffusion_transformer_elementwise_gb300 as dit
+    assert lib.dit_get_statistic() == 0
+    assert lib.dit_set_statistic(1) == OK and lib.dit_get_statistic() == 1
+    assert lib.dit_set_statistic(2) == BADSTAT and lib.dit_get_statistic() == 1
+    assert lib.dit_set_statistic(-1) == BADSTAT
+    assert lib.dit_set_statistic(0) == OK and lib.dit_get_statistic() == 0
+    with dit.statistic("exact"):
+        assert dit.get_statistic() == "exact"
+    assert dit.get_statistic() == "fast"
+    with pytest.raises(ValueError):
+        dit.set_statistic("approximate")
+
+
+def test_modulating_row_limit(lib):
+    """Rows longer than 2^24 elements are rejected by the modulating ops."""
+    G1 = 1 << 30
+    D = (1 << 24) + 1
+    assert mod(lib, out=G1, x=2 * G1, s=3 * G1, sh=4 * G1, D=D, L=1) == SHAPE
+    assert fused(lib, r=G1, m=2 * G1, h=3 * G1, u=4 * G1, g=5 * G1, s=6 * G1, sh=7 * G1, D=D,
+                 L=1) == SHAPE

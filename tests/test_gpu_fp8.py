@@ -1,11 +1,15 @@
 """GPU parity of the E4M3-output modulation and fused op against the oracle.
 
-Criterion: bit-exact codes.  The row statistic is the same fp32 value on
-both sides (single roundings of exact values), the fp32 modulation value y
-is formed by the same IEEE operations, then scaled by fl(1/s) and rounded
-once to E4M3 (nearest even, saturating) -- so every code equals the
-oracle's; NaN codes match NaN codes.  The residual of the fused op is
-bit-exact.
+Criterion under the exact row statistic (dit_set_statistic): bit-exact
+codes.  The statistic is the same fp32 value on both sides (single roundings
+of exact values), the fp32 modulation value y is formed by the same IEEE
+operations, then scaled by fl(1/s) and rounded once to E4M3 (nearest even,
+saturating).  Under the fast statistic (the default) y is within a few fp32
+ulps of the oracle's, far below one E4M3 step (2^-3 relative), so each code is
+the oracle's or the next one over in the ordered codes; where the final add
+cancels (|y| << |t|) a code may instead be within one E4M3 spacing of
+max(|t|, |y|) / s.  Either way NaN codes match NaN codes and the residual of
+the fused op is bit-exact.
 """
 import numpy as np
 import pytest
@@ -29,18 +33,45 @@ def _codes(t):
     return t.view(torch.uint8).cpu().numpy().reshape(-1).astype(np.int32)
 
 
+def _ordinal(c):
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def _value(c):
+    e, m = (c >> 3) & 15, c & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (8 + m) * 2.0 ** (e.astype(np.float64) - 10))
+    return np.where(c & 0x80, -v, v)
+
+
+def _spacing(a):
+    """E4M3 spacing at magnitude a (2^-9 below 2^-6, 2^(E-3) in [2^E, 2^(E+1)))."""
+    a = np.maximum(np.abs(a), 2.0 ** -6)
+    return 2.0 ** (np.floor(np.log2(a)) - 3)
+
+
 def check_fp8(gpu, ref, t, inv, what=""):
-    """Bit-exact E4M3 codes (NaN codes at the same places); returns the count
-    of differing codes (0) and a second count kept for the callers (0)."""
+    """The criterion of the library's current row statistic; returns (codes
+    not bit-exact, codes admitted by the cancellation rule)."""
+    exact = dit.get_statistic() == "exact"
     g, r = _codes(gpu), _codes(ref)
     nan_g, nan_r = (g & 0x7F) == 0x7F, (r & 0x7F) == 0x7F
     assert np.array_equal(nan_g, nan_r), f"{what}: NaN codes differ"
     ok = ~nan_r
     g, r = g[ok], r[ok]
-    idx = np.nonzero(g != r)[0]
-    assert idx.size == 0, (f"{what}: {idx.size} codes differ, first {g[idx[:5]]} vs "
+    step = np.abs(_ordinal(g) - _ordinal(r))
+    if exact:
+        fallback = np.zeros(step.shape, bool)
+        bad = step != 0
+    else:
+        tt = np.abs(t.numpy().reshape(-1)[ok].astype(np.float64)) * inv
+        scale = np.maximum(tt, np.abs(_value(r)))
+        fallback = (step > 1) & (np.abs(_value(g) - _value(r)) <= _spacing(scale))
+        bad = (step > 1) & ~fallback
+    idx = np.nonzero(bad)[0]
+    assert idx.size == 0, (f"{what}: {idx.size} codes off, first {g[idx[:5]]} vs "
                            f"{r[idx[:5]]} (t {t.numpy().reshape(-1)[ok][idx[:5]]})")
-    return 0, 0
+    return int(np.count_nonzero(step)), int(np.count_nonzero(fallback))
 
 
 def _oracle_mod8(orc, x, sc, sh, dtype, lay, qs, eps=EPS):
@@ -75,7 +106,7 @@ SHAPES = [(1, 5, 64), (2, 37, 2048), (1, 9, 3072), (1, 33, 4096), (2, 6, 8192)]
 @pytest.mark.parametrize("qs", [1.0, 0.005, 3.0])
 @pytest.mark.parametrize("layout", ["bcast", "full"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-def test_modulate_fp8(orc, dtype, layout, qs):
+def test_modulate_fp8(orc, statistic, dtype, layout, qs):
     for B, L, D in SHAPES:
         if dtype == "fp32" and D > 4096:
             continue
@@ -89,7 +120,7 @@ def test_modulate_fp8(orc, dtype, layout, qs):
 @pytest.mark.parametrize("layouts", [("bcast", "bcast"), ("full", "bcast"), ("bcast", "full"),
                                      ("full", "full")])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-def test_fused_fp8(orc, dtype, layouts):
+def test_fused_fp8(orc, statistic, dtype, layouts):
     glay, mlay = layouts
     for B, L, D in SHAPES[:4]:
         h, u, g = rga_inputs(B, L, D, dtype, glay, tag="fp8f")

@@ -71,7 +71,7 @@ WORKLOADS = [
 
 
 @pytest.mark.parametrize("w", WORKLOADS, ids=[w[0] for w in WORKLOADS])
-def test_workload(orc, w):
+def test_workload(orc, statistic, w):
     name, B, L, D, dtype, gl, ml, spread = w
     h, u, g, sc, sh = inputs(name, B, L, D, dtype, gl, ml, spread)
     idx = sample_rows(L, 48, name)

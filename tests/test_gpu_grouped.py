@@ -62,7 +62,7 @@ def test_grouped_residual_gate(orc, name, gate_layout):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("name", ["video_audio", "video_audio_b2", "widths", "eight",
                                   "with_empty", "unaligned", "long_rows", "single"])
-def test_grouped_modulate(orc, name, dtype):
+def test_grouped_modulate(orc, statistic, name, dtype):
     shapes = SETS[name]  # fp32 rows above 4096 elements take one launch per problem
     cpu = [mod_inputs(B, L, D, dtype, "bcast", tag=f"grp-mod{i}")
            for i, (B, L, D) in enumerate(shapes)]
@@ -77,7 +77,7 @@ def test_grouped_modulate(orc, name, dtype):
                                      ("full", "full")])
 @pytest.mark.parametrize("name", ["video_audio", "video_audio_b2", "widths", "eight",
                                   "with_empty", "unaligned", "long_rows"])
-def test_grouped_fused(orc, name, layouts):
+def test_grouped_fused(orc, statistic, name, layouts):
     dtype = "bf16"
     glay, mlay = layouts
     cpu = [_fused_inputs(B, L, D, dtype, glay, mlay, f"grp-fused{i}")

@@ -74,7 +74,7 @@ def test_residual_gate_misaligned(orc, dtype, layout, offsets):
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("layout", ["bcast", "full"])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_modulate(orc, dtype, layout, shape):
+def test_modulate(orc, statistic, dtype, layout, shape):
     B, L, D = shape
     x, sc, sh = mod_inputs(B, L, D, dtype, layout, row_spread=True)
     out, untouched = guarded(shape, TORCH_DTYPES[dtype], "cuda")
@@ -87,7 +87,7 @@ def test_modulate(orc, dtype, layout, shape):
 
 @pytest.mark.parametrize("offset", [1, 2, 3])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_modulate_misaligned(orc, dtype, offset):
+def test_modulate_misaligned(orc, statistic, dtype, offset):
     B, L, D = 2, 13, 4096
     x, sc, sh = mod_inputs(B, L, D, dtype, "bcast")
     xo = offset_copy(x.cuda(), offset)
@@ -102,7 +102,7 @@ def test_modulate_misaligned(orc, dtype, offset):
 @pytest.mark.parametrize("gl,ml", [("bcast", "bcast"), ("full", "bcast"), ("bcast", "full"),
                                    ("full", "full")])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_fused(orc, dtype, gl, ml, shape):
+def test_fused(orc, statistic, dtype, gl, ml, shape):
     B, L, D = shape
     h, u, g = rga_inputs(B, L, D, dtype, gl, tag="fz", row_spread=True)
     _, sc, sh = mod_inputs(B, L, D, dtype, ml, tag="fz")
@@ -146,7 +146,7 @@ def test_empty_tensors_launch_nothing(shape):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_special_values(orc, dtype):
+def test_special_values(orc, statistic, dtype):
     """inf, -inf, NaN, subnormals and overflow propagate as IEEE arithmetic
     says, identically on both sides (NaN payloads aside)."""
     B, L, D = 1, 4, 64

@@ -74,7 +74,7 @@ def test_residual_gate_in_place(orc, case):
 
 @pytest.mark.parametrize("layout", ["bcast", "full"])
 @pytest.mark.parametrize("case", CASES, ids=IDS)
-def test_modulate(orc, case, layout):
+def test_modulate(orc, statistic, case, layout):
     B, L, D, dtype = case
     x, sc, sh = mod_inputs(B, L, D, dtype, layout, tag="ph", row_spread=True)
     out, untouched = guarded((B, L, D), TORCH_DTYPES[dtype], "cuda")
@@ -88,7 +88,7 @@ def test_modulate(orc, case, layout):
 @pytest.mark.parametrize("gl,ml", [("bcast", "bcast"), ("full", "bcast"), ("bcast", "full"),
                                    ("full", "full")])
 @pytest.mark.parametrize("case", CASES, ids=IDS)
-def test_fused(orc, case, gl, ml):
+def test_fused(orc, statistic, case, gl, ml):
     B, L, D, dtype = case
     h, u, g = rga_inputs(B, L, D, dtype, gl, tag="phf", row_spread=True)
     _, sc, sh = mod_inputs(B, L, D, dtype, ml, tag="phf")

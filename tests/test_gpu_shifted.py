@@ -32,7 +32,7 @@ def _cases():
 
 
 @pytest.mark.parametrize("dtype,D", list(_cases()))
-def test_shifted_rows(orc, dtype, D):
+def test_shifted_rows(orc, statistic, dtype, D):
     B, L = 2, 7
     for glay in ("bcast", "full"):
         h, u, g = rga_inputs(B, L, D, dtype, glay, tag="shift")

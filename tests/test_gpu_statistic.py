@@ -12,6 +12,10 @@ or below one; every row a seeded permutation, optionally scaled by 2^j (the
 squares by 4^j: the same boundaries).  eps = 0 and shift = -2^j, scale = 0 expose r in
 the output: an element x = 2^j gives y = 2^j r - 2^j exactly.  Which of
 these rows need the exact path depends on the pair's bound; ties always do.
+
+Every test here runs with the exact row statistic (dit_set_statistic); the
+last one repeats the boundary rows with the fast statistic under its own
+criterion.
 """
 import zlib
 
@@ -32,6 +36,12 @@ DTYPES = ["bf16", "fp16", "fp32"]
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     ensure_built()
+
+
+@pytest.fixture(autouse=True)
+def _exact_statistic():
+    with dit.statistic("exact"):
+        yield
 
 
 def exposing_vectors(B, D, dtype, scale_exp=0, full_L=None):
@@ -140,3 +150,17 @@ def test_squares_beyond_fp32_range(orc, dtype, D):
         o = out.cpu().float()
         assert torch.isfinite(o[0, 0]).all() and torch.isfinite(o[0, 2]).all()
         assert torch.isnan(o[0, 1]).all()
+
+
+@pytest.mark.parametrize("case", CASES[::3], ids=lambda c: "x".join(map(str, c)))
+def test_fast_statistic_on_rounding_boundaries(orc, case):
+    """The same rows with the fast statistic: its criterion, not bit-exact."""
+    B, L, D, dtype = case
+    x, _ = boundary_tensor(B, L, D, dtype, seed=11)
+    sc, sh = exposing_vectors(B, D, dtype)
+    with dit.statistic("fast"):
+        assert dit.get_statistic() == "fast"
+        out = dit.rmsnorm_modulate(x.cuda(), sc.cuda(), sh.cuda(), 0.0)
+        torch.cuda.synchronize()
+    ref, t = oracle_mod(orc, x, sc, sh, dtype, "bcast", 0.0, with_t=True)
+    modulation_stats(out, ref, t.numpy(), dtype, f"fast {case}", exact=False)
