@@ -728,6 +728,42 @@ def run_ours(args):
     return 0
 
 
+def run_copy(args):
+    """torch's copy_ of 512 MB of bf16 (256 Mi elements) back to back: the
+    plain copy the roofline's denominator stands for, timed here (and
+    profiled under ncu) with the same clocking as the library's kernels.
+    Bytes per call = read + write = 1 GiB.  No kernel of this library runs."""
+    import torch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    n = 256 << 20
+    a = torch.ones(n, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(args.warmup):
+        b.copy_(a)
+    torch.cuda.synchronize()
+    times = []
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        for _ in range(args.steps):
+            s.record()
+            b.copy_(a)
+            e.record()
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e))
+    nbytes = 2 * n * 2
+    peak, _ = hbm_peak()
+    med = statistics.median(times)
+    print(json.dumps({"workload": "torch copy_ of [268435456] bf16 (512 MB read + 512 MB "
+                                  "written per call)", "bytes": nbytes, "steps": args.steps,
+                      "median_us": med * 1e3, "min_us": min(times) * 1e3,
+                      "GB_s": nbytes / (med * 1e-3) / 1e9,
+                      "GB_s_best": nbytes / (min(times) * 1e-3) / 1e9,
+                      "of_measured_peak": nbytes / (med * 1e-3) / 1e9 / peak,
+                      "clocks": clk.summary(), "gpu_launches": 0}), flush=True)
+    return 0
+
+
 def run_shapes(args):
     """One line per (shape, op): device-timed us per call with an L2 flush
     before every call, outside the timed region.  The flush *reads* a buffer
@@ -874,7 +910,8 @@ def main():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["hotpath", "chain", "chain_av", "shapes", "gelu", "fp8"],
+    p.add_argument("--workload", choices=["hotpath", "chain", "chain_av", "shapes", "gelu", "fp8",
+                                          "copy"],
                    default="hotpath")
     p.add_argument("--chain-shape", default="2,32640,4096",
                    help="B,L,D of --workload chain (e.g. 1,126,2048: the audio stream)")
@@ -907,6 +944,8 @@ def main():
         dit.set_statistic(args.statistic)
     if args.workload == "shapes":
         return run_shapes(args)
+    if args.workload == "copy":
+        return run_copy(args)
     return run_ours(args)
 
 

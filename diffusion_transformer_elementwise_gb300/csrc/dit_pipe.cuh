@@ -149,7 +149,7 @@ __device__ __forceinline__ void mask_part(F2 (&x)[Granule<T>::P], int lo, int hi
 // elements of its neighbours, masked out of the sum and never stored) and
 // holds its [B, 1, D] operands shifted by the same offset.
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS,
-          bool Q8 = false, bool PH = false>
+          bool Q8 = false, bool PH = false, bool EX = false>
 __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, const int64_t slice) {
   using G = Granule<T>;
   constexpr int P = G::P;  // fp32 pairs per 16-byte granule
@@ -359,7 +359,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   using Acc = SqAcc<T, kNA>;
   // terms per scalar accumulator: 16-bit P / kNA per granule, fp32 one
   constexpr int kTerms = (sizeof(T) == 2 ? P / kNA : 1) * VPT;
-  const float coef = Acc::coef(kTerms);
+  [[maybe_unused]] const float coef = Acc::coef(kTerms);
   constexpr int kLevels = Log2<Acc::kScalar>::value + 5 + 4;  // thread, warp, 16 warps
   int buf = 0;
   uint32_t stage = base;
@@ -406,14 +406,19 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
             if (EDGE && partial(k)) mask_part<T>(x, plo(k), phi(k));
 #pragma unroll
             for (int i = 0; i < P; ++i) {
-              if (a.exact)
+              if constexpr (EX)
                 acc.add_pair(i % kNA, x[i]);
               else
                 acc.add_pair_fast(i % kNA, x[i]);
             }
           }
         }
-        if constexpr (kReduce) ss[j] = acc.total();
+        if constexpr (kReduce) {
+          if constexpr (EX)
+            ss[j] = acc.total();
+          else
+            ss[j] = SumPair{acc.fast_total(), 0.0f};
+        }
       }
     };
     if constexpr (!PH) {
@@ -432,36 +437,40 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
       // every warp takes warp l % 16's pair, a 16-lane butterfly merges them)
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
-        const SumPair w = warp_merge(ss[j]);
+        // the fast statistic: plain fp32 sums, the same butterflies
+        const SumPair w = EX ? warp_merge(ss[j]) : SumPair{warp_sum(ss[j].h), 0.0f};
         if (lane == 0) part[buf][j][warp] = w;
       }
       __syncthreads();
       float rr[RC];
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
-        const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
-        // the exact path reads the row back from this thread's ring slots
-        const uint32_t sl0 = stage + j * JS + kX * OS;
-        auto each = [=](auto&& f) {
+        if constexpr (!EX) {
+          rr[j] = fast_inverse_rms(group_sum<16>(part[buf][j][lane & 15].h), a.d_f, a.inv_d,
+                                   a.eps);
+        } else {
+          const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
+          // the exact path reads the row back from this thread's ring slots
+          const uint32_t sl0 = stage + j * JS + kX * OS;
+          auto each = [=](auto&& f) {
 #pragma unroll
-          for (int k = 0; k < VPT; ++k) {
-            if (!cval[k]) continue;
-            F2 x[P];
-            G::widen(lds16(sl0 + k * KS), x);
-            if constexpr (PH) {
-              const uint32_t bk = (bounds >> (8 * k)) & 255u;
-              if (bk != (uint32_t)EPG << 4) mask_part<T>(x, (int)(bk & 15u), (int)(bk >> 4));
-            }
+            for (int k = 0; k < VPT; ++k) {
+              if (!cval[k]) continue;
+              F2 x[P];
+              G::widen(lds16(sl0 + k * KS), x);
+              if constexpr (PH) {
+                const uint32_t bk = (bounds >> (8 * k)) & 255u;
+                if (bk != (uint32_t)EPG << 4) mask_part<T>(x, (int)(bk & 15u), (int)(bk >> 4));
+              }
 #pragma unroll
-            for (int i = 0; i < P; ++i) {
-              f(f2_lo(x[i]));
-              f(f2_hi(x[i]));
+              for (int i = 0; i < P; ++i) {
+                f(f2_lo(x[i]));
+                f(f2_hi(x[i]));
+              }
             }
-          }
-        };
-        rr[j] = a.exact ? row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each,
-                                          CtaRow{exact_scratch})
-                        : fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
+          };
+          rr[j] = row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each, CtaRow{exact_scratch});
+        }
       }
       buf ^= 1;
       // pass two: normalise, modulate, store
@@ -523,9 +532,9 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
 }
 
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS,
-          bool Q8 = false, bool PH = false>
+          bool Q8 = false, bool PH = false, bool EX = false>
 __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
-  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>(a, blockIdx.x, blockIdx.y);
+  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH, EX>(a, blockIdx.x, blockIdx.y);
 }
 
 // The fused op's own entry, held to 80 registers: at its natural 94 two
@@ -543,9 +552,9 @@ __global__ void DIT_PIPE_BOUNDS pipe_kernel(RowArgs a) {
 #define DIT_PIPE_FUSED_BOUNDS __maxnreg__(DIT_PIPE_FUSED_MAXNREG)  // 80 x 512 threads fit
 #endif
 template <class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false,
-          bool PH = false>
+          bool PH = false, bool EX = false>
 __global__ void DIT_PIPE_FUSED_BOUNDS pipe_fused_kernel(RowArgs a) {
-  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>(a, blockIdx.x, blockIdx.y);
+  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH, EX>(a, blockIdx.x, blockIdx.y);
 }
 
 // The fused op on phased rows: its own entry and register cap.  At 80 it
@@ -560,21 +569,21 @@ __global__ void DIT_PIPE_FUSED_BOUNDS pipe_fused_kernel(RowArgs a) {
 #else
 #define DIT_PIPE_FUSED_PH_BOUNDS __maxnreg__(DIT_PIPE_FUSED_PH_MAXNREG)
 #endif
-template <class T, int VPT, int S, int RC, bool GFULL, bool MFULL>
+template <class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool EX>
 __global__ void DIT_PIPE_FUSED_PH_BOUNDS pipe_fused_phased_kernel(RowArgs a) {
-  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, false, false, true>(a, blockIdx.x, blockIdx.y);
+  pipe_body<OP_FUSED, T, VPT, S, RC, GFULL, MFULL, false, false, true, EX>(a, blockIdx.x, blockIdx.y);
 }
 
 // The kernel of one instantiation of the staged row path.
 template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8,
-          bool PH>
+          bool PH, bool EX>
 constexpr auto pipe_kernel_for() {
   if constexpr (OP == OP_FUSED && PH)
-    return pipe_fused_phased_kernel<T, VPT, S, RC, GFULL, MFULL>;
+    return pipe_fused_phased_kernel<T, VPT, S, RC, GFULL, MFULL, EX>;
   else if constexpr (OP == OP_FUSED)
-    return pipe_fused_kernel<T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, false>;
+    return pipe_fused_kernel<T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, false, EX>;
   else
-    return pipe_kernel<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>;
+    return pipe_kernel<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS, Q8, PH, EX>;
 }
 
 // Several problems of one operation in one launch: problem p owns the CTAs
@@ -601,13 +610,14 @@ struct GroupArgs {
 template <int OP>
 constexpr int group_min_blocks() { return OP == OP_MOD ? 2 : 1; }
 
-template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS0>
+template <int OP, class T, int VPT, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS0, bool EX>
 __global__ void __launch_bounds__(512, group_min_blocks<OP>())
     pipe_group_kernel(const __grid_constant__ GroupArgs ga) {
   if ((int64_t)blockIdx.x < ga.begin[1]) {  // uniform over the CTA
     const int64_t sl = ga.slices[0];
     const int64_t cta = (int64_t)blockIdx.x / sl;
-    pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS0>(ga.p[0], cta, (int64_t)blockIdx.x - cta * sl);
+    pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, ALLCOLS0, false, false, EX>(
+        ga.p[0], cta, (int64_t)blockIdx.x - cta * sl);
     return;
   }
   int p = 1;
@@ -621,7 +631,7 @@ __global__ void __launch_bounds__(512, group_min_blocks<OP>())
         reinterpret_cast<const uint64_t*>(&ga.p[p])[threadIdx.x];
   __syncthreads();
   const int64_t cta = local / sl;
-  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, false>(sa, cta, local - cta * sl);
+  pipe_body<OP, T, VPT, S, RC, GFULL, MFULL, false, false, false, EX>(sa, cta, local - cta * sl);
 }
 
 // Stages and rows per stage of each operation (tuning builds may override).
@@ -704,11 +714,11 @@ __host__ __device__ constexpr int pipe_rows() {
 
 // Launch the staged kernel with S stages; returns cudaErrorNotSupported when
 // the row is too long for it (the caller then uses the two-pass kernel).
-template <int OP, class T, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8 = false,
-          bool PH = false>
+template <int OP, class T, int S, int RC, bool GFULL, bool MFULL, bool ALLCOLS, bool Q8, bool PH,
+          bool EX>
 cudaError_t launch_pipe_s(const DeviceInfo& dev, RowArgs a, int64_t B, int block,
                           unsigned slices, size_t smem, cudaStream_t stream) {
-  auto kern = pipe_kernel_for<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8, PH>();
+  auto kern = pipe_kernel_for<OP, T, pipe_vpt<OP>(), S, RC, GFULL, MFULL, ALLCOLS, Q8, PH, EX>();
   static std::atomic<int> opted[kOptinDevices];
   const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
   if (e != cudaSuccess) return e;
@@ -746,7 +756,7 @@ constexpr int64_t kRgaDeepRowsPerSm = 128;  // below: 2 rows per stage
 
 // phased: rows whose pitch is not a multiple of 16 bytes, every streamed
 // tensor 16-byte aligned (one row per group; see pipe_body).
-template <int OP, bool GFULL, bool MFULL, bool Q8 = false>
+template <int OP, bool GFULL, bool MFULL, bool Q8, bool EX>
 cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
                         cudaStream_t stream, bool phased = false) {
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
@@ -793,8 +803,8 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       constexpr int SS_ = decltype(stages)::value;
       constexpr int RR_ = decltype(rows)::value;
       return launch_pipe_s<OP, T, SS_, RR_, GFULL, MFULL, decltype(cols)::value, Q8,
-                           decltype(ph)::value>(dev, a, B, block, slices, SS_ * per_stage,
-                                                stream);
+                           decltype(ph)::value, EX>(dev, a, B, block, slices, SS_ * per_stage,
+                                                    stream);
     };
     auto by_cols = [&](auto stages, auto rows) -> cudaError_t {
       return allcols ? go(stages, rows, std::true_type{}, std::false_type{})
@@ -834,7 +844,7 @@ cudaError_t launch_pipe(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
 // cudaErrorNotSupported otherwise, having launched nothing.  The block is the
 // widest problem's; one wave of resident CTAs is split over the problems in
 // proportion to their row groups (at least one schedule position each).
-template <int OP, bool GFULL, bool MFULL>
+template <int OP, bool GFULL, bool MFULL, bool EX>
 cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs* args_in,
                                 const int64_t* B_in, int count, cudaStream_t stream) {
   constexpr int NS = streamed_operands<OP, GFULL, MFULL>();
@@ -887,7 +897,7 @@ cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs*
     using T = typename decltype(tt)::type;
     auto go = [&](auto stages, auto cols) -> cudaError_t {
       constexpr int SS_ = decltype(stages)::value;
-      auto kern = pipe_group_kernel<OP, T, VPT, SS_, RC, GFULL, MFULL, decltype(cols)::value>;
+      auto kern = pipe_group_kernel<OP, T, VPT, SS_, RC, GFULL, MFULL, decltype(cols)::value, EX>;
       const size_t smem = SS_ * per_stage;
       static std::atomic<int> opted[kOptinDevices];
       const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
@@ -954,30 +964,58 @@ cudaError_t launch_pipe_grouped(const DeviceInfo& dev, int dtype, const RowArgs*
 
 // Instantiated once each, in k_instances.cu (the residual gate's in
 // k_residual_gate.cu, where it is used).
-#define DIT_PIPE_SIG(o, g, m, q)                                                             \
-  template cudaError_t launch_pipe<o, g, m, q>(const DeviceInfo&, int, RowArgs, int64_t, \
-                                               cudaStream_t, bool)
-#define DIT_GROUPED_SIG(o, g, m)                                                                 \
-  template cudaError_t launch_pipe_grouped<o, g, m>(const DeviceInfo&, int, const RowArgs*, \
-                                                    const int64_t*, int, cudaStream_t)
-extern DIT_PIPE_SIG(OP_MOD, false, false, false);
-extern DIT_PIPE_SIG(OP_MOD, false, true, false);
-extern DIT_PIPE_SIG(OP_MOD, false, false, true);
-extern DIT_PIPE_SIG(OP_MOD, false, true, true);
-extern DIT_PIPE_SIG(OP_FUSED, false, false, false);
-extern DIT_PIPE_SIG(OP_FUSED, false, true, false);
-extern DIT_PIPE_SIG(OP_FUSED, true, false, false);
-extern DIT_PIPE_SIG(OP_FUSED, true, true, false);
-extern DIT_PIPE_SIG(OP_FUSED, false, false, true);
-extern DIT_PIPE_SIG(OP_FUSED, false, true, true);
-extern DIT_PIPE_SIG(OP_FUSED, true, false, true);
-extern DIT_PIPE_SIG(OP_FUSED, true, true, true);
-extern DIT_GROUPED_SIG(OP_RGA, false, false);
-extern DIT_GROUPED_SIG(OP_MOD, false, false);
-extern DIT_GROUPED_SIG(OP_MOD, false, true);
-extern DIT_GROUPED_SIG(OP_FUSED, false, false);
-extern DIT_GROUPED_SIG(OP_FUSED, false, true);
-extern DIT_GROUPED_SIG(OP_FUSED, true, false);
-extern DIT_GROUPED_SIG(OP_FUSED, true, true);
+// f(std::bool_constant<EX>{}) with EX the call's row statistic: the exact
+// one or the fast one (the residual gate computes none: always false).
+template <int OP, class F>
+cudaError_t with_statistic(bool exact, F&& f) {
+  if constexpr (OP == OP_RGA)
+    return f(std::false_type{});
+  else
+    return exact ? f(std::true_type{}) : f(std::false_type{});
+}
+
+#define DIT_PIPE_SIG(o, g, m, q, e)                                                          \
+  template cudaError_t launch_pipe<o, g, m, q, e>(const DeviceInfo&, int, RowArgs, int64_t, \
+                                                  cudaStream_t, bool)
+#define DIT_GROUPED_SIG(o, g, m, e)                                                              \
+  template cudaError_t launch_pipe_grouped<o, g, m, e>(const DeviceInfo&, int, const RowArgs*, \
+                                                       const int64_t*, int, cudaStream_t)
+extern DIT_PIPE_SIG(OP_MOD, false, false, false, false);
+extern DIT_PIPE_SIG(OP_MOD, false, true, false, false);
+extern DIT_PIPE_SIG(OP_MOD, false, false, true, false);
+extern DIT_PIPE_SIG(OP_MOD, false, true, true, false);
+extern DIT_PIPE_SIG(OP_FUSED, false, false, false, false);
+extern DIT_PIPE_SIG(OP_FUSED, false, true, false, false);
+extern DIT_PIPE_SIG(OP_FUSED, true, false, false, false);
+extern DIT_PIPE_SIG(OP_FUSED, true, true, false, false);
+extern DIT_PIPE_SIG(OP_FUSED, false, false, true, false);
+extern DIT_PIPE_SIG(OP_FUSED, false, true, true, false);
+extern DIT_PIPE_SIG(OP_FUSED, true, false, true, false);
+extern DIT_PIPE_SIG(OP_FUSED, true, true, true, false);
+extern DIT_PIPE_SIG(OP_MOD, false, false, false, true);
+extern DIT_PIPE_SIG(OP_MOD, false, true, false, true);
+extern DIT_PIPE_SIG(OP_MOD, false, false, true, true);
+extern DIT_PIPE_SIG(OP_MOD, false, true, true, true);
+extern DIT_PIPE_SIG(OP_FUSED, false, false, false, true);
+extern DIT_PIPE_SIG(OP_FUSED, false, true, false, true);
+extern DIT_PIPE_SIG(OP_FUSED, true, false, false, true);
+extern DIT_PIPE_SIG(OP_FUSED, true, true, false, true);
+extern DIT_PIPE_SIG(OP_FUSED, false, false, true, true);
+extern DIT_PIPE_SIG(OP_FUSED, false, true, true, true);
+extern DIT_PIPE_SIG(OP_FUSED, true, false, true, true);
+extern DIT_PIPE_SIG(OP_FUSED, true, true, true, true);
+extern DIT_GROUPED_SIG(OP_RGA, false, false, false);
+extern DIT_GROUPED_SIG(OP_MOD, false, false, false);
+extern DIT_GROUPED_SIG(OP_MOD, false, true, false);
+extern DIT_GROUPED_SIG(OP_FUSED, false, false, false);
+extern DIT_GROUPED_SIG(OP_FUSED, false, true, false);
+extern DIT_GROUPED_SIG(OP_FUSED, true, false, false);
+extern DIT_GROUPED_SIG(OP_FUSED, true, true, false);
+extern DIT_GROUPED_SIG(OP_MOD, false, false, true);
+extern DIT_GROUPED_SIG(OP_MOD, false, true, true);
+extern DIT_GROUPED_SIG(OP_FUSED, false, false, true);
+extern DIT_GROUPED_SIG(OP_FUSED, false, true, true);
+extern DIT_GROUPED_SIG(OP_FUSED, true, false, true);
+extern DIT_GROUPED_SIG(OP_FUSED, true, true, true);
 
 }  // namespace dit

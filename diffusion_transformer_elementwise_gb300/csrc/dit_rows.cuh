@@ -57,7 +57,7 @@ constexpr int row_min_blocks() { return VB == 2 ? 2 : 1; }
 #define DIT_ROW_BOUNDS(VB) __launch_bounds__(kRowBlockMax, row_min_blocks<VB>())
 #endif
 
-template <int OP, class T, int VB, int R, bool GFULL, bool MFULL>
+template <int OP, class T, int VB, int R, bool GFULL, bool MFULL, bool EX>
 __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
   using V = Vec<T, VB>;
   constexpr int N = V::N;
@@ -102,7 +102,7 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
   // element e of the thread's row part into accumulator e % 4
   using Acc = Sq32<4>;
   constexpr int kTerms = (VPT * N + 3) / 4;
-  const float coef = Acc::coef(kTerms);
+  [[maybe_unused]] const float coef = Acc::coef(kTerms);
   constexpr int kLevels = 2 + 5 + 4;  // thread, warp, 16 warps
   int buf = 0;
   const int lane = tid & 31;
@@ -170,40 +170,45 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
           V::widen(xv[j][k], f);
 #pragma unroll
           for (int e = 0; e < N; ++e) {
-            if (a.exact)
+            if constexpr (EX)
               acc.add((k * N + e) % 4, f[e]);
             else
               acc.add_fast((k * N + e) % 4, f[e]);
           }
         }
       }
-      ss[j] = acc.total();
+      ss[j] = EX ? acc.total() : SumPair{acc.fast_total(), 0.0f};
     }
     if constexpr (kReduce) {
       // row pairs over the warp, then over the warps
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        const SumPair w = warp_merge(ss[j]);
+        // the fast statistic: plain fp32 sums over the same butterflies
+        const SumPair w = EX ? warp_merge(ss[j]) : SumPair{warp_sum(ss[j].h), 0.0f};
         if (lane == 0) part[buf][j][warp] = w;
       }
       __syncthreads();
       float rinv[R];
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
-        auto each = [=](auto&& f) {
+        if constexpr (!EX) {
+          rinv[j] = fast_inverse_rms(group_sum<16>(part[buf][j][lane & 15].h), a.d_f, a.inv_d,
+                                     a.eps);
+        } else {
+          const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
+          auto each = [=](auto&& f) {
 #pragma unroll
-          for (int k = 0; k < VPT; ++k) {
-            if (!(rval[j] && cval[k])) continue;
-            float x[N];
-            V::widen(xv[j][k], x);
+            for (int k = 0; k < VPT; ++k) {
+              if (!(rval[j] && cval[k])) continue;
+              float x[N];
+              V::widen(xv[j][k], x);
 #pragma unroll
-            for (int e = 0; e < N; ++e) f(x[e]);
-          }
-        };
-        rinv[j] = a.exact ? row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each,
-                                            CtaRow{exact_scratch})
-                          : fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
+              for (int e = 0; e < N; ++e) f(x[e]);
+            }
+          };
+          rinv[j] = row_inverse_rms(p, coef, kLevels, a.D, a.d_f, a.eps, each,
+                                    CtaRow{exact_scratch});
+        }
       }
       buf ^= 1;
 
@@ -227,8 +232,11 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
   }
 }
 
-// Rows longer than one CTA can hold: two passes over each row.
-template <int OP, class T, int VB, bool GFULL, bool MFULL>
+// Rows longer than one CTA can hold: two passes over each row.  The fast
+// statistic keeps the compensated merge across a thread's vectors here: a
+// thread may take thousands of them, and a plain fp32 running sum would then
+// carry an error bound of that many units.
+template <int OP, class T, int VB, bool GFULL, bool MFULL, bool EX>
 __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
   using V = Vec<T, VB>;
   constexpr int N = V::N;
@@ -248,8 +256,8 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
   // level per vector the thread takes
   using Acc = Sq32<4>;
   const int64_t per_thread = (a.nvec + nthr - 1) / nthr;
-  const float coef = Acc::coef((N + 3) / 4);
-  const int levels = (int)per_thread + 2 + 5 + 5;  // D <= 2^24: per_thread < 2^24
+  [[maybe_unused]] const float coef = Acc::coef((N + 3) / 4);
+  [[maybe_unused]] const int levels = (int)per_thread + 2 + 5 + 5;  // D <= 2^24
 
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t b = row / a.L;
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
       acc.zero();
 #pragma unroll
       for (int e = 0; e < N; ++e) {
-        if (a.exact)
+        if constexpr (EX)
           acc.add(e % 4, f[e]);
         else
           acc.add_fast(e % 4, f[e]);
@@ -301,9 +309,11 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
         for (int e = 0; e < N; ++e) f(x[e]);
       }
     };
-    const float rinv = a.exact ? row_inverse_rms(p, coef, levels, a.D, a.d_f, a.eps, each,
-                                                 CtaRow{exact_scratch})
-                               : fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
+    float rinv;
+    if constexpr (EX)
+      rinv = row_inverse_rms(p, coef, levels, a.D, a.d_f, a.eps, each, CtaRow{exact_scratch});
+    else
+      rinv = fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
 
     // second pass: each thread re-reads exactly the vectors it handled above
     void* dst = OP == OP_FUSED ? a.out2 : a.out;
@@ -359,13 +369,15 @@ cudaError_t launch_long_rows(const DeviceInfo& dev, int dtype, int vb, RowArgs a
     using T = typename decltype(tt)::type;
     constexpr int VB = decltype(w)::value;
     if constexpr (VB == 16 || VB == (int)sizeof(T)) {
-      const void* fn = (const void*)long_row_kernel<OP, T, VB, GFULL, MFULL>;
-      const int block = 1024;
-      int64_t grid = (int64_t)dev.sm_count * resident_ctas(dev, fn, block);
-      if (grid > a.rows) grid = a.rows;
-      if (grid < 1) grid = 1;
-      long_row_kernel<OP, T, VB, GFULL, MFULL><<<(unsigned)grid, block, 0, stream>>>(a);
-      return cudaGetLastError();
+      return with_statistic<OP>(a.exact, [&](auto ex) -> cudaError_t {
+        auto kern = long_row_kernel<OP, T, VB, GFULL, MFULL, decltype(ex)::value>;
+        const int block = 1024;
+        int64_t grid = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block);
+        if (grid > a.rows) grid = a.rows;
+        if (grid < 1) grid = 1;
+        kern<<<(unsigned)grid, block, 0, stream>>>(a);
+        return cudaGetLastError();
+      });
     } else {
       return cudaErrorInvalidValue;
     }
@@ -398,7 +410,10 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
 #ifndef DIT_ROWS_IN_REGISTERS
   if (vb < 16 && (OP == OP_RGA || vb < 8) && streamed_bases_aligned<OP, GFULL, MFULL>(a)) {
-    const cudaError_t e = launch_pipe<OP, GFULL, MFULL>(dev, dtype, a, B, stream, true);
+    const cudaError_t e = with_statistic<OP>(a.exact, [&](auto ex) {
+      return launch_pipe<OP, GFULL, MFULL, false, decltype(ex)::value>(dev, dtype, a, B, stream,
+                                                                        true);
+    });
     if (e != cudaErrorNotSupported) return e;
   }
 #endif
@@ -408,10 +423,14 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
   if (vb >= 16) {
 #endif
     if constexpr (OP != OP_RGA) {  // one warp per row when the row fits its registers
-      const cudaError_t w = launch_wrow<OP, GFULL, MFULL>(dev, dtype, a, B, stream);
+      const cudaError_t w = with_statistic<OP>(a.exact, [&](auto ex) {
+        return launch_wrow<OP, GFULL, MFULL, false, decltype(ex)::value>(dev, dtype, a, B, stream);
+      });
       if (w != cudaErrorNotSupported) return w;
     }
-    const cudaError_t e = launch_pipe<OP, GFULL, MFULL>(dev, dtype, a, B, stream);
+    const cudaError_t e = with_statistic<OP>(a.exact, [&](auto ex) {
+      return launch_pipe<OP, GFULL, MFULL, false, decltype(ex)::value>(dev, dtype, a, B, stream);
+    });
     if (e != cudaErrorNotSupported) return e;
     if constexpr (OP == OP_RGA) {
       return cudaErrorInvalidValue;  // unreachable: the residual gate tiles columns
@@ -434,7 +453,9 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
     constexpr int TB = thread_bytes<VB>();
     constexpr int R = rows_in_flight<OP, GFULL, MFULL, VB>();
     const int64_t threads_needed = (row_bytes + TB - 1) / TB;
-    const void* fn = (const void*)row_kernel<OP, T, VB, R, GFULL, MFULL>;
+    return with_statistic<OP>(a.exact, [&](auto ex) -> cudaError_t {
+    auto kern = row_kernel<OP, T, VB, R, GFULL, MFULL, decltype(ex)::value>;
+    const void* fn = (const void*)kern;
     int block;
     unsigned slices = 1;
     if (OP == OP_RGA) {
@@ -458,9 +479,9 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
     if (G > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
     a.step_b = G / a.gpb;
     a.step_g = G - a.step_b * a.gpb;
-    row_kernel<OP, T, VB, R, GFULL, MFULL><<<dim3((unsigned)G, slices, 1), dim3((unsigned)block, 1, 1), 0,
-                                             stream>>>(a);
+    kern<<<dim3((unsigned)G, slices, 1), dim3((unsigned)block, 1, 1), 0, stream>>>(a);
     return cudaGetLastError();
+    });
     }
   });
   if (e != cudaSuccess || !too_long) return e;

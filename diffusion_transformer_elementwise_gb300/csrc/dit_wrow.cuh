@@ -27,14 +27,25 @@
 // g * EPG + 4q .. + 3, so a warp's 16-byte reads of one plane are 512
 // contiguous bytes (no bank conflicts).
 //
-// Schedule: the CTAs are split over the batches (CTAs per batch = grid /
-// min(B, grid)); CTA k of a batch's CTAs gives its team t rows
-// k * T + t, then + (CTAs per batch) * T, ... (T teams per CTA): the teams of
-// a batch sweep its rows in order, one moving window per batch.  With more
-// batches than CTAs a CTA takes batches c, c + grid, ..., reloading the
-// vectors (two barriers) between them.
+// Schedule.  On large tensors (more than 8 rows per team in one wave of
+// CTAs) a CTA gives each of its teams a few rows (four for the modulation,
+// two for the fused op) of one batch, and the grid holds as many CTAs as that
+// takes -- several waves, handed to the SMs by the hardware as earlier CTAs
+// finish.  A one-wave persistent grid, each CTA striding over the tensor,
+// left SMs idle at the end there: the SMs do not stream at the same rate,
+// and a static split of the rows made the slowest SM set the kernel's length
+// (on [1,32640,4096] bf16 the modulation took 98 us back to back with it, 86
+// us with four rows per team; the fused op 182 and 160 us with two).  Smaller
+// tensors run exactly one wave with the rows split statically: there a
+// second, partial wave of short CTAs costs more than the imbalance
+// ([1,8160,4096]: 510 CTAs of four rows per team, 1.1 waves, ran the
+// modulation in 35.7 us L2-flushed).  CTA k of a batch's CTAs gives its team t rows k * T + t, then
+// + (CTAs per batch) * T, ... (T teams per CTA).  The grid is capped at 64
+// waves; with more batches than that a CTA takes batches c, c + grid, ...,
+// reloading the vectors (two barriers) between them.
 #pragma once
 
+#include <algorithm>
 #include <atomic>
 
 #include "dit_device.cuh"
@@ -89,7 +100,10 @@ struct TeamRow {
   }
 };
 
-template <int OP, class T, int NG, bool GFULL, bool MFULL, bool Q8>
+// EX: the exact row statistic (dit_set_statistic); otherwise the fast one.
+// Each is its own instantiation, so the fast kernel carries none of the
+// exact path's registers.
+template <int OP, class T, int NG, bool GFULL, bool MFULL, bool Q8, bool EX>
 __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wrow_kernel(RowArgs a) {
   using G = Granule<T>;
   constexpr int P = G::P;     // fp32 pairs per granule
@@ -149,6 +163,21 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
   int par = 0;
 
   for (int64_t b = slot; b < nbatch; b += a.ngroups) {
+    // copy this warp's half of row l into the stage (an empty group past the end)
+    auto prefetch = [&](int64_t l) {
+      if (l < a.L) {
+        const int64_t rowoff = (b * a.L + l) * pitch + lg * 16;
+#pragma unroll
+        for (int op = 0; op < NS; ++op)
+#pragma unroll
+          for (int j = 0; j < NG; ++j)
+            if (val[j]) cp_async16(stage[op] + j * 512, src[op] + rowoff + j * 1024);
+      }
+      cp_async_commit();
+    };
+
+    int64_t l = kc * nteams + team;
+    prefetch(l);  // in flight while the vectors load
     if constexpr (NV > 0) {
       __syncthreads();  // the previous batch's vectors are no longer read
       for (int64_t g = threadIdx.x; g < ngr; g += blockDim.x) {
@@ -176,21 +205,6 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
       __syncthreads();
     }
 
-    // copy this warp's half of row l into the stage (an empty group past the end)
-    auto prefetch = [&](int64_t l) {
-      if (l < a.L) {
-        const int64_t rowoff = (b * a.L + l) * pitch + lg * 16;
-#pragma unroll
-        for (int op = 0; op < NS; ++op)
-#pragma unroll
-          for (int j = 0; j < NG; ++j)
-            if (val[j]) cp_async16(stage[op] + j * 512, src[op] + rowoff + j * 1024);
-      }
-      cp_async_commit();
-    };
-
-    int64_t l = kc * nteams + team;
-    prefetch(l);
     for (; l < a.L; l += rstep) {
       const int64_t row = b * a.L + l;
       const int64_t rowoff = row * pitch + lg * 16;
@@ -227,10 +241,10 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
           if (val[j]) xr[j] = lds16(stage[0] + j * 512);
       }
 
-      // pass one and the statistic (the exact one or the fast one, as the
-      // call chose); the stage's next copy is issued once xr is read out
+      // pass one and the statistic (the exact one or the fast one); the
+      // stage's next copy is issued once xr is read out
       float r;
-      if (a.exact) {
+      if constexpr (EX) {
         Acc acc;
         acc.zero();
 #pragma unroll
@@ -325,15 +339,18 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
   }
 }
 
-// Granules per lane of the instantiated kernels: 2, 4, 8, 12, 16 (a row of
-// n granules takes the smallest NG >= n / 64).
-constexpr int kWrowMaxNG = 16;
+// Granules per lane of the instantiated kernels: 2, 4, 8 (a row of n
+// granules takes the smallest NG >= n / 64): rows up to 8 KB.  Longer rows
+// take the CTA-per-row kernel: with 12 granules per lane the fused op needed
+// 244 registers (one CTA per SM) and the modulation 126 (two), and both ran
+// slower than the CTA-per-row kernel on [1,4096,4608] bf16.
+constexpr int kWrowMaxNG = 8;
 
 // Launch the two-warps-per-row kernel; cudaErrorNotSupported when the row
 // does not fit it (more than 64 * kWrowMaxNG granules, or the stages and the
 // vectors do not fit shared memory) -- the caller then takes the CTA-per-row
 // kernel.
-template <int OP, bool GFULL, bool MFULL, bool Q8 = false>
+template <int OP, bool GFULL, bool MFULL, bool Q8, bool EX>
 cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
                         cudaStream_t stream) {
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
@@ -348,7 +365,7 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
     using T = typename decltype(tt)::type;
     auto go = [&](auto ng) -> cudaError_t {
       constexpr int NG = decltype(ng)::value;
-      auto kern = wrow_kernel<OP, T, NG, GFULL, MFULL, Q8>;
+      auto kern = wrow_kernel<OP, T, NG, GFULL, MFULL, Q8, EX>;
       const size_t smem = vbytes + (size_t)kWrowWarps * NS * NG * 512;
       if (smem > limit) return cudaErrorNotSupported;
       static std::atomic<int> opted[kOptinDevices];
@@ -356,9 +373,22 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       if (e != cudaSuccess) return e;
       const int block = kWrowWarps * 32;
       const int teams = kWrowWarps / 2;
-      int64_t G = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
-      const int64_t ctas_for_rows = B * ((a.L + teams - 1) / teams);  // no idle CTAs
-      if (G > ctas_for_rows) G = ctas_for_rows;
+      // short-lived CTAs of a few rows per team, handed to SMs by the
+      // hardware as they free up, and at least one wave of them when the
+      // rows allow (one row per team at least)
+      const int64_t wave = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
+      const int64_t most = (a.L + teams - 1) / teams;  // CTAs per batch, one row per team
+      int64_t per_batch;
+      if (B * a.L <= 8 * wave * teams) {
+        // at most 8 rows per team in one wave: exactly one wave (fewer rows
+        // than teams: one row per team), the rows split statically
+        per_batch = std::min(most, (wave + B - 1) / B);
+      } else {
+        const int64_t rows_per_team = OP == OP_FUSED ? 2 : 4;
+        per_batch = (a.L + teams * rows_per_team - 1) / (teams * rows_per_team);
+      }
+      int64_t G = B * per_batch;
+      if (G > 64 * wave) G = 64 * wave;  // very many batches: CTAs stride over them
       if (G < 1) G = 1;
       const int64_t nb = B < G ? B : G;  // batches served at once
       const int64_t cpb = G / nb;         // CTAs per batch
@@ -371,20 +401,25 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
     };
     if (need <= 2) return go(std::integral_constant<int, 2>{});
     if (need <= 4) return go(std::integral_constant<int, 4>{});
-    if (need <= 8) return go(std::integral_constant<int, 8>{});
-    if (need <= 12) return go(std::integral_constant<int, 12>{});
-    return go(std::integral_constant<int, 16>{});
+    return go(std::integral_constant<int, 8>{});
   });
 }
 
 // Instantiated once, in k_instances.cu.
-#define DIT_WROW_SIG(o, g, m, q) \
-  template cudaError_t launch_wrow<o, g, m, q>(const DeviceInfo&, int, RowArgs, int64_t, cudaStream_t)
-extern DIT_WROW_SIG(OP_MOD, false, false, false);
-extern DIT_WROW_SIG(OP_MOD, false, true, false);
-extern DIT_WROW_SIG(OP_FUSED, false, false, false);
-extern DIT_WROW_SIG(OP_FUSED, false, true, false);
-extern DIT_WROW_SIG(OP_FUSED, true, false, false);
-extern DIT_WROW_SIG(OP_FUSED, true, true, false);
+#define DIT_WROW_SIG(o, g, m, q, e)                                                       \
+  template cudaError_t launch_wrow<o, g, m, q, e>(const DeviceInfo&, int, RowArgs, int64_t, \
+                                                  cudaStream_t)
+extern DIT_WROW_SIG(OP_MOD, false, false, false, false);
+extern DIT_WROW_SIG(OP_MOD, false, true, false, false);
+extern DIT_WROW_SIG(OP_FUSED, false, false, false, false);
+extern DIT_WROW_SIG(OP_FUSED, false, true, false, false);
+extern DIT_WROW_SIG(OP_FUSED, true, false, false, false);
+extern DIT_WROW_SIG(OP_FUSED, true, true, false, false);
+extern DIT_WROW_SIG(OP_MOD, false, false, false, true);
+extern DIT_WROW_SIG(OP_MOD, false, true, false, true);
+extern DIT_WROW_SIG(OP_FUSED, false, false, false, true);
+extern DIT_WROW_SIG(OP_FUSED, false, true, false, true);
+extern DIT_WROW_SIG(OP_FUSED, true, false, false, true);
+extern DIT_WROW_SIG(OP_FUSED, true, true, false, true);
 
 }  // namespace dit

@@ -24,21 +24,29 @@ cudaError_t launch_fused(const DeviceInfo& dev, int dtype, int vb, bool gate_ful
 
 cudaError_t launch_fused_fp8(const DeviceInfo& dev, int dtype, bool gate_full, bool mod_full,
                              const RowArgs& a, int64_t B, cudaStream_t stream) {
-  if (gate_full)
-    return mod_full ? launch_pipe<OP_FUSED, true, true, true>(dev, dtype, a, B, stream)
-                    : launch_pipe<OP_FUSED, true, false, true>(dev, dtype, a, B, stream);
-  return mod_full ? launch_pipe<OP_FUSED, false, true, true>(dev, dtype, a, B, stream)
-                  : launch_pipe<OP_FUSED, false, false, true>(dev, dtype, a, B, stream);
+  return with_statistic<OP_FUSED>(a.exact, [&](auto ex) {
+    constexpr bool EX = decltype(ex)::value;
+    if (gate_full)
+      return mod_full ? launch_pipe<OP_FUSED, true, true, true, EX>(dev, dtype, a, B, stream)
+                      : launch_pipe<OP_FUSED, true, false, true, EX>(dev, dtype, a, B, stream);
+    return mod_full ? launch_pipe<OP_FUSED, false, true, true, EX>(dev, dtype, a, B, stream)
+                    : launch_pipe<OP_FUSED, false, false, true, EX>(dev, dtype, a, B, stream);
+  });
 }
 
 cudaError_t launch_fused_grouped(const DeviceInfo& dev, int dtype, bool gate_full,
                                  bool mod_full, const RowArgs* a, const int64_t* B, int count,
                                  cudaStream_t stream) {
-  if (gate_full)
-    return mod_full ? launch_pipe_grouped<OP_FUSED, true, true>(dev, dtype, a, B, count, stream)
-                    : launch_pipe_grouped<OP_FUSED, true, false>(dev, dtype, a, B, count, stream);
-  return mod_full ? launch_pipe_grouped<OP_FUSED, false, true>(dev, dtype, a, B, count, stream)
-                  : launch_pipe_grouped<OP_FUSED, false, false>(dev, dtype, a, B, count, stream);
+  return with_statistic<OP_FUSED>(count > 0 && a[0].exact, [&](auto ex) {
+    constexpr bool EX = decltype(ex)::value;
+    if (gate_full)
+      return mod_full
+                 ? launch_pipe_grouped<OP_FUSED, true, true, EX>(dev, dtype, a, B, count, stream)
+                 : launch_pipe_grouped<OP_FUSED, true, false, EX>(dev, dtype, a, B, count, stream);
+    return mod_full
+               ? launch_pipe_grouped<OP_FUSED, false, true, EX>(dev, dtype, a, B, count, stream)
+               : launch_pipe_grouped<OP_FUSED, false, false, EX>(dev, dtype, a, B, count, stream);
+  });
 }
 
 }  // namespace dit

@@ -15,51 +15,96 @@
 namespace dit {
 
 #if DIT_INSTANCE == 0
-DIT_WROW_SIG(OP_MOD, false, false, false);
+DIT_WROW_SIG(OP_MOD, false, false, false, false);
 #elif DIT_INSTANCE == 1
-DIT_WROW_SIG(OP_MOD, false, true, false);
+DIT_WROW_SIG(OP_MOD, false, true, false, false);
 #elif DIT_INSTANCE == 2
-DIT_WROW_SIG(OP_FUSED, false, false, false);
+DIT_WROW_SIG(OP_FUSED, false, false, false, false);
 #elif DIT_INSTANCE == 3
-DIT_WROW_SIG(OP_FUSED, false, true, false);
+DIT_WROW_SIG(OP_FUSED, false, true, false, false);
 #elif DIT_INSTANCE == 4
-DIT_WROW_SIG(OP_FUSED, true, false, false);
+DIT_WROW_SIG(OP_FUSED, true, false, false, false);
 #elif DIT_INSTANCE == 5
-DIT_WROW_SIG(OP_FUSED, true, true, false);
+DIT_WROW_SIG(OP_FUSED, true, true, false, false);
 #elif DIT_INSTANCE == 6
-DIT_PIPE_SIG(OP_MOD, false, false, false);
+DIT_WROW_SIG(OP_MOD, false, false, false, true);
 #elif DIT_INSTANCE == 7
-DIT_PIPE_SIG(OP_MOD, false, true, false);
+DIT_WROW_SIG(OP_MOD, false, true, false, true);
 #elif DIT_INSTANCE == 8
-DIT_PIPE_SIG(OP_MOD, false, false, true);
+DIT_WROW_SIG(OP_FUSED, false, false, false, true);
 #elif DIT_INSTANCE == 9
-DIT_PIPE_SIG(OP_MOD, false, true, true);
+DIT_WROW_SIG(OP_FUSED, false, true, false, true);
 #elif DIT_INSTANCE == 10
-DIT_PIPE_SIG(OP_FUSED, false, false, false);
+DIT_WROW_SIG(OP_FUSED, true, false, false, true);
 #elif DIT_INSTANCE == 11
-DIT_PIPE_SIG(OP_FUSED, false, true, false);
+DIT_WROW_SIG(OP_FUSED, true, true, false, true);
 #elif DIT_INSTANCE == 12
-DIT_PIPE_SIG(OP_FUSED, true, false, false);
+DIT_PIPE_SIG(OP_MOD, false, false, false, false);
 #elif DIT_INSTANCE == 13
-DIT_PIPE_SIG(OP_FUSED, true, true, false);
+DIT_PIPE_SIG(OP_MOD, false, true, false, false);
 #elif DIT_INSTANCE == 14
-DIT_PIPE_SIG(OP_FUSED, false, false, true);
+DIT_PIPE_SIG(OP_MOD, false, false, true, false);
 #elif DIT_INSTANCE == 15
-DIT_PIPE_SIG(OP_FUSED, false, true, true);
+DIT_PIPE_SIG(OP_MOD, false, true, true, false);
 #elif DIT_INSTANCE == 16
-DIT_PIPE_SIG(OP_FUSED, true, false, true);
+DIT_PIPE_SIG(OP_FUSED, false, false, false, false);
 #elif DIT_INSTANCE == 17
-DIT_PIPE_SIG(OP_FUSED, true, true, true);
+DIT_PIPE_SIG(OP_FUSED, false, true, false, false);
 #elif DIT_INSTANCE == 18
-DIT_GROUPED_SIG(OP_RGA, false, false);
-DIT_GROUPED_SIG(OP_MOD, false, false);
-DIT_GROUPED_SIG(OP_MOD, false, true);
+DIT_PIPE_SIG(OP_FUSED, true, false, false, false);
 #elif DIT_INSTANCE == 19
-DIT_GROUPED_SIG(OP_FUSED, false, false);
-DIT_GROUPED_SIG(OP_FUSED, false, true);
+DIT_PIPE_SIG(OP_FUSED, true, true, false, false);
 #elif DIT_INSTANCE == 20
-DIT_GROUPED_SIG(OP_FUSED, true, false);
-DIT_GROUPED_SIG(OP_FUSED, true, true);
+DIT_PIPE_SIG(OP_FUSED, false, false, true, false);
+#elif DIT_INSTANCE == 21
+DIT_PIPE_SIG(OP_FUSED, false, true, true, false);
+#elif DIT_INSTANCE == 22
+DIT_PIPE_SIG(OP_FUSED, true, false, true, false);
+#elif DIT_INSTANCE == 23
+DIT_PIPE_SIG(OP_FUSED, true, true, true, false);
+#elif DIT_INSTANCE == 24
+DIT_PIPE_SIG(OP_MOD, false, false, false, true);
+#elif DIT_INSTANCE == 25
+DIT_PIPE_SIG(OP_MOD, false, true, false, true);
+#elif DIT_INSTANCE == 26
+DIT_PIPE_SIG(OP_MOD, false, false, true, true);
+#elif DIT_INSTANCE == 27
+DIT_PIPE_SIG(OP_MOD, false, true, true, true);
+#elif DIT_INSTANCE == 28
+DIT_PIPE_SIG(OP_FUSED, false, false, false, true);
+#elif DIT_INSTANCE == 29
+DIT_PIPE_SIG(OP_FUSED, false, true, false, true);
+#elif DIT_INSTANCE == 30
+DIT_PIPE_SIG(OP_FUSED, true, false, false, true);
+#elif DIT_INSTANCE == 31
+DIT_PIPE_SIG(OP_FUSED, true, true, false, true);
+#elif DIT_INSTANCE == 32
+DIT_PIPE_SIG(OP_FUSED, false, false, true, true);
+#elif DIT_INSTANCE == 33
+DIT_PIPE_SIG(OP_FUSED, false, true, true, true);
+#elif DIT_INSTANCE == 34
+DIT_PIPE_SIG(OP_FUSED, true, false, true, true);
+#elif DIT_INSTANCE == 35
+DIT_PIPE_SIG(OP_FUSED, true, true, true, true);
+#elif DIT_INSTANCE == 36
+DIT_GROUPED_SIG(OP_RGA, false, false, false);
+DIT_GROUPED_SIG(OP_MOD, false, false, false);
+DIT_GROUPED_SIG(OP_MOD, false, true, false);
+#elif DIT_INSTANCE == 37
+DIT_GROUPED_SIG(OP_MOD, false, false, true);
+DIT_GROUPED_SIG(OP_MOD, false, true, true);
+#elif DIT_INSTANCE == 38
+DIT_GROUPED_SIG(OP_FUSED, false, false, false);
+DIT_GROUPED_SIG(OP_FUSED, false, true, false);
+#elif DIT_INSTANCE == 39
+DIT_GROUPED_SIG(OP_FUSED, true, false, false);
+DIT_GROUPED_SIG(OP_FUSED, true, true, false);
+#elif DIT_INSTANCE == 40
+DIT_GROUPED_SIG(OP_FUSED, false, false, true);
+DIT_GROUPED_SIG(OP_FUSED, false, true, true);
+#elif DIT_INSTANCE == 41
+DIT_GROUPED_SIG(OP_FUSED, true, false, true);
+DIT_GROUPED_SIG(OP_FUSED, true, true, true);
 #else
 #error "no such instance group"
 #endif

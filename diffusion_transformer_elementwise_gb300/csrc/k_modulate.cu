@@ -20,15 +20,21 @@ cudaError_t launch_modulate(const DeviceInfo& dev, int dtype, int vb, bool mod_f
 
 cudaError_t launch_modulate_fp8(const DeviceInfo& dev, int dtype, bool mod_full,
                                 const RowArgs& a, int64_t B, cudaStream_t stream) {
-  return mod_full ? launch_pipe<OP_MOD, false, true, true>(dev, dtype, a, B, stream)
-                  : launch_pipe<OP_MOD, false, false, true>(dev, dtype, a, B, stream);
+  return with_statistic<OP_MOD>(a.exact, [&](auto ex) {
+    constexpr bool EX = decltype(ex)::value;
+    return mod_full ? launch_pipe<OP_MOD, false, true, true, EX>(dev, dtype, a, B, stream)
+                    : launch_pipe<OP_MOD, false, false, true, EX>(dev, dtype, a, B, stream);
+  });
 }
 
 cudaError_t launch_modulate_grouped(const DeviceInfo& dev, int dtype, bool mod_full,
                                     const RowArgs* a, const int64_t* B, int count,
                                     cudaStream_t stream) {
-  return mod_full ? launch_pipe_grouped<OP_MOD, false, true>(dev, dtype, a, B, count, stream)
-                  : launch_pipe_grouped<OP_MOD, false, false>(dev, dtype, a, B, count, stream);
+  return with_statistic<OP_MOD>(count > 0 && a[0].exact, [&](auto ex) {
+    constexpr bool EX = decltype(ex)::value;
+    return mod_full ? launch_pipe_grouped<OP_MOD, false, true, EX>(dev, dtype, a, B, count, stream)
+                    : launch_pipe_grouped<OP_MOD, false, false, EX>(dev, dtype, a, B, count, stream);
+  });
 }
 
 }  // namespace dit

@@ -117,7 +117,7 @@ cudaError_t launch_rga_bcast(const DeviceInfo& dev, int dtype, int vb, const Row
 
 cudaError_t launch_rga_grouped(const DeviceInfo& dev, int dtype, const RowArgs* a,
                                const int64_t* B, int count, cudaStream_t stream) {
-  return launch_pipe_grouped<OP_RGA, false, false>(dev, dtype, a, B, count, stream);
+  return launch_pipe_grouped<OP_RGA, false, false, false>(dev, dtype, a, B, count, stream);
 }
 
 }  // namespace dit

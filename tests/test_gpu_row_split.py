@@ -6,14 +6,22 @@ rows.  This is the property the multi-GPU path rests on (rows are
 independent; the RMS statistic is per row), checked under both row
 statistics, at widths that reach the staged (4096), phased (3077), 8-byte
 (3076) and two-pass (20000) kernels, with block boundaries that fall off a
-16-byte boundary."""
+16-byte boundary.
+
+One exception, by design: the fast statistic's fp32 sum depends on the
+kernel's summation order, and a block whose view starts off a 16-byte
+boundary takes another kernel (narrower accesses) than the whole call.  The
+modulated outputs of such a split are therefore checked against the oracle
+under the fast statistic's criterion instead of bitwise; every residual, and
+every output under the exact statistic, is compared bit for bit.
+"""
 import numpy as np
 import pytest
 import torch
 
 import diffusion_transformer_elementwise_gb300 as dit
-from _cases import bits, mod_inputs, rga_inputs
-from _gpu import ensure_built
+from _cases import bits, mod_inputs, oracle_fused, oracle_mod, rga_inputs
+from _gpu import ensure_built, modulation_stats
 from diffusion_transformer_elementwise_gb300.replicas import row_block
 
 pytestmark = pytest.mark.gpu
@@ -38,45 +46,67 @@ def _same(a, b, what):
 
 @pytest.mark.parametrize("world", [2, 3])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
-def test_row_blocks_equal_one_call(statistic, case, world):
+def test_row_blocks_equal_one_call(orc, statistic, case, world):
     L, D, dtype = case
+    es = 4 if dtype == "fp32" else 2
     h, u, gb = (t.cuda() for t in rga_inputs(1, L, D, dtype, "bcast", tag="split"))
     gf = rga_inputs(1, L, D, dtype, "full", tag="splitf")[2].cuda()
     _, scb, shb = (t.cuda() for t in mod_inputs(1, L, D, dtype, "bcast", tag="split"))
     _, scf, shf = (t.cuda() for t in mod_inputs(1, L, D, dtype, "full", tag="splitf"))
     qs = torch.full((1,), 0.02, dtype=torch.float32, device="cuda")
+    blocks = _blocks(L, world)
+    # every block's view starts on a 16-byte boundary: the same kernel as the
+    # whole call (the tensors themselves are 256-byte aligned)
+    aligned = all((s * D * es) % 16 == 0 for s, _ in blocks)
 
     def rows(t, s, e):
         return t[:, s:e] if t.shape[1] == L else t
 
+    # name: (call, outputs, index of the modulated output or None, oracle of it)
     ops = {
         "rga_bcast": (lambda s, e, o: dit.residual_gate_add(rows(h, s, e), rows(u, s, e),
-                                                             gb, out=o[0]), 1),
+                                                             gb, out=o[0]), 1, None, None),
         "rga_full": (lambda s, e, o: dit.residual_gate_add(rows(h, s, e), rows(u, s, e),
-                                                            rows(gf, s, e), out=o[0]), 1),
+                                                            rows(gf, s, e), out=o[0]), 1, None,
+                     None),
         "mod_bcast": (lambda s, e, o: dit.rmsnorm_modulate(rows(h, s, e), scb, shb, EPS,
-                                                            out=o[0]), 1),
+                                                            out=o[0]), 1, 0,
+                      lambda: oracle_mod(orc, h.cpu(), scb.cpu(), shb.cpu(), dtype, "bcast",
+                                         EPS, with_t=True)),
         "mod_full": (lambda s, e, o: dit.rmsnorm_modulate(rows(h, s, e), rows(scf, s, e),
-                                                           rows(shf, s, e), EPS, out=o[0]), 1),
+                                                           rows(shf, s, e), EPS, out=o[0]), 1, 0,
+                     lambda: oracle_mod(orc, h.cpu(), scf.cpu(), shf.cpu(), dtype, "full", EPS,
+                                        with_t=True)),
         "fused_bcast": (lambda s, e, o: dit.gate_add_rmsnorm_modulate(
             rows(h, s, e), rows(u, s, e), gb, scb, shb, EPS, residual_out=o[0],
-            modulated_out=o[1]), 2),
+            modulated_out=o[1]), 2, 1,
+            lambda: oracle_fused(orc, h.cpu(), u.cpu(), gb.cpu(), scb.cpu(), shb.cpu(), dtype,
+                                 "bcast", "bcast", EPS, with_t=True)[1:]),
         "fused_full_full": (lambda s, e, o: dit.gate_add_rmsnorm_modulate(
             rows(h, s, e), rows(u, s, e), rows(gf, s, e), rows(scf, s, e), rows(shf, s, e), EPS,
-            residual_out=o[0], modulated_out=o[1]), 2),
-        "mod_fp8": (lambda s, e, o: dit.rmsnorm_modulate_fp8(rows(h, s, e), scb, shb, qs, EPS,
-                                                              out=o[0]), 1),
+            residual_out=o[0], modulated_out=o[1]), 2, 1,
+            lambda: oracle_fused(orc, h.cpu(), u.cpu(), gf.cpu(), scf.cpu(), shf.cpu(), dtype,
+                                 "full", "full", EPS, with_t=True)[1:]),
     }
-    for name, (call, nout) in ops.items():
+    if (D * es) % 16 == 0 and D * es <= 16384:  # rows the E4M3 output takes
+        ops["mod_fp8"] = (lambda s, e, o: dit.rmsnorm_modulate_fp8(rows(h, s, e), scb, shb, qs,
+                                                                   EPS, out=o[0]), 1, None, None)
+    for name, (call, nout, mk, ref) in ops.items():
         fp8 = name.endswith("fp8")
+
         def outputs():
             if fp8:
                 return [torch.full((1, L, D), 0x55, dtype=torch.uint8, device="cuda")]
             return [torch.full_like(h, 3.0) for _ in range(nout)]
         whole, split = outputs(), outputs()
         call(0, L, whole)
-        for s, e in _blocks(L, world):
+        for s, e in blocks:
             call(s, e, [o[:, s:e] for o in split])
         torch.cuda.synchronize()
         for k in range(nout):
-            _same(split[k], whole[k], f"{name} output {k} world {world} {case}")
+            what = f"{name} output {k} world {world} {case}"
+            if k == mk and statistic == "fast" and not aligned:
+                r, t = ref()
+                modulation_stats(split[k].cpu(), r, t.numpy(), dtype, what)
+            else:
+                _same(split[k], whole[k], what)
