@@ -729,38 +729,44 @@ def run_ours(args):
 
 
 def run_copy(args):
-    """torch's copy_ of 512 MB of bf16 (256 Mi elements) back to back: the
-    plain copy the roofline's denominator stands for, timed here (and
-    profiled under ncu) with the same clocking as the library's kernels.
-    Bytes per call = read + write = 1 GiB.  No kernel of this library runs."""
+    """Reference copies of 512 MB of bf16 (256 Mi elements) back to back, with
+    the clocking of the library's kernels: torch's copy_ (a device-to-device
+    memcpy, the copy MEASURED_PEAKS.json's peak was taken with; ncu profiles
+    kernels only, so it cannot see it) and the same bytes through an SM
+    kernel ncu can profile -- torch's elementwise multiply by one (exact),
+    reading 512 MB and writing 512 MB.  Bytes per call = read + write = 1 GiB.
+    No kernel of this library runs."""
     import torch
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     n = 256 << 20
     a = torch.ones(n, dtype=torch.bfloat16, device=dev)
     b = torch.empty_like(a)
-    for _ in range(args.warmup):
-        b.copy_(a)
-    torch.cuda.synchronize()
-    times = []
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(0) as clk:
-        for _ in range(args.steps):
-            s.record()
-            b.copy_(a)
-            e.record()
-            torch.cuda.synchronize()
-            times.append(s.elapsed_time(e))
     nbytes = 2 * n * 2
     peak, _ = hbm_peak()
-    med = statistics.median(times)
-    print(json.dumps({"workload": "torch copy_ of [268435456] bf16 (512 MB read + 512 MB "
-                                  "written per call)", "bytes": nbytes, "steps": args.steps,
-                      "median_us": med * 1e3, "min_us": min(times) * 1e3,
-                      "GB_s": nbytes / (med * 1e-3) / 1e9,
-                      "GB_s_best": nbytes / (min(times) * 1e-3) / 1e9,
-                      "of_measured_peak": nbytes / (med * 1e-3) / 1e9 / peak,
-                      "clocks": clk.summary(), "gpu_launches": 0}), flush=True)
+    calls = {"copy_": lambda: b.copy_(a), "mul_by_one_kernel": lambda: torch.mul(a, 1.0, out=b)}
+    out = {}
+    with ClockSampler(0) as clk:
+        for name, fn in calls.items():
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            times = []
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(args.steps):
+                s.record()
+                fn()
+                e.record()
+                torch.cuda.synchronize()
+                times.append(s.elapsed_time(e))
+            med = statistics.median(times)
+            out[name] = {"median_us": med * 1e3, "min_us": min(times) * 1e3,
+                         "GB_s": nbytes / (med * 1e-3) / 1e9,
+                         "GB_s_best": nbytes / (min(times) * 1e-3) / 1e9,
+                         "of_measured_peak": nbytes / (med * 1e-3) / 1e9 / peak}
+    print(json.dumps({"workload": "copy of [268435456] bf16 (512 MB read + 512 MB written per "
+                                  "call)", "bytes": nbytes, "steps": args.steps,
+                      "results": out, "clocks": clk.summary(), "gpu_launches": 0}), flush=True)
     return 0
 
 

@@ -77,6 +77,37 @@ __host__ __device__ constexpr int streamed_operands() {
   return OP == OP_MOD ? (MFULL ? 3 : 1) : OP == OP_RGA ? 2 : (2 + (GFULL ? 1 : 0) + (MFULL ? 2 : 0));
 }
 
+// The fast statistic's row sums of a group of RC rows over the warp: the
+// rows are first spread over lane groups (a transpose-reduce: each step
+// halves the rows a lane carries and exchanges the other half), then each
+// group finishes with a butterfly, so RC rows cost about as many shuffles as
+// one.  Returns the sum of row (lane >> (5 - log2 RC)) in every lane.
+template <int RC>
+__device__ __forceinline__ float warp_sum_rows(const float (&v)[RC]) {
+  const int lane = threadIdx.x & 31;
+  float z;
+  if constexpr (RC == 1) {
+    z = v[0];
+  } else if constexpr (RC == 2) {
+    const bool hi = lane & 16;
+    const float send = hi ? v[0] : v[1];
+    const float keep = hi ? v[1] : v[0];
+    z = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 16));
+  } else {
+    static_assert(RC == 4, "rows per group: 1, 2 or 4");
+    const bool b4 = lane & 16, b3 = lane & 8;
+    const float s0 = b4 ? v[0] : v[2], s1 = b4 ? v[1] : v[3];
+    const float k0 = b4 ? v[2] : v[0], k1 = b4 ? v[3] : v[1];
+    const float w0 = __fadd_rn(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 16));
+    const float w1 = __fadd_rn(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 16));
+    z = __fadd_rn(b3 ? w1 : w0, __shfl_xor_sync(0xFFFFFFFFu, b3 ? w0 : w1, 8));
+  }
+  constexpr int first = RC == 1 ? 16 : RC == 2 ? 8 : 4;
+#pragma unroll
+  for (int o = first; o > 0; o >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xFFFFFFFFu, z, o));
+  return z;
+}
+
 // ALLCOLS: every thread owns VPT valid granules (T * VPT * slices == nvec),
 // so no column predicate is evaluated.  A group of RC rows that lies wholly
 // inside the CTA's rows takes a path without row predicates; only the last
@@ -352,8 +383,12 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   // not have stay zero (merging a zero pair is exact)
   __shared__ __align__(16) SumPair part[2][RC][16];
   __shared__ uint64_t exact_scratch[16];  // the exact path's warp totals
+  __shared__ __align__(16) float partf[2][RC][16];  // the fast statistic's warp sums
   for (int i = tid; i < 2 * RC * 16; i += nthr)
-    if ((i & 15) >= nwarps) (&part[0][0][0])[i] = SumPair{0.0f, 0.0f};
+    if ((i & 15) >= nwarps) {
+      (&part[0][0][0])[i] = SumPair{0.0f, 0.0f};
+      (&partf[0][0][0])[i] = 0.0f;
+    }
   // the statistic's accumulators: two packed slots per thread and row
   constexpr int kNA = 2;
   using Acc = SqAcc<T, kNA>;
@@ -368,16 +403,21 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
   auto group = [&](int64_t row0, int64_t rend, auto check_tag) {
     constexpr bool CHECK = decltype(check_tag)::value;
     SumPair ss[RC];
+    [[maybe_unused]] float ssf[RC];  // the fast statistic's row sums
     // pass one: the residual (stored), the row sums of squares
     auto pass1 = [&](auto edge_tag) {
       [[maybe_unused]] constexpr bool EDGE = decltype(edge_tag)::value;
 #pragma unroll
       for (int j = 0; j < RC; ++j) {
         ss[j] = SumPair{0.0f, 0.0f};
+        ssf[j] = 0.0f;
         if (CHECK && row0 + j >= rend) continue;
         [[maybe_unused]] const int64_t rowoff = (row0 + j) * pitch - off;
         Acc acc;
         acc.zero();
+        [[maybe_unused]] F2 facc[P];  // fast: independent packed accumulators
+#pragma unroll
+        for (int i = 0; i < P; ++i) facc[i] = f2(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           if (!cval[k]) continue;
@@ -409,7 +449,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
               if constexpr (EX)
                 acc.add_pair(i % kNA, x[i]);
               else
-                acc.add_pair_fast(i % kNA, x[i]);
+                facc[i] = f2_fma(x[i], x[i], facc[i]);
             }
           }
         }
@@ -417,7 +457,11 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
           if constexpr (EX)
             ss[j] = acc.total();
           else
-            ss[j] = SumPair{acc.fast_total(), 0.0f};
+          {
+#pragma unroll
+            for (int i = 1; i < P; ++i) facc[0] = f2_add(facc[0], facc[i]);
+            ssf[j] = __fadd_rn(f2_lo(facc[0]), f2_hi(facc[0]));
+          }
         }
       }
     };
@@ -433,22 +477,39 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
     }
 
     if constexpr (kReduce) {
-      // row pairs: merged over the warp, then over the warps (lane l of
-      // every warp takes warp l % 16's pair, a 16-lane butterfly merges them)
-#pragma unroll
-      for (int j = 0; j < RC; ++j) {
-        // the fast statistic: plain fp32 sums, the same butterflies
-        const SumPair w = EX ? warp_merge(ss[j]) : SumPair{warp_sum(ss[j].h), 0.0f};
-        if (lane == 0) part[buf][j][warp] = w;
-      }
-      __syncthreads();
       float rr[RC];
+      if constexpr (!EX) {
+        // the fast statistic: the RC rows spread over lane groups of the warp,
+        // then the warps' sums -- lane l finishes row l % RC with a tree of
+        // 16-byte loads and broadcasts it
+        const float w = warp_sum_rows<RC>(ssf);
+        constexpr int grp_lanes = 32 / RC;
+        if ((lane & (grp_lanes - 1)) == 0) partf[buf][lane / grp_lanes][warp] = w;
+        __syncthreads();
+        const int jr = lane % RC;
+        const float4* pp = reinterpret_cast<const float4*>(&partf[buf][jr][0]);
+        const float4 p0 = pp[0], p1 = pp[1];
+        float tot = __fadd_rn(__fadd_rn(__fadd_rn(p0.x, p0.y), __fadd_rn(p0.z, p0.w)),
+                              __fadd_rn(__fadd_rn(p1.x, p1.y), __fadd_rn(p1.z, p1.w)));
+        if (nwarps > 8) {  // uniform
+          const float4 p2 = pp[2], p3 = pp[3];
+          tot = __fadd_rn(tot, __fadd_rn(__fadd_rn(__fadd_rn(p2.x, p2.y), __fadd_rn(p2.z, p2.w)),
+                                         __fadd_rn(__fadd_rn(p3.x, p3.y), __fadd_rn(p3.z, p3.w))));
+        }
+        const float rl = fast_inverse_rms(tot, a.d_f, a.inv_d, a.eps);
 #pragma unroll
-      for (int j = 0; j < RC; ++j) {
-        if constexpr (!EX) {
-          rr[j] = fast_inverse_rms(group_sum<16>(part[buf][j][lane & 15].h), a.d_f, a.inv_d,
-                                   a.eps);
-        } else {
+        for (int j = 0; j < RC; ++j) rr[j] = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
+      } else {
+        // row pairs: merged over the warp, then over the warps (lane l of
+        // every warp takes warp l % 16's pair, a 16-lane butterfly merges them)
+#pragma unroll
+        for (int j = 0; j < RC; ++j) {
+          const SumPair w = warp_merge(ss[j]);
+          if (lane == 0) part[buf][j][warp] = w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < RC; ++j) {
           const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
           // the exact path reads the row back from this thread's ring slots
           const uint32_t sl0 = stage + j * JS + kX * OS;

@@ -96,8 +96,10 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
 
   __shared__ SumPair part[2][R][16];       // per-warp row pairs (<= 16 warps)
   __shared__ uint64_t exact_scratch[16];   // the exact path's warp totals
+  __shared__ float partf[2][R][16];        // the fast statistic's warp sums
   for (int i = tid; i < 2 * R * 16; i += nthr)
     if ((i & 15) >= (nthr >> 5)) (&part[0][0][0])[i] = SumPair{0.0f, 0.0f};
+  const int nwarps = nthr >> 5;
   // the statistic: four scalar (hi, lo) accumulators per thread and row,
   // element e of the thread's row part into accumulator e % 4
   using Acc = Sq32<4>;
@@ -147,10 +149,12 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
     }
 
     SumPair ss[R];
+    [[maybe_unused]] float ssf[R];  // the fast statistic: one FMA chain per row
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       Acc acc;
       acc.zero();
+      ssf[j] = 0.0f;
       const int64_t rowoff = (r0 + j) * pitch;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -173,27 +177,33 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
             if constexpr (EX)
               acc.add((k * N + e) % 4, f[e]);
             else
-              acc.add_fast((k * N + e) % 4, f[e]);
+              ssf[j] = __fmaf_rn(f[e], f[e], ssf[j]);
           }
         }
       }
-      ss[j] = EX ? acc.total() : SumPair{acc.fast_total(), 0.0f};
+      if constexpr (EX) ss[j] = acc.total();
     }
     if constexpr (kReduce) {
       // row pairs over the warp, then over the warps
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        // the fast statistic: plain fp32 sums over the same butterflies
-        const SumPair w = EX ? warp_merge(ss[j]) : SumPair{warp_sum(ss[j].h), 0.0f};
-        if (lane == 0) part[buf][j][warp] = w;
+        if constexpr (EX) {
+          const SumPair w = warp_merge(ss[j]);
+          if (lane == 0) part[buf][j][warp] = w;
+        } else {
+          const float w = warp_sum(ssf[j]);
+          if (lane == 0) partf[buf][j][warp] = w;
+        }
       }
       __syncthreads();
       float rinv[R];
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         if constexpr (!EX) {
-          rinv[j] = fast_inverse_rms(group_sum<16>(part[buf][j][lane & 15].h), a.d_f, a.inv_d,
-                                     a.eps);
+          // the fast statistic: the warps' sums in order
+          float tot = 0.0f;
+          for (int w = 0; w < nwarps; ++w) tot = __fadd_rn(tot, partf[buf][j][w]);
+          rinv[j] = fast_inverse_rms(tot, a.d_f, a.inv_d, a.eps);
         } else {
           const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
           auto each = [=](auto&& f) {
@@ -422,7 +432,11 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
 #else
   if (vb >= 16) {
 #endif
-    if constexpr (OP != OP_RGA) {  // one warp per row when the row fits its registers
+    // two warps per row (dit_wrow.cuh) when the row fits their registers;
+    // not for the fused op with a full gate: a third staged operand (96 KB of
+    // stages) leaves one CTA per SM, and the CTA-per-row kernel was faster
+    // ([1,8160,4096] bf16, L2-flushed: 53.8 vs 65.9 us)
+    if constexpr (OP != OP_RGA && !(OP == OP_FUSED && GFULL)) {
       const cudaError_t w = with_statistic<OP>(a.exact, [&](auto ex) {
         return launch_wrow<OP, GFULL, MFULL, false, decltype(ex)::value>(dev, dtype, a, B, stream);
       });

@@ -4,15 +4,15 @@
 // instantiated once for each, so neither carries the other's registers.
 //
 // The fast statistic (default).  S = the squares summed in fp32 -- one FMA
-// per element into a few per-thread accumulators, those added in a tree,
-// then butterflies over the warp (and the row's warps or the CTA's 16-leaf
-// tree); the long-row kernel merges its per-vector sums as (hi, lo) pairs,
+// per element into one or a few per-thread accumulators, those added in a
+// tree, then butterflies over the warp and a sum over the row's warps; the
+// long-row kernel merges its per-vector sums as (hi, lo) pairs,
 // since a thread there may take thousands of vectors.  ms = S * fl(1/D) with
 // one correction from the exact remainder S - q D (an FMA); v = fl(ms + eps);
 // r = rsqrtf(v) and one Newton-Raphson step (fast_inverse_rms).  On
 // non-negative terms S's relative error is at most (roundings on the longest
-// path) * u, u = 2^-24 -- at most 17 u in these kernels -- and r's then at
-// most about 11 u: the modulated value is within 2^-18 of max(|t|, |y|) of
+// path) * u, u = 2^-24 -- at most 29 u in these kernels -- and r's then at
+// most about 17 u: the modulated value is within 2^-18 of max(|t|, |y|) of
 // the correctly rounded one, far below a bf16/fp16 ulp unless the final add
 // cancels.  The sum's order depends on the kernel, so two kernels (say, for a
 // row in an aligned tensor and the same row in a sub-view off a 16-byte

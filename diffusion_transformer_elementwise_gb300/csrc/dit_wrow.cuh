@@ -357,6 +357,7 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
   a.nvec = row_bytes / 16;
   const int64_t need = (a.nvec + 63) / 64;
   if (need > kWrowMaxNG) return cudaErrorNotSupported;
+  static_assert(!(OP == OP_FUSED && GFULL), "the fused op with a full gate is not instantiated");
   constexpr int NV = wrow_vectors<OP, GFULL, MFULL>();
   constexpr int NS = wrow_staged<OP, GFULL>();
   const size_t vbytes = (size_t)NV * (size_t)a.nvec * 16 * (dtype == 2 ? 1 : 2);
@@ -379,7 +380,12 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       const int64_t wave = (int64_t)dev.sm_count * resident_ctas(dev, (const void*)kern, block, smem);
       const int64_t most = (a.L + teams - 1) / teams;  // CTAs per batch, one row per team
       int64_t per_batch;
-      if (B * a.L <= 8 * wave * teams) {
+      const bool small = B * a.L <= 8 * wave * teams;
+      // the fused op takes this kernel on large tensors only: on smaller ones
+      // the CTA-per-row kernel, with three CTAs per SM to its two, was faster
+      // ([1,4608,3072] bf16, L2-flushed: 25.3 vs 27.1 us)
+      if (OP == OP_FUSED && small) return cudaErrorNotSupported;
+      if (small) {
         // at most 8 rows per team in one wave: exactly one wave (fewer rows
         // than teams: one row per team), the rows split statically
         per_batch = std::min(most, (wave + B - 1) / B);
@@ -413,13 +419,9 @@ extern DIT_WROW_SIG(OP_MOD, false, false, false, false);
 extern DIT_WROW_SIG(OP_MOD, false, true, false, false);
 extern DIT_WROW_SIG(OP_FUSED, false, false, false, false);
 extern DIT_WROW_SIG(OP_FUSED, false, true, false, false);
-extern DIT_WROW_SIG(OP_FUSED, true, false, false, false);
-extern DIT_WROW_SIG(OP_FUSED, true, true, false, false);
 extern DIT_WROW_SIG(OP_MOD, false, false, false, true);
 extern DIT_WROW_SIG(OP_MOD, false, true, false, true);
 extern DIT_WROW_SIG(OP_FUSED, false, false, false, true);
 extern DIT_WROW_SIG(OP_FUSED, false, true, false, true);
-extern DIT_WROW_SIG(OP_FUSED, true, false, false, true);
-extern DIT_WROW_SIG(OP_FUSED, true, true, false, true);
 
 }  // namespace dit

@@ -8,7 +8,10 @@
 // slot in the staged kernels, held in registers in the register kernel -- so
 // the row is read from HBM once (hidden, update, gate) and written twice
 // (residual, modulated output).
-// Kernels: dit_rows.cuh (OP_FUSED).
+// Kernels (chosen in dit_rows.cuh): two warps per row on large tensors with
+// a [B, 1, D] gate (dit_wrow.cuh), the staged CTA-per-row kernel otherwise
+// (dit_pipe.cuh), the register and two-pass kernels for unaligned or long
+// rows.
 #include "dit_rows.cuh"
 
 namespace dit {

@@ -5,8 +5,10 @@
 // _ltx2_rms_norm_modulate) and section "implementation breakdown", item 2
 // (weightless RMSNormNoWeight, the whole expression in one launch).
 //
-// 16-byte aligned rows: the staged CTA-per-row kernel (dit_pipe.cuh);
-// unaligned rows: the register kernel; long rows: the two-pass kernel
+// 16-byte aligned rows of up to 8 KB: two warps per row (dit_wrow.cuh);
+// other 16-byte aligned rows, the E4M3 output and the grouped launch: the
+// staged CTA-per-row kernel (dit_pipe.cuh); unaligned rows: the phased staged
+// kernel or the register kernel; long rows: the two-pass kernel
 // (dit_rows.cuh).
 #include "dit_rows.cuh"
 

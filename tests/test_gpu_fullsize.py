@@ -6,8 +6,10 @@ and properties that hold at any size are checked on every element:
 * residual gate: equals torch's own fp32 multiply then fp32 add, rounded to
   the dtype (two separately rounded eager kernels: the same arithmetic);
 * modulation: scale = -1 gives exactly the shift everywhere;
-* fused: the residual equals the residual gate and the modulated output
-  equals the modulation of that residual, bitwise, over the whole tensor.
+* fused: the residual equals the residual gate, and the modulated output
+  equals the modulation of that residual over the whole tensor -- bitwise
+  under the exact statistic; under the fast one (whose sum order is the
+  kernel's) within 2^-5 absolute, on fewer than 1% of the elements.
 
 Shapes: sglang PR #29361, B200 kernel benchmark table (ltx2_bcast_s32640_c4096,
 ltx2_full_s8160_c4096, ideogram4_bcast_s4096_c4608, flux2_bcast_s4608_c3072),
@@ -105,7 +107,15 @@ def test_workload(orc, statistic, w):
     assert torch.equal(res, out)
     m2 = dit.rmsnorm_modulate(res, sc, sh, EPS)
     torch.cuda.synchronize()
-    assert torch.equal(mod, m2)
+    if statistic == "exact":
+        # one correctly rounded statistic: every kernel gives the same bits
+        assert torch.equal(mod, m2)
+    else:
+        # the fast statistic's sum order is the kernel's (the fused op and the
+        # modulation may take different kernels): the last bit may differ
+        d = (mod.float() - m2.float()).abs()
+        assert float(d.max()) <= 2.0 ** -5, float(d.max())
+        assert int((d > 0).sum()) <= mod.numel() // 100
     rref, mref2, t2 = oracle_fused(orc, hs, us, gs, scs, shs, dtype, gl, ml, EPS, with_t=True)
     assert_bit_exact(gather(res, idx, L), rref)
     print(name, "fused", modulation_stats(gather(mod, idx, L), mref2, t2.numpy(), dtype, name))

@@ -125,14 +125,18 @@ def test_grouped_in_place_and_adaln_tables(orc):
 
 
 def test_grouped_video_equals_single_call():
-    """The widest problem runs with its own block size, so its arithmetic is
-    that of the single call: bitwise equal outputs."""
+    """The grouped launch gives the widest problem the same outputs as its
+    single call, bit for bit -- under the exact statistic, which every kernel
+    computes to the same bits (the fast statistic's sum order is the
+    kernel's, and the single call may take the two-warp kernel)."""
     dtype = "bf16"
     video, audio = (_fused_inputs(B, L, D, dtype, "bcast", "bcast", f"grp-eq{i}")
                     for i, (B, L, D) in enumerate(SETS["video_audio"]))
     vg = tuple(t.cuda() for t in video)
-    (rg, mg), _ = dit.gate_add_rmsnorm_modulate_grouped([vg, tuple(t.cuda() for t in audio)], EPS)
-    rs, ms = dit.gate_add_rmsnorm_modulate(*vg, EPS)
+    with dit.statistic("exact"):
+        (rg, mg), _ = dit.gate_add_rmsnorm_modulate_grouped([vg, tuple(t.cuda() for t in audio)],
+                                                            EPS)
+        rs, ms = dit.gate_add_rmsnorm_modulate(*vg, EPS)
     torch.cuda.synchronize()
     assert torch.equal(rg.view(torch.int16), rs.view(torch.int16))
     assert torch.equal(mg.view(torch.int16), ms.view(torch.int16))
