@@ -94,7 +94,12 @@ def modulation_stats(gpu: torch.Tensor, ref: torch.Tensor, t: np.ndarray, dtype:
                            f"(max {int(d.max())} ulp), first {idx[:5]}: gpu {gv[idx[:5]]} "
                            f"oracle {rv[idx[:5]]} t {tt[idx[:5]]}")
     denom = np.sqrt(np.sum(rv * rv))
+    pos = scale > 0
+    err_u = float((diff[pos] / scale[pos]).max()) / 2.0 ** -24 if pos.any() else 0.0
     return {
+        # |gpu - oracle| / max(|t|, |y|) in units of 2^-24 (the fp32
+        # criterion's measure: 2^-18 is 64 of them)
+        "max_err_u": err_u,
         "statistic": "exact" if exact else "fast",
         "max_ulp": int(d.max()) if d.size else 0,
         "not_bit_exact": int(np.count_nonzero(d)),
