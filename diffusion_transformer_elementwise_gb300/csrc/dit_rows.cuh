@@ -419,6 +419,15 @@ cudaError_t launch_row_op(const DeviceInfo& dev, int dtype, int vb, RowArgs a, i
                           cudaStream_t stream) {
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
 #ifndef DIT_ROWS_IN_REGISTERS
+  if constexpr (OP != OP_RGA && !GFULL && !MFULL) {
+    // the modulating ops on rows of other pitches in 16-byte aligned tensors,
+    // with the fast statistic: two warps per row, by phase
+    if (vb < 16 && !a.exact && streamed_bases_aligned<OP, GFULL, MFULL>(a)) {
+      const cudaError_t w =
+          launch_wrow<OP, GFULL, MFULL, false, false>(dev, dtype, a, B, stream, true);
+      if (w != cudaErrorNotSupported) return w;
+    }
+  }
   if (vb < 16 && (OP == OP_RGA || vb < 8) && streamed_bases_aligned<OP, GFULL, MFULL>(a)) {
     const cudaError_t e = with_statistic<OP>(a.exact, [&](auto ex) {
       return launch_pipe<OP, GFULL, MFULL, false, decltype(ex)::value>(dev, dtype, a, B, stream,

@@ -1,5 +1,6 @@
 // dit_wrow.cuh -- the modulation and the fused op with two warps per row
-// (sm_103a; rows whose pitch and tensors are 16-byte aligned, up to 16 KB).
+// (sm_103a; rows of up to 8 KB in 16-byte aligned tensors, whose pitch is a
+// multiple of 16 bytes -- or any pitch, by phase, with the fast statistic).
 //
 // A row belongs to a team of two warps; lane l of member m holds 16-byte
 // granules l + 32 m + 64 j, j < NG, in registers, so every warp-wide access is
@@ -103,7 +104,20 @@ struct TeamRow {
 // EX: the exact row statistic (dit_set_statistic); otherwise the fast one.
 // Each is its own instantiation, so the fast kernel carries none of the
 // exact path's registers.
-template <int OP, class T, int NG, bool GFULL, bool MFULL, bool Q8, bool EX>
+//
+// PH (phased rows; the fast statistic, [B, 1, D] operands only): the row
+// pitch is not a multiple of 16 bytes but every streamed tensor starts on a
+// 16-byte boundary.  Row r then starts (r * pitch) mod 16 bytes past a
+// boundary, a value of period P = 16 / gcd(pitch mod 16, 16) rows, so the
+// CTAs of a batch are split into P phase classes: class c takes rows
+// c, c + P, c + 2P, ..., all at one offset `off`.  A team copies a row's
+// 16-byte granules from the boundary below its start (the last row's last
+// granule only up to the tensors' end); a row's first and last granule hold
+// elements of its neighbours, masked out of the sum and never stored (the
+// row's own elements of them are stored one by one).  The CTA's vector
+// planes are written at the same offset, so granule k of the window meets
+// the vector columns of its elements.
+template <int OP, class T, int NG, bool GFULL, bool MFULL, bool Q8, bool EX, bool PH = false>
 __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wrow_kernel(RowArgs a) {
   using G = Granule<T>;
   constexpr int P = G::P;     // fp32 pairs per granule
@@ -118,6 +132,9 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
   constexpr int kTerms = (NG + R - 1) / R;
   constexpr int kLevels = Log2<Acc::kScalar>::value + 5 + 1;  // thread, warp, team
   constexpr uint32_t kStage = NG * 512;  // bytes of one staged operand per warp
+  constexpr int ES = (int)sizeof(T);
+  constexpr int EPG = 16 / ES;  // elements per granule
+  static_assert(!PH || (!EX && !Q8 && !MFULL && !GFULL), "phased rows: fast statistic, [B,1,D]");
 
   extern __shared__ float4 vsm[];  // [NV][NPL][ngr] vectors, then [W][NS][NG * 32] stages
   __shared__ SumPair xch_pair[2][kWrowWarps / 2][2];  // the team's pair exchange, by row parity
@@ -125,7 +142,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int team = warp >> 1, m = warp & 1;
   const int nteams = blockDim.x >> 6;
-  const int64_t ngr = a.nvec;  // granules per row
+  const int64_t ngr = a.nvec;  // granules per row (phased: at most, over the offsets)
   const uint32_t pls = (uint32_t)ngr * 16;  // bytes per vector plane
   // this lane's granules: l + 32 m + 64 j
   const uint32_t lg = (uint32_t)(lane + 32 * m);
@@ -154,8 +171,16 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
   const int64_t cpb = a.gpb;
   const int64_t slot = (int64_t)blockIdx.x / cpb, kc = (int64_t)blockIdx.x - slot * cpb;
   const int64_t nbatch = a.rows / (a.L > 0 ? a.L : 1);
-  const int64_t pitch = ngr * 16;
-  const int64_t rstep = cpb * nteams;
+  const int64_t pitch = a.D * (int64_t)ES;
+  // phased rows: this CTA's phase class c of the period (cpb is a multiple
+  // of it), kq its index among the class's CTAs
+  int64_t period = 1;
+  if constexpr (PH) {
+    const int64_t mm = pitch & 15;
+    period = mm ? 16 / (mm & -mm) : 1;
+  }
+  const int64_t phase = kc % period, kq = kc / period;
+  const int64_t rstep = cpb * nteams;  // = period * (cpb / period) * nteams
   float qinv_s = 1.0f;
   if constexpr (Q8) qinv_s = __frcp_rn(__ldg(a.qscale));
   const F2 qinv = f2(qinv_s, qinv_s);
@@ -163,29 +188,79 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
   int par = 0;
 
   for (int64_t b = slot; b < nbatch; b += a.ngroups) {
+    // phased rows: the offset of this CTA's rows past a 16-byte boundary,
+    // the granules of a row's window, and this lane's edge bounds (element
+    // slots [lo, hi) of a granule belong to the row)
+    int off = 0;
+    int64_t ngw = ngr;
+    if constexpr (PH) {
+      off = (int)(((b * a.L + phase) * pitch) & 15);
+      ngw = (off + pitch + 15) >> 4;
+#pragma unroll
+      for (int j = 0; j < NG; ++j) val[j] = lg + 64 * j < ngw;
+    }
+    // (only granule 0 and granule ngw - 1 of a row are partial: this lane
+    // owns the first when lg == 0, the last as its granule last_j)
+    [[maybe_unused]] const bool first = PH && lg == 0;
+    [[maybe_unused]] const int last_j = PH && (ngw - 1) % 64 == lg ? (int)((ngw - 1) / 64) : -1;
+    [[maybe_unused]] const int lo_first = off / ES;
+    [[maybe_unused]] const int hi_last = (int)((off + pitch - 16 * (ngw - 1)) / ES);
+    auto edge = [&](int j) { return PH && ((j == 0 && first) || j == last_j); };
+    auto lo_of = [&](int j) { return j == 0 && first ? lo_first : 0; };
+    auto hi_of = [&](int j) { return j == last_j ? hi_last : EPG; };
+
     // copy this warp's half of row l into the stage (an empty group past the end)
     auto prefetch = [&](int64_t l) {
       if (l < a.L) {
-        const int64_t rowoff = (b * a.L + l) * pitch + lg * 16;
+        const int64_t row = b * a.L + l;
+        const int64_t rowoff = row * pitch - off + lg * 16;
+        // phased rows: the last row's last granule may run past the end
+        const bool tail = PH && row == a.rows - 1;
 #pragma unroll
         for (int op = 0; op < NS; ++op)
 #pragma unroll
-          for (int j = 0; j < NG; ++j)
-            if (val[j]) cp_async16(stage[op] + j * 512, src[op] + rowoff + j * 1024);
+          for (int j = 0; j < NG; ++j) {
+            if (!val[j]) continue;
+            if (tail) {
+              const int64_t left = a.rows * pitch - (rowoff + j * 1024);
+              if (left < 16) {
+                cp_async16_part(stage[op] + j * 512, src[op] + rowoff + j * 1024, (uint32_t)left);
+                continue;
+              }
+            }
+            cp_async16(stage[op] + j * 512, src[op] + rowoff + j * 1024);
+          }
       }
       cp_async_commit();
     };
 
-    int64_t l = kc * nteams + team;
+    int64_t l = PH ? phase + period * (kq * nteams + team) : kc * nteams + team;
     prefetch(l);  // in flight while the vectors load
     if constexpr (NV > 0) {
       __syncthreads();  // the previous batch's vectors are no longer read
-      for (int64_t g = threadIdx.x; g < ngr; g += blockDim.x) {
+      for (int64_t g = threadIdx.x; g < ngw; g += blockDim.x) {
         const int64_t vo = b * a.vstride + g * 16;
         int v = 0;
         auto put = [&](const void* vsrc, bool plus_one) {
           F2 f[P];
-          G::widen(ld_bcast<16>((const char*)vsrc + vo), f);
+          if constexpr (PH) {
+            // element by element, at the rows' offset (slots outside the row: 0)
+            const int64_t e0 = (g * 16 - off) / ES;  // the row element at slot 0
+            float e[EPG];
+#pragma unroll
+            for (int i = 0; i < EPG; ++i) {
+              e[i] = 0.0f;
+              if (e0 + i >= 0 && e0 + i < a.D) {
+                float w[1];
+                Vec<T, ES>::widen(ld_bcast<ES>((const char*)vsrc + b * a.vstride + (e0 + i) * ES), w);
+                e[i] = w[0];
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < P; ++i) f[i] = f2(e[2 * i], e[2 * i + 1]);
+          } else {
+            G::widen(ld_bcast<16>((const char*)vsrc + vo), f);
+          }
           if (plus_one) {
 #pragma unroll
             for (int i = 0; i < P; ++i) f[i] = f2_add(f2(1.0f, 1.0f), f[i]);
@@ -207,7 +282,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
 
     for (; l < a.L; l += rstep) {
       const int64_t row = b * a.L + l;
-      const int64_t rowoff = row * pitch + lg * 16;
+      const int64_t rowoff = row * pitch - off + lg * 16;
       cp_async_wait<0>();  // this lane's copies of row l have landed
       Raw<16> xr[NG];
       if constexpr (OP == OP_FUSED) {
@@ -232,7 +307,10 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
 #pragma unroll
           for (int i = 0; i < P; ++i) x[i] = residual_gate2<T>(h[i], u[i], g[i]);
           xr[j] = G::narrow(x);
-          st_stream<16>(res + j * 1024, xr[j]);
+          if (edge(j))
+            store_part<T>(res + j * 1024, xr[j], lo_of(j), hi_of(j));
+          else
+            st_stream<16>(res + j * 1024, xr[j]);
         }
         prefetch(l + rstep);  // the stage has been read
       } else {
@@ -289,6 +367,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
           if (!val[j]) continue;
           F2 x[P];
           G::widen(xr[j], x);
+          if (edge(j)) mask_part<T>(x, lo_of(j), hi_of(j));
 #pragma unroll
           for (int i = 0; i < P; ++i) acc.add_pair_fast((j % R) * P + i, x[i]);
         }
@@ -331,6 +410,8 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
         for (int i = 0; i < P; ++i) y[i] = modulate2(f2_mul(x[i], r2), one[i], sh[i]);
         if constexpr (Q8)
           st_stream<2 * P>(mout + j * 64 * QB, quantise_e4m3<P>(y, qinv));
+        else if (edge(j))
+          store_part<T>(mout + j * 1024, G::narrow(y), lo_of(j), hi_of(j));
         else
           st_stream<16>(mout + j * 1024, G::narrow(y));
       }
@@ -350,11 +431,19 @@ constexpr int kWrowMaxNG = 8;
 // does not fit it (more than 64 * kWrowMaxNG granules, or the stages and the
 // vectors do not fit shared memory) -- the caller then takes the CTA-per-row
 // kernel.
+// phased: rows whose pitch is not a multiple of 16 bytes, every streamed
+// tensor 16-byte aligned (the fast statistic and [B, 1, D] operands only;
+// cudaErrorNotSupported otherwise).
 template <int OP, bool GFULL, bool MFULL, bool Q8, bool EX>
 cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool phased = false) {
+  constexpr bool kPhasedOk = !EX && !Q8 && !MFULL && !GFULL;
+  if (phased && !kPhasedOk) return cudaErrorNotSupported;
   const int64_t row_bytes = a.D * (dtype == 2 ? 4 : 2);
-  a.nvec = row_bytes / 16;
+  // granules per row (phased: at most, over the rows' offsets)
+  a.nvec = phased ? (row_bytes + 30) / 16 : row_bytes / 16;
+  const int64_t mm = row_bytes & 15;
+  const int64_t period = phased && mm ? 16 / (mm & -mm) : 1;
   const int64_t need = (a.nvec + 63) / 64;
   if (need > kWrowMaxNG) return cudaErrorNotSupported;
   static_assert(!(OP == OP_FUSED && GFULL), "the fused op with a full gate is not instantiated");
@@ -366,11 +455,15 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
     using T = typename decltype(tt)::type;
     auto go = [&](auto ng) -> cudaError_t {
       constexpr int NG = decltype(ng)::value;
-      auto kern = wrow_kernel<OP, T, NG, GFULL, MFULL, Q8, EX>;
+      auto kern = wrow_kernel<OP, T, NG, GFULL, MFULL, Q8, EX, false>;
+      if constexpr (kPhasedOk)
+        if (phased) kern = wrow_kernel<OP, T, NG, GFULL, MFULL, Q8, EX, true>;
       const size_t smem = vbytes + (size_t)kWrowWarps * NS * NG * 512;
       if (smem > limit) return cudaErrorNotSupported;
-      static std::atomic<int> opted[kOptinDevices];
-      const cudaError_t e = allow_dynamic_smem((const void*)kern, dev, smem, opted);
+      // one opt-in record per kernel (the phased kernel is another function)
+      static std::atomic<int> opted_plain[kOptinDevices], opted_phased[kOptinDevices];
+      const cudaError_t e =
+          allow_dynamic_smem((const void*)kern, dev, smem, phased ? opted_phased : opted_plain);
       if (e != cudaSuccess) return e;
       const int block = kWrowWarps * 32;
       const int teams = kWrowWarps / 2;
@@ -384,7 +477,7 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       // the fused op takes this kernel on large tensors only: on smaller ones
       // the CTA-per-row kernel, with three CTAs per SM to its two, was faster
       // ([1,4608,3072] bf16, L2-flushed: 25.3 vs 27.1 us)
-      if (OP == OP_FUSED && small) return cudaErrorNotSupported;
+      if (OP == OP_FUSED && small && !phased) return cudaErrorNotSupported;
       if (small) {
         // at most 8 rows per team in one wave: exactly one wave (fewer rows
         // than teams: one row per team), the rows split statically
@@ -393,11 +486,13 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
         const int64_t rows_per_team = OP == OP_FUSED ? 2 : 4;
         per_batch = (a.L + teams * rows_per_team - 1) / (teams * rows_per_team);
       }
+      per_batch = (per_batch + period - 1) / period * period;  // whole phase classes
       int64_t G = B * per_batch;
       if (G > 64 * wave) G = 64 * wave;  // very many batches: CTAs stride over them
       if (G < 1) G = 1;
       const int64_t nb = B < G ? B : G;  // batches served at once
-      const int64_t cpb = G / nb;         // CTAs per batch
+      int64_t cpb = G / nb / period * period;  // CTAs per batch, a multiple of the period
+      if (cpb < period) cpb = period;
       a.gpb = cpb;
       a.ngroups = nb;
       const int64_t grid = nb * cpb;
@@ -414,7 +509,7 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
 // Instantiated once, in k_instances.cu.
 #define DIT_WROW_SIG(o, g, m, q, e)                                                       \
   template cudaError_t launch_wrow<o, g, m, q, e>(const DeviceInfo&, int, RowArgs, int64_t, \
-                                                  cudaStream_t)
+                                                  cudaStream_t, bool)
 extern DIT_WROW_SIG(OP_MOD, false, false, false, false);
 extern DIT_WROW_SIG(OP_MOD, false, true, false, false);
 extern DIT_WROW_SIG(OP_FUSED, false, false, false, false);
