@@ -518,5 +518,9 @@ extern DIT_WROW_SIG(OP_MOD, false, false, false, true);
 extern DIT_WROW_SIG(OP_MOD, false, true, false, true);
 extern DIT_WROW_SIG(OP_FUSED, false, false, false, true);
 extern DIT_WROW_SIG(OP_FUSED, false, true, false, true);
+extern DIT_WROW_SIG(OP_MOD, false, false, true, true);
+extern DIT_WROW_SIG(OP_MOD, false, true, true, true);
+extern DIT_WROW_SIG(OP_FUSED, false, false, true, true);
+extern DIT_WROW_SIG(OP_FUSED, false, true, true, true);
 
 }  // namespace dit

@@ -32,6 +32,14 @@ cudaError_t launch_fused_fp8(const DeviceInfo& dev, int dtype, bool gate_full, b
     if (gate_full)
       return mod_full ? launch_pipe<OP_FUSED, true, true, true, EX>(dev, dtype, a, B, stream)
                       : launch_pipe<OP_FUSED, true, false, true, EX>(dev, dtype, a, B, stream);
+    if constexpr (EX) {
+      // the exact statistic on large tensors: two warps per row (the staged
+      // kernel's exact instantiation for E4M3 spills)
+      const cudaError_t w =
+          mod_full ? launch_wrow<OP_FUSED, false, true, true, true>(dev, dtype, a, B, stream)
+                   : launch_wrow<OP_FUSED, false, false, true, true>(dev, dtype, a, B, stream);
+      if (w != cudaErrorNotSupported) return w;
+    }
     return mod_full ? launch_pipe<OP_FUSED, false, true, true, EX>(dev, dtype, a, B, stream)
                     : launch_pipe<OP_FUSED, false, false, true, EX>(dev, dtype, a, B, stream);
   });

@@ -97,6 +97,14 @@ DIT_GROUPED_SIG(OP_FUSED, false, true, true);
 #elif DIT_INSTANCE == 37
 DIT_GROUPED_SIG(OP_FUSED, true, false, true);
 DIT_GROUPED_SIG(OP_FUSED, true, true, true);
+#elif DIT_INSTANCE == 38
+DIT_WROW_SIG(OP_MOD, false, false, true, true);
+#elif DIT_INSTANCE == 39
+DIT_WROW_SIG(OP_MOD, false, true, true, true);
+#elif DIT_INSTANCE == 40
+DIT_WROW_SIG(OP_FUSED, false, false, true, true);
+#elif DIT_INSTANCE == 41
+DIT_WROW_SIG(OP_FUSED, false, true, true, true);
 #else
 #error "no such instance group"
 #endif
