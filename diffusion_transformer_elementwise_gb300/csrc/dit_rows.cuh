@@ -97,6 +97,7 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
   __shared__ SumPair part[2][R][16];       // per-warp row pairs (<= 16 warps)
   __shared__ uint64_t exact_scratch[16];   // the exact path's warp totals
   __shared__ float partf[2][R][16];        // the fast statistic's warp sums
+  __shared__ float part_scaled[16];         // and its rescaled sums (rare)
   for (int i = tid; i < 2 * R * 16; i += nthr)
     if ((i & 15) >= (nthr >> 5)) (&part[0][0][0])[i] = SumPair{0.0f, 0.0f};
   const int nwarps = nthr >> 5;
@@ -204,6 +205,29 @@ __global__ void DIT_ROW_BOUNDS(VB) row_kernel(RowArgs a) {
           float tot = 0.0f;
           for (int w = 0; w < nwarps; ++w) tot = __fadd_rn(tot, partf[buf][j][w]);
           rinv[j] = fast_inverse_rms(tot, a.d_f, a.inv_d, a.eps);
+          if (rval[j] && !fast_sum_in_range(tot)) {
+            // rare, uniform over the CTA: the row's squares again, scaled
+            const float sc = fast_rescale(tot);
+            float s2 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+              if (!cval[k]) continue;
+              float x[N];
+              V::widen(xv[j][k], x);
+#pragma unroll
+              for (int e = 0; e < N; ++e) {
+                const float u0 = __fmul_rn(x[e], sc);
+                s2 = __fmaf_rn(u0, u0, s2);
+              }
+            }
+            s2 = warp_sum(s2);
+            if (lane == 0) part_scaled[warp] = s2;
+            __syncthreads();
+            float S2 = 0.0f;
+            for (int w = 0; w < nwarps; ++w) S2 = __fadd_rn(S2, part_scaled[w]);
+            __syncthreads();  // read before the next row's writes
+            rinv[j] = fast_inverse_rms_scaled(S2, sc, a.d_f, a.inv_d, a.eps);
+          }
         } else {
           const SumPair p = group_merge<16>(part[buf][j][lane & 15]);
           auto each = [=](auto&& f) {
@@ -320,10 +344,40 @@ __global__ void __launch_bounds__(1024) long_row_kernel(RowArgs a) {
       }
     };
     float rinv;
-    if constexpr (EX)
+    if constexpr (EX) {
       rinv = row_inverse_rms(p, coef, levels, a.D, a.d_f, a.eps, each, CtaRow{exact_scratch});
-    else
+    } else if (fast_sum_in_range(p.h) && !isnan(p.h)) {
       rinv = fast_inverse_rms(p.h, a.d_f, a.inv_d, a.eps);
+    } else {
+      // rare, uniform over the CTA: the row's squares again, scaled, merged
+      // as pairs like the first pass.  Here a NaN sum is not only a NaN in
+      // the row: the pair merges turn an infinite square into NaN (inf - inf
+      // in TwoSum), so infinities are counted apart and give r = 0.
+      const float sc = isnan(p.h) ? 0x1p-64f : fast_rescale(p.h);
+      SumPair s2{0.0f, 0.0f};
+      bool inf_seen = false;
+      for (int64_t v = tid; v < nvec; v += nthr) {
+        float x[N];
+        V::widen(ld_stream<VB>((const char*)src + rowoff + v * VB), x);
+        Acc acc;
+        acc.zero();
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          const bool inf = fabsf(x[e]) == __int_as_float(0x7f800000);
+          inf_seen = inf_seen || inf;
+          acc.add_fast(e % 4, inf ? 0.0f : __fmul_rn(x[e], sc));
+        }
+        s2 = merge(s2, acc.total());
+      }
+      const SumPair w2 = warp_merge(s2);
+      if (lane == 0) part[buf][warp] = w2;
+      const bool any_inf = __syncthreads_or(inf_seen) != 0;
+      const SumPair p2 = warp_merge(part[buf][lane]);
+      buf ^= 1;
+      // a NaN in the row wins (the sum of squares is NaN), then an infinity
+      rinv = isnan(p2.h) ? p2.h
+                         : any_inf ? 0.0f : fast_inverse_rms_scaled(p2.h, sc, a.d_f, a.inv_d, a.eps);
+    }
 
     // second pass: each thread re-reads exactly the vectors it handled above
     void* dst = OP == OP_FUSED ? a.out2 : a.out;

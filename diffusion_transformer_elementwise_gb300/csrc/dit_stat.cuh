@@ -632,16 +632,12 @@ __device__ __forceinline__ float rsqrt_rn(float v) {
   return __fmul_rn(__uint_as_float(yb), back);
 }
 
-// r of one row from its merged pair: the fast decision, else the exact path.
-// Uniform over the row's threads (they hold the same pair).
 // The fast statistic (the library's default): from the row's fp32 sum of
 // squares S -- each thread's squares added with one FMA each, merged in tree
 // order -- ms = S * fl(1/D) with one correction by the exact residual
 // S - q D (an FMA; the correctly rounded S / D except in rare near-halfway
 // cases), v = fl(ms + eps), and r = rsqrtf(v) refined by one Newton-Raphson
-// step.  The sum carries up to about 15 fp32 ulps of rounding in tree order,
-// the quotient one, the root about one: r is within some ten fp32 ulps of the
-// exact statistic's.
+// step.  For S in [2^-100, 2^100] (fast_sum_in_range).
 __device__ __forceinline__ float fast_inverse_rms(float S, float Df, float inv_d, float eps) {
   const float q = __fmul_rn(S, inv_d);
   const float ms = __fmaf_rn(__fmaf_rn(-q, Df, S), inv_d, q);
@@ -651,9 +647,60 @@ __device__ __forceinline__ float fast_inverse_rms(float S, float Df, float inv_d
   return __fmaf_rn(__fmul_rn(0.5f, y0), e, y0);
 }
 
+// Outside [2^-100, 2^100] the fp32 sum is not a usable statistic: a square
+// overflowed (S = +inf, though the row's mean may be finite: one element of
+// 3e19), the row holds infinities, or its squares fell below fp32's normal
+// range.  The kernels then sum the row's squares again, of x * fast_rescale(S)
+// (2^-64 for a large S, 2^64 for a small one), and take r from
+// fast_inverse_rms_scaled.  NaN counts as in range: it propagates, as in the
+// definition.  The branch is uniform over a row's threads, which hold the
+// same S.
+__device__ __forceinline__ bool fast_sum_in_range(float S) {
+  return !(S < 0x1p-100f) && !(S > 0x1p100f);
+}
+__device__ __forceinline__ float fast_rescale(float S) { return S > 1.0f ? 0x1p-64f : 0x1p64f; }
+
+// 1 / sqrt(v) for any v >= 0 (rsqrtf and one Newton step on v scaled by an
+// even power of two into rsqrtf's range): +0 -> +inf, +inf -> 0, NaN -> NaN.
+__device__ __forceinline__ float fast_rsqrt(float v) {
+  float w = v, back = 1.0f;
+  if (v < 0x1p-100f) {
+    w = __fmul_rn(v, 0x1p100f);
+    back = 0x1p50f;
+  } else if (v > 0x1p100f) {
+    w = __fmul_rn(v, 0x1p-100f);
+    back = 0x1p-50f;
+  }
+  if (w == 0.0f) return __int_as_float(0x7f800000);
+  if (w == __int_as_float(0x7f800000)) return 0.0f;
+  const float y0 = rsqrtf(w);
+  const float e = __fmaf_rn(__fmul_rn(-w, y0), y0, 1.0f);
+  return __fmul_rn(__fmaf_rn(__fmul_rn(0.5f, y0), e, y0), back);
+}
+
+// r from S2, the row's sum of (x * scale)^2 (scale from fast_rescale): the
+// mean of the scaled squares, scaled back by 1 / scale^2 = 2^(+-128) in two
+// exact steps of 2^64 (the second may overflow to +inf -- then r = 0, as
+// when the exact mean rounds past fp32's range -- or round into the
+// subnormal range), then v = fl(ms + eps) and r = 1 / sqrt(v).  S2 = +inf
+// (an infinity in the row) gives r = 0, NaN gives NaN.
+__device__ __forceinline__ float fast_inverse_rms_scaled(float S2, float scale, float Df,
+                                                         float inv_d, float eps) {
+  // an infinity in the row: ms = +inf, r = 0 (the remainder step would
+  // turn inf - inf into NaN)
+  if (S2 == __int_as_float(0x7f800000)) return 0.0f;
+  const float q = __fmul_rn(S2, inv_d);
+  const float mss = __fmaf_rn(__fmaf_rn(-q, Df, S2), inv_d, q);
+  const float step = scale < 1.0f ? 0x1p64f : 0x1p-64f;
+  const float ms = __fmul_rn(__fmul_rn(mss, step), step);
+  return fast_rsqrt(__fadd_rn(ms, eps));
+}
+
 // `each` is taken by value (and should capture by value): only the exact
 // path, a separate function, needs the row's elements in memory.
 template <class Each, class Row>
+// r of one row from its merged pair: the fast decision, else the exact path.
+// Uniform over the row's threads (they hold the same pair).
 __device__ __forceinline__ float row_inverse_rms(SumPair p, float coef, int levels, int64_t D,
                                                  float Df, float eps, const Each& each, Row row) {
   float ms;

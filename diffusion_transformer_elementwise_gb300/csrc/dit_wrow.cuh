@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
   extern __shared__ float4 vsm[];  // [NV][NPL][ngr] vectors, then [W][NS][NG * 32] stages
   __shared__ SumPair xch_pair[2][kWrowWarps / 2][2];  // the team's pair exchange, by row parity
   __shared__ uint64_t xch_exact[kWrowWarps / 2][2];
+  __shared__ float xch_scaled[kWrowWarps / 2][2];  // the fast statistic's rescaled sums
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int team = warp >> 1, m = warp & 1;
   const int nteams = blockDim.x >> 6;
@@ -377,7 +378,31 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
         asm volatile("bar.sync %0, 64;" ::"r"(1 + team) : "memory");
         // both warps add the two halves in the same order
         const float S = __fadd_rn(xch_pair[par][team][0].h, xch_pair[par][team][1].h);
-        r = fast_inverse_rms(S, a.d_f, a.inv_d, a.eps);
+        if (fast_sum_in_range(S)) {
+          r = fast_inverse_rms(S, a.d_f, a.inv_d, a.eps);
+        } else {
+          // rare (both warps of the team): the squares of the row scaled
+          const float sc = fast_rescale(S);
+          float s2 = 0.0f;
+#pragma unroll
+          for (int j = 0; j < NG; ++j) {
+            if (!val[j]) continue;
+            F2 x[P];
+            G::widen(xr[j], x);
+            if (edge(j)) mask_part<T>(x, lo_of(j), hi_of(j));
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+              const float u0 = __fmul_rn(f2_lo(x[i]), sc), u1 = __fmul_rn(f2_hi(x[i]), sc);
+              s2 = __fmaf_rn(u1, u1, __fmaf_rn(u0, u0, s2));
+            }
+          }
+          s2 = warp_sum(s2);
+          if (lane == 0) xch_scaled[team][m] = s2;
+          asm volatile("bar.sync %0, 64;" ::"r"(1 + team) : "memory");
+          const float S2 = __fadd_rn(xch_scaled[team][0], xch_scaled[team][1]);
+          asm volatile("bar.sync %0, 64;" ::"r"(1 + team) : "memory");  // read before reuse
+          r = fast_inverse_rms_scaled(S2, sc, a.d_f, a.inv_d, a.eps);
+        }
       }
       par ^= 1;
       const F2 r2 = f2(r, r);

@@ -1,6 +1,8 @@
-"""GPU parity of the phased staged kernel: rows whose byte pitch is not a
+"""GPU parity of the phased kernels: rows whose byte pitch is not a
 multiple of 16 (odd D, D = 2 mod 4 ...) in tensors that start on 16-byte
-boundaries.  Every offset period (2, 4 and 8 rows), fewer rows than the
+boundaries -- the staged CTA-per-row kernel (the residual gate, the exact
+statistic, full scale/shift, rows above 8 KB) and the two-warp kernel (the
+modulating ops with the fast statistic and [B,1,D] operands).  Every offset period (2, 4 and 8 rows), fewer rows than the
 period, more rows than the grid (each CTA takes rows of one offset), batches
 changing inside a CTA's run, rows shorter than a granule, the last row's
 granule that runs past the tensors' end, rows too long for one CTA (column

@@ -164,3 +164,46 @@ def test_fast_statistic_on_rounding_boundaries(orc, case):
         torch.cuda.synchronize()
     ref, t = oracle_mod(orc, x, sc, sh, dtype, "bcast", 0.0, with_t=True)
     modulation_stats(out, ref, t.numpy(), dtype, f"fast {case}", exact=False)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("D", [4096, 3077, 20000])
+def test_fast_statistic_outside_its_range(orc, dtype, D):
+    """The fast statistic on rows whose fp32 sum of squares leaves
+    [2^-100, 2^100]: a square that overflows (3e19, 2^64: the mean stays
+    finite), rows of +inf or holding one, a mean near 2^120, squares near
+    2^-120 and squares that round to zero.  The kernels sum such rows again
+    scaled by 2^-64 or 2^64; every element must meet the fast criterion,
+    NaN exactly where the oracle has NaN.  (A mean square in fp32's
+    subnormal range with eps = 0 is left out: there the fast statistic may
+    be one subnormal step of ms off, which the fp32 criterion does not
+    allow.)"""
+    B, L = 1, 8
+    rng = np.random.default_rng(D + 1)
+    rows = rng.standard_normal((L, D))
+    rows[0, 5] = 3e19
+    rows[1, :] = np.inf
+    rows[2, 7] = 2.0 ** 64
+    rows[2, 8] = -(2.0 ** 64)
+    rows[3] *= 2.0 ** -60   # squares near 2^-120: the sum below 2^-100
+    rows[4] *= 2.0 ** -80   # squares round to zero
+    rows[5] *= 2.0 ** 60    # mean near 2^120
+    rows[6, 0] = np.inf
+    x = torch.tensor(rows[None], dtype=torch.float64).to(TORCH_DTYPES[dtype])
+    sc = torch.tensor(rng.normal(0, 0.1, (B, 1, D))).to(x.dtype)
+    sh = torch.tensor(rng.normal(0, 0.1, (B, 1, D))).to(x.dtype)
+    with dit.statistic("fast"):
+        for eps in (0.0, 1e-6):
+            out = dit.rmsnorm_modulate(x.cuda(), sc.cuda(), sh.cuda(), eps)
+            u = torch.zeros_like(x)
+            g = torch.zeros((B, 1, D), dtype=x.dtype)
+            res, mod = dit.gate_add_rmsnorm_modulate(x.cuda(), u.cuda(), g.cuda(), sc.cuda(),
+                                                     sh.cuda(), eps)
+            torch.cuda.synchronize()
+            ref, t = oracle_mod(orc, x, sc, sh, dtype, "bcast", eps, with_t=True)
+            modulation_stats(out, ref, t.numpy(), dtype, f"fast D={D} eps={eps}", exact=False)
+            modulation_stats(mod, ref, t.numpy(), dtype, f"fast fused D={D} eps={eps}",
+                             exact=False)
+            o = out.cpu().float()
+            assert torch.isfinite(o[0, 0]).all() and torch.isfinite(o[0, 2]).all()
+            assert torch.isnan(o[0, 1]).all()
