@@ -499,37 +499,40 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int64_t cta, c
         }
         const float rl = fast_inverse_rms(tot, a.d_f, a.inv_d, a.eps);
 #pragma unroll
-        for (int j = 0; j < RC; ++j) {
-          rr[j] = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
-          // rare: row j's sum outside the fast range (uniform over the CTA:
-          // every warp summed the same partials) -- its squares again, scaled
-          const float totj = RC == 1 ? tot : __shfl_sync(0xFFFFFFFFu, tot, j);
-          if ((CHECK && row0 + j >= rend) || fast_sum_in_range(totj)) continue;
-          const float sc = fast_rescale(totj);
-          float s2 = 0.0f;
-          const uint32_t sl0 = stage + j * JS + kX * OS;
+        for (int j = 0; j < RC; ++j) rr[j] = RC == 1 ? rl : __shfl_sync(0xFFFFFFFFu, rl, j);
+        // rare: a row's sum outside the fast range (uniform over the CTA:
+        // every warp summed the same partials) -- its squares again, scaled
+        if (__any_sync(0xFFFFFFFFu, !fast_sum_in_range(tot))) {
 #pragma unroll
-          for (int k = 0; k < VPT; ++k) {
-            if (!cval[k]) continue;
-            F2 x[P];
-            G::widen(lds16(sl0 + k * KS), x);
-            if constexpr (PH) {
-              const uint32_t bk = (bounds >> (8 * k)) & 255u;
-              if (bk != (uint32_t)EPG << 4) mask_part<T>(x, (int)(bk & 15u), (int)(bk >> 4));
-            }
+          for (int j = 0; j < RC; ++j) {
+            const float totj = RC == 1 ? tot : __shfl_sync(0xFFFFFFFFu, tot, j);
+            if ((CHECK && row0 + j >= rend) || fast_sum_in_range(totj)) continue;
+            const float sc = fast_rescale(totj);
+            float s2 = 0.0f;
+            const uint32_t sl0 = stage + j * JS + kX * OS;
 #pragma unroll
-            for (int i = 0; i < P; ++i) {
-              const float u0 = __fmul_rn(f2_lo(x[i]), sc), u1 = __fmul_rn(f2_hi(x[i]), sc);
-              s2 = __fmaf_rn(u1, u1, __fmaf_rn(u0, u0, s2));
+            for (int k = 0; k < VPT; ++k) {
+              if (!cval[k]) continue;
+              F2 x[P];
+              G::widen(lds16(sl0 + k * KS), x);
+              if constexpr (PH) {
+                const uint32_t bk = (bounds >> (8 * k)) & 255u;
+                if (bk != (uint32_t)EPG << 4) mask_part<T>(x, (int)(bk & 15u), (int)(bk >> 4));
+              }
+#pragma unroll
+              for (int i = 0; i < P; ++i) {
+                const float u0 = __fmul_rn(f2_lo(x[i]), sc), u1 = __fmul_rn(f2_hi(x[i]), sc);
+                s2 = __fmaf_rn(u1, u1, __fmaf_rn(u0, u0, s2));
+              }
             }
+            s2 = warp_sum(s2);
+            if (lane == 0) part_scaled[warp] = s2;
+            __syncthreads();
+            float S2 = 0.0f;
+            for (int w = 0; w < nwarps; ++w) S2 = __fadd_rn(S2, part_scaled[w]);
+            __syncthreads();  // read before the next row's writes
+            rr[j] = fast_inverse_rms_scaled(S2, sc, a.d_f, a.inv_d, a.eps);
           }
-          s2 = warp_sum(s2);
-          if (lane == 0) part_scaled[warp] = s2;
-          __syncthreads();
-          float S2 = 0.0f;
-          for (int w = 0; w < nwarps; ++w) S2 = __fadd_rn(S2, part_scaled[w]);
-          __syncthreads();  // read before the next row's writes
-          rr[j] = fast_inverse_rms_scaled(S2, sc, a.d_f, a.inv_d, a.eps);
         }
       } else {
         // row pairs: merged over the warp, then over the warps (lane l of
