@@ -29,14 +29,15 @@
 // contiguous bytes (no bank conflicts).
 //
 // Schedule.  On large tensors (more than 8 rows per team in one wave of
-// CTAs) a CTA gives each of its teams a few rows (four for the modulation,
+// CTAs) a CTA gives each of its teams a few rows (three for the modulation,
 // two for the fused op) of one batch, and the grid holds as many CTAs as that
 // takes -- several waves, handed to the SMs by the hardware as earlier CTAs
 // finish.  A one-wave persistent grid, each CTA striding over the tensor,
 // left SMs idle at the end there: the SMs do not stream at the same rate,
 // and a static split of the rows made the slowest SM set the kernel's length
 // (on [1,32640,4096] bf16 the modulation took 98 us back to back with it, 86
-// us with four rows per team; the fused op 182 and 160 us with two).  Smaller
+// us with four rows per team, 84 with three -- 1, 2, 6 and 8 were slower, as
+// were 12-warp CTAs; the fused op 182 and 160 us with two).  Smaller
 // tensors run exactly one wave with the rows split statically: there a
 // second, partial wave of short CTAs costs more than the imbalance
 // ([1,8160,4096]: 510 CTAs of four rows per team, 1.1 waves, ran the
@@ -508,7 +509,7 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
         // than teams: one row per team), the rows split statically
         per_batch = std::min(most, (wave + B - 1) / B);
       } else {
-        const int64_t rows_per_team = OP == OP_FUSED ? 2 : 4;
+        const int64_t rows_per_team = OP == OP_FUSED ? 2 : 3;
         per_batch = (a.L + teams * rows_per_team - 1) / (teams * rows_per_team);
       }
       per_batch = (per_batch + period - 1) / period * period;  // whole phase classes
