@@ -108,11 +108,16 @@ const char* dit_status_string(dit_status status);
  *   DIT_STATISTIC_FAST (default): the row's fp32 sum of squares, one FMA per
  *     element, merged in tree order; ms = S / D by a corrected quotient;
  *     r = rsqrtf(fl(ms + eps)) refined by one Newton-Raphson step.  r is
- *     within about ten fp32 ulps of the exact statistic's, so each output
- *     element is within one bf16/fp16 ulp of the exact definition's except
- *     where the final + shift cancels (|y| much smaller than
+ *     within about seventeen fp32 ulps of the exact statistic's, so each
+ *     output element is within one bf16/fp16 ulp of the exact definition's
+ *     except where the final + shift cancels (|y| much smaller than
  *     |x r (1 + scale)|), where the difference stays below one dtype ulp of
- *     max(|t|, |y|), t = n (1 + scale).
+ *     max(|t|, |y|), t = n (1 + scale); fp32 outputs within 2^-18 of
+ *     max(|t|, |y|).  A row whose fp32 sum leaves [2^-100, 2^100] (a square
+ *     that overflows fp32, infinities, squares below its normal range) is
+ *     summed again with its elements scaled by 2^-64 or 2^64; a mean square
+ *     in fp32's subnormal range with eps = 0 may then be one subnormal step
+ *     off.
  *   DIT_STATISTIC_EXACT: ms = RN32(mean(x^2)), the exact mean of the row's
  *     squares rounded once to fp32, and r = RN32(1 / sqrt(fl(ms + eps))),
  *     correctly rounded: every output element equals the definition
@@ -120,15 +125,18 @@ const char* dit_status_string(dit_status status);
  *     whatever kernel or launch shape computes it.  The squares are summed in
  *     compensated (TwoSum) pairs with a proven error bound and the rounding
  *     decided from it; rows the bound cannot decide (ties and near-ties) are
- *     summed exactly.  It costs up to about a quarter of the modulation's
- *     throughput (the compensated sum makes it compute-bound).
+ *     summed exactly.  It costs time: on [1,32640,4096] bf16 the modulation
+ *     takes about a third longer and the fused op an eighth (the compensated
+ *     sum makes them issue-bound).
  *
  * Sources: the statistic is fp32 and the result is held to one bf16 ulp per
  * element (prhub summary of sglang PR #34172, "implementation breakdown"
  * item 2 and risks item 1).
  *
- * The mode is read when a call is made (host side); set it before launching,
- * not concurrently with calls from other threads.  dit_set_statistic returns
+ * The mode is read when a call is made (host side) and selects the kernel
+ * it launches -- a CUDA graph keeps the statistic its captured calls were
+ * made with; set it before launching, not concurrently with calls from other
+ * threads.  dit_set_statistic returns
  * DIT_ERR_BAD_STATISTIC for other values and leaves the mode unchanged.
  */
 typedef enum {
