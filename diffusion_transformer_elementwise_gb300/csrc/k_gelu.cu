@@ -21,8 +21,9 @@
 // expf and an IEEE division, each operation rounded to nearest.
 //
 // The tensor is walked as one flat array: a grid-stride loop of 32-byte (or
-// narrower) vector accesses, two vectors in flight per thread; a scalar head
-// when input and output share a misalignment; a scalar tail.
+// narrower) vector accesses, two vectors in flight per thread, over a grid of
+// two vectors per thread; a scalar head when input and output share a
+// misalignment; a scalar tail.
 #include "dit_device.cuh"
 #include "dit_internal.h"
 
@@ -155,11 +156,13 @@ cudaError_t launch_gelu(const DeviceInfo& dev, int dtype, void* out, const void*
   return dispatch_dtype_width(dtype, vb, [&](auto tt, auto w) -> cudaError_t {
     using T = typename decltype(tt)::type;
     constexpr int VB = decltype(w)::value;
-    const void* fn = (const void*)gelu_flat_kernel<T, VB>;
     const int block = 256;
-    int64_t grid = (a.n_vec + block - 1) / block;
-    const int64_t wave = (int64_t)dev.sm_count * resident_ctas(dev, fn, block);
-    if (grid > wave) grid = wave;
+    // two vectors per thread (one pass of the loop): short CTAs handed to the
+    // SMs by the hardware, as for the full-gate residual gate (a one-wave
+    // grid left SMs idle at the end); the loop covers what a grid of at most
+    // 2^30 CTAs does not
+    int64_t grid = (a.n_vec + 2 * block - 1) / (2 * block);
+    if (grid > (int64_t(1) << 30)) grid = int64_t(1) << 30;
     const int64_t edge = (a.n_head + a.n_tail + block - 1) / block;
     if (grid < edge) grid = edge;
     if (grid < 1) grid = 1;
