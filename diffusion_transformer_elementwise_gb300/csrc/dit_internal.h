@@ -56,6 +56,10 @@ struct RowArgs {
   int64_t step_b;     // G / gpb
   int64_t step_g;     // G % gpb
   const float* qscale;  // E4M3 output: the per-tensor quantisation scale (device)
+  // two-warp kernel: the first `head` CTAs of a batch stride over its rows
+  // [0, head_rows); the others take one row per team of the rest
+  int64_t head;
+  int64_t head_rows;
 };
 
 struct DeviceInfo {

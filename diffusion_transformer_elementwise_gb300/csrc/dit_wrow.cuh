@@ -32,8 +32,12 @@
 // CTAs) a CTA gives each of its teams a few rows (three for the modulation,
 // two for the fused op) of one batch, and the grid holds as many CTAs as that
 // takes -- several waves, handed to the SMs by the hardware as earlier CTAs
-// finish.  A one-wave persistent grid, each CTA striding over the tensor,
-// left SMs idle at the end there: the SMs do not stream at the same rate,
+// finish.  With the fast statistic the last wave of each batch's CTAs takes
+// one row per team: an SM whose last long CTA ends early picks these up, so
+// the SMs finish within about one row of each other instead of three (ncu,
+// modulation of [1,32640,4096] bf16: active cycles per SM 146k-166k without
+// the tail, 148k-156k with it).  A one-wave persistent grid, each CTA
+// striding over the tensor, left SMs idle at the end there: the SMs do not stream at the same rate,
 // and a static split of the rows made the slowest SM set the kernel's length
 // (on [1,32640,4096] bf16 the modulation took 98 us back to back with it, 86
 // us with four rows per team, 84 with three -- 1, 2, 6 and 8 were slower, as
@@ -41,10 +45,13 @@
 // tensors run exactly one wave with the rows split statically: there a
 // second, partial wave of short CTAs costs more than the imbalance
 // ([1,8160,4096]: 510 CTAs of four rows per team, 1.1 waves, ran the
-// modulation in 35.7 us L2-flushed).  CTA k of a batch's CTAs gives its team t rows k * T + t, then
-// + (CTAs per batch) * T, ... (T teams per CTA).  The grid is capped at 64
-// waves; with more batches than that a CTA takes batches c, c + grid, ...,
-// reloading the vectors (two barriers) between them.
+// modulation in 35.7 us L2-flushed).  Of a batch's CTAs the first H (the
+// head) give their team t rows k * T + t, k * T + t + H * T, ... of the
+// batch's first head_rows rows (T teams per CTA; without a tail H is all of
+// them and head_rows the whole batch); tail CTA k gives team t the one row
+// head_rows + (k - H) * T + t.  The grid is capped at 64 waves; with more
+// batches than that a CTA takes batches c, c + grid, ..., reloading the
+// vectors (two barriers) between them, and there is no tail.
 #pragma once
 
 #include <algorithm>
@@ -211,9 +218,24 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
     auto lo_of = [&](int j) { return j == 0 && first ? lo_first : 0; };
     auto hi_of = [&](int j) { return j == last_j ? hi_last : EPG; };
 
+    // this team's rows of the batch: l, l + lstep, ... below lend -- a head
+    // CTA strides over rows [0, head_rows), a tail CTA takes one row of the
+    // rest (phased rows: the CTA's phase class, over the whole batch)
+    int64_t l, lend = a.L, lstep = rstep;
+    if constexpr (PH) {
+      l = phase + period * (kq * nteams + team);
+    } else if (kc < a.head) {
+      l = kc * nteams + team;
+      lend = a.head_rows;
+      lstep = a.head * nteams;
+    } else {
+      l = a.head_rows + (kc - a.head) * nteams + team;
+      lstep = a.L;
+    }
+
     // copy this warp's half of row l into the stage (an empty group past the end)
     auto prefetch = [&](int64_t l) {
-      if (l < a.L) {
+      if (l < lend) {
         const int64_t row = b * a.L + l;
         const int64_t rowoff = row * pitch - off + lg * 16;
         // phased rows: the last row's last granule may run past the end
@@ -236,7 +258,6 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
       cp_async_commit();
     };
 
-    int64_t l = PH ? phase + period * (kq * nteams + team) : kc * nteams + team;
     prefetch(l);  // in flight while the vectors load
     if constexpr (NV > 0) {
       __syncthreads();  // the previous batch's vectors are no longer read
@@ -282,7 +303,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
       __syncthreads();
     }
 
-    for (; l < a.L; l += rstep) {
+    for (; l < lend; l += lstep) {
       const int64_t row = b * a.L + l;
       const int64_t rowoff = row * pitch - off + lg * 16;
       cp_async_wait<0>();  // this lane's copies of row l have landed
@@ -314,7 +335,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
           else
             st_stream<16>(res + j * 1024, xr[j]);
         }
-        prefetch(l + rstep);  // the stage has been read
+        prefetch(l + lstep);  // the stage has been read
       } else {
 #pragma unroll
         for (int j = 0; j < NG; ++j)
@@ -335,7 +356,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
 #pragma unroll
           for (int i = 0; i < P; ++i) acc.add_pair((j % R) * P + i, x[i]);
         }
-        if constexpr (OP != OP_FUSED) prefetch(l + rstep);
+        if constexpr (OP != OP_FUSED) prefetch(l + lstep);
         SumPair p = warp_merge(acc.total());
         // the other warp of the row: exchange through shared memory (one
         // slot pair per row parity, so a slot is rewritten only after the
@@ -373,7 +394,7 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
 #pragma unroll
           for (int i = 0; i < P; ++i) acc.add_pair_fast((j % R) * P + i, x[i]);
         }
-        if constexpr (OP != OP_FUSED) prefetch(l + rstep);
+        if constexpr (OP != OP_FUSED) prefetch(l + lstep);
         const float ws = warp_sum(acc.fast_total());
         if (lane == 0) xch_pair[par][team][m] = SumPair{ws, 0.0f};
         asm volatile("bar.sync %0, 64;" ::"r"(1 + team) : "memory");
@@ -453,6 +474,12 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
 // slower than the CTA-per-row kernel on [1,4096,4608] bf16.
 constexpr int kWrowMaxNG = 8;
 
+// Tenths of a wave of one-row-per-team CTAs that end each batch's CTAs on
+// large tensors.  [1,32640,4096] bf16 back to back, modulation: none 84.3 us,
+// half a wave 82.0, one wave 82.2, one and a half 82.3, two and a half 82.7;
+// the fused op 158.9 against 157.8-158.2 (0.5 to 1.2 waves).
+constexpr int kWrowTaper = 10;
+
 // Launch the two-warps-per-row kernel; cudaErrorNotSupported when the row
 // does not fit it (more than 64 * kWrowMaxNG granules, or the stages and the
 // vectors do not fit shared memory) -- the caller then takes the CTA-per-row
@@ -500,6 +527,8 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       const int64_t most = (a.L + teams - 1) / teams;  // CTAs per batch, one row per team
       int64_t per_batch;
       const bool small = B * a.L <= 8 * wave * teams;
+      // all CTAs stride over the whole batch, unless tapered below
+      int64_t head = -1, head_rows = a.L;
       // the fused op takes this kernel on large tensors only: on smaller ones
       // the CTA-per-row kernel, with three CTAs per SM to its two, was faster
       // ([1,4608,3072] bf16, L2-flushed: 25.3 vs 27.1 us)
@@ -511,6 +540,18 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       } else {
         const int64_t rows_per_team = OP == OP_FUSED ? 2 : 3;
         per_batch = (a.L + teams * rows_per_team - 1) / (teams * rows_per_team);
+        if (!phased && !EX) {
+          // tapered: the last kWrowTaper / 10 waves of CTAs (over all
+          // batches) take one row per team, so the SMs finish together.  Not
+          // under the exact statistic, whose kernels are issue-bound rather
+          // than held up by the tail (the hot-path step's exact modulation
+          // 112.2 us with the tail, 112.3 without)
+          const int64_t tail_ctas = (kWrowTaper * wave / 10 + B - 1) / B;  // per batch
+          const int64_t tail_rows = std::min(a.L, tail_ctas * teams);
+          head_rows = a.L - tail_rows;
+          head = (head_rows + teams * rows_per_team - 1) / (teams * rows_per_team);
+          per_batch = head + (tail_rows + teams - 1) / teams;
+        }
       }
       per_batch = (per_batch + period - 1) / period * period;  // whole phase classes
       int64_t G = B * per_batch;
@@ -521,6 +562,9 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       if (cpb < period) cpb = period;
       a.gpb = cpb;
       a.ngroups = nb;
+      const bool tapered = head >= 0 && nb == B && cpb == per_batch;
+      a.head = tapered ? head : cpb;
+      a.head_rows = tapered ? head_rows : a.L;
       const int64_t grid = nb * cpb;
       if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
       kern<<<(unsigned)grid, block, smem, stream>>>(a);

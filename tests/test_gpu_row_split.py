@@ -110,3 +110,60 @@ def test_row_blocks_equal_one_call(orc, statistic, case, world):
                 modulation_stats(split[k].cpu(), r, t.numpy(), dtype, what)
             else:
                 _same(split[k], whole[k], what)
+
+
+
+# Large tensors: the two-warp kernel's tapered schedule (CTAs of several rows
+# per team, then a last wave of one row per team, in every batch) against the
+# same rows called in blocks small enough for its one-wave schedule.  The
+# modulation runs the same kernel instantiation either way (same granules per
+# lane), whose per-row arithmetic does not depend on which team takes the
+# row, so its bits must agree under either statistic.  The fused op takes the
+# CTA-per-row kernel on small blocks, so there its residual (exact
+# arithmetic) is compared bit for bit, its modulated output bitwise under the
+# exact statistic and against the oracle on sampled rows of every batch under
+# the fast one.  NaN-filled outputs show any element left unwritten.
+# Ragged L, several batches, two and four granules per lane.
+LARGE = [(1, 60013, 1024, "bf16"), (3, 20011, 1024, "bf16"), (2, 30001, 1024, "fp32")]
+
+
+@pytest.mark.parametrize("case", LARGE, ids=lambda c: "x".join(map(str, c)))
+def test_large_tensor_schedule_equals_blocks(orc, statistic, case):
+    B, L, D, dtype = case
+    from diffusion_transformer_elementwise_gb300.synth import draw, seed_for
+    h = draw("act", (B, L, D), seed_for("large", "h", *case), dtype, "cuda")
+    u = draw("act", (B, L, D), seed_for("large", "u", *case), dtype, "cuda")
+    g = draw("gate", (B, 1, D), seed_for("large", "g", *case), dtype, "cuda")
+    sc = draw("mod", (B, 1, D), seed_for("large", "sc", *case), dtype, "cuda")
+    sh = draw("mod", (B, 1, D), seed_for("large", "sh", *case), dtype, "cuda")
+    block = 2048  # rows per call: far below one wave's eight rows per team
+    calls = {
+        "mod": (1, lambda hs, us, gs, scs, shs, o: dit.rmsnorm_modulate(hs, scs, shs, EPS,
+                                                                       out=o[0])),
+        "fused": (2, lambda hs, us, gs, scs, shs, o: dit.gate_add_rmsnorm_modulate(
+            hs, us, gs, scs, shs, EPS, residual_out=o[0], modulated_out=o[1])),
+    }
+    for name, (nout, call) in calls.items():
+        whole = [torch.full_like(h, float("nan")) for _ in range(nout)]
+        parts = [torch.full_like(h, float("nan")) for _ in range(nout)]
+        call(h, u, g, sc, sh, whole)
+        for b in range(B):
+            for s in range(0, L, block):
+                e = min(L, s + block)
+                call(h[b:b + 1, s:e], u[b:b + 1, s:e], g[b:b + 1], sc[b:b + 1], sh[b:b + 1],
+                     [o[b:b + 1, s:e] for o in parts])
+        torch.cuda.synchronize()
+        for k in range(nout):
+            what = f"{name} output {k} {case}"
+            assert not torch.isnan(whole[k]).any(), what + ": unwritten elements"
+            if name == "fused" and k == 1 and statistic == "fast":
+                idx = torch.tensor(sorted({0, L - 1, *np.random.default_rng(
+                    seed_for("large rows", *case) & 0xFFFFFFFF).choice(L, 254, replace=False)
+                    .tolist()}))
+                d = idx.cuda()
+                rows = [t[:, d].contiguous().cpu() for t in (h, u)]
+                _, ref, t = oracle_fused(orc, *rows, g.cpu(), sc.cpu(), sh.cpu(), dtype,
+                                         "bcast", "bcast", EPS, with_t=True, threads=8)
+                modulation_stats(whole[k][:, d].contiguous().cpu(), ref, t.numpy(), dtype, what)
+            else:
+                _same(whole[k], parts[k], what)
