@@ -53,13 +53,13 @@ struct RowArgs {
   // straddling a batch; CTA c takes groups c, c + G, c + 2G, ...
   int64_t gpb;        // groups per batch
   int64_t ngroups;    // B * gpb
+  // (the two-warp kernel: step_b = `head`, the first CTAs of a batch, which
+  // stride over its rows [0, step_g); the others take one row per team of
+  // the rest.  Reused rather than added: a larger struct made the grouped
+  // kernel, which holds eight of them, 3.7% slower)
   int64_t step_b;     // G / gpb
   int64_t step_g;     // G % gpb
   const float* qscale;  // E4M3 output: the per-tensor quantisation scale (device)
-  // two-warp kernel: the first `head` CTAs of a batch stride over its rows
-  // [0, head_rows); the others take one row per team of the rest
-  int64_t head;
-  int64_t head_rows;
 };
 
 struct DeviceInfo {

@@ -219,17 +219,18 @@ __global__ void __launch_bounds__(kWrowWarps * 32, wrow_min_blocks<OP, NG>()) wr
     auto hi_of = [&](int j) { return j == last_j ? hi_last : EPG; };
 
     // this team's rows of the batch: l, l + lstep, ... below lend -- a head
-    // CTA strides over rows [0, head_rows), a tail CTA takes one row of the
-    // rest (phased rows: the CTA's phase class, over the whole batch)
+    // CTA (kc < a.step_b) strides over rows [0, a.step_g), a tail CTA takes
+    // one row of the rest (phased rows: the CTA's phase class, over the
+    // whole batch)
     int64_t l, lend = a.L, lstep = rstep;
     if constexpr (PH) {
       l = phase + period * (kq * nteams + team);
-    } else if (kc < a.head) {
+    } else if (kc < a.step_b) {
       l = kc * nteams + team;
-      lend = a.head_rows;
-      lstep = a.head * nteams;
+      lend = a.step_g;
+      lstep = a.step_b * nteams;
     } else {
-      l = a.head_rows + (kc - a.head) * nteams + team;
+      l = a.step_g + (kc - a.step_b) * nteams + team;
       lstep = a.L;
     }
 
@@ -563,8 +564,8 @@ cudaError_t launch_wrow(const DeviceInfo& dev, int dtype, RowArgs a, int64_t B,
       a.gpb = cpb;
       a.ngroups = nb;
       const bool tapered = head >= 0 && nb == B && cpb == per_batch;
-      a.head = tapered ? head : cpb;
-      a.head_rows = tapered ? head_rows : a.L;
+      a.step_b = tapered ? head : cpb;
+      a.step_g = tapered ? head_rows : a.L;
       const int64_t grid = nb * cpb;
       if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
       kern<<<(unsigned)grid, block, smem, stream>>>(a);
